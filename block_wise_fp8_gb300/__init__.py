@@ -1,0 +1,254 @@
+"""Block-wise FP8 W8A8 linear for GB300: Python binding of the C ABI (include/fp8bq.h).
+
+Every function here has the name of the C entry point it calls and does
+argument marshalling only: torch tensors become device pointers and sizes, the
+current CUDA stream becomes the `stream` argument, and a non-zero status
+becomes an :class:`Fp8bqError`.  All computation runs in the CUDA library
+``_build/libfp8bq.so`` (build it with ``__graft_entry__.build()``); importing
+this package without that library raises ImportError -- there is no fallback.
+
+Tensor conventions: BF16 tensors are ``torch.bfloat16``; E4M3 codes are
+``torch.float8_e4m3fn`` or ``torch.uint8``; FP32 scales ``torch.float32``;
+UE8M0 scale codes ``torch.uint8``.  Matrices are row-major with unit stride in
+the last dimension.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import _build
+
+__all__ = [
+    "Fp8bqError", "SCALE_ROW_MAJOR", "SCALE_COL_MAJOR", "OP_GEMM", "OP_LINEAR",
+    "OP_MX_GEMM", "OP_MX_LINEAR", "OP_STATIC_GEMM", "OP_STATIC_LINEAR", "library_path",
+    "fp8bq_version", "fp8bq_status_string", "fp8bq_last_cuda_error",
+    "fp8bq_workspace_bytes", "fp8bq_workspace_init", "fp8bq_poll_status",
+    "fp8bq_quant_act", "fp8bq_gemm", "fp8bq_linear", "fp8bq_mx_quant_act",
+    "fp8bq_mx_gemm", "fp8bq_mx_linear", "fp8bq_static_quant_act", "fp8bq_static_gemm",
+    "fp8bq_static_linear", "fp8bq_quant_weight_block", "fp8bq_absmax_scale",
+    "new_workspace",
+]
+
+SCALE_ROW_MAJOR, SCALE_COL_MAJOR = 0, 1
+(OP_GEMM, OP_LINEAR, OP_MX_GEMM, OP_MX_LINEAR, OP_STATIC_GEMM,
+ OP_STATIC_LINEAR) = range(6)
+
+STATUS_NAMES = {0: "FP8BQ_OK", 1: "FP8BQ_ERR_NULL", 2: "FP8BQ_ERR_SHAPE",
+                3: "FP8BQ_ERR_ALIGN", 4: "FP8BQ_ERR_UNSUPPORTED", 5: "FP8BQ_ERR_ARCH",
+                6: "FP8BQ_ERR_WORKSPACE", 7: "FP8BQ_ERR_CUDA", 8: "FP8BQ_ERR_TIMEOUT"}
+
+
+class Fp8bqError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        self.name = STATUS_NAMES.get(status, str(status))
+        msg = f"{what}: {self.name} ({_lib.fp8bq_status_string(status).decode()})"
+        if status == 7:
+            msg += f", cudaError {_lib.fp8bq_last_cuda_error()}"
+        super().__init__(msg)
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def _load():
+    if not os.path.exists(_build.LIB):
+        raise ImportError(
+            f"CUDA library {_build.LIB} is not built; run __graft_entry__.build() "
+            "(there is no CPU fallback)")
+    lib = ctypes.CDLL(_build.LIB)
+    P, I64, I32, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+    sigs = {
+        "fp8bq_version": (I32, []),
+        "fp8bq_status_string": (ctypes.c_char_p, [I32]),
+        "fp8bq_last_cuda_error": (I32, []),
+        "fp8bq_workspace_bytes": (SZ, [I32, I64, I64, I64]),
+        "fp8bq_workspace_init": (I32, [P, SZ, P]),
+        "fp8bq_poll_status": (I32, [P, P]),
+        "fp8bq_quant_act": (I32, [P, I64, I64, I64, P, P, I32, P]),
+        "fp8bq_gemm": (I32, [P, P, I32, P, P, P, P, I64, I64, I64, P, SZ, P]),
+        "fp8bq_linear": (I32, [P, I64, P, P, P, P, I64, I64, I64, P, SZ, P]),
+        "fp8bq_mx_quant_act": (I32, [P, I64, I64, I64, P, P, P]),
+        "fp8bq_mx_gemm": (I32, [P, P, P, P, P, P, I64, I64, I64, P, SZ, P]),
+        "fp8bq_mx_linear": (I32, [P, I64, P, P, P, P, I64, I64, I64, P, SZ, P]),
+        "fp8bq_static_quant_act": (I32, [P, I64, I64, I64, P, P, P]),
+        "fp8bq_static_gemm": (I32, [P, P, P, P, P, I32, P, P, I64, I64, I64, P, SZ, P]),
+        "fp8bq_static_linear": (I32, [P, I64, P, P, P, P, I32, P, P, I64, I64, I64, P, SZ,
+                                      P]),
+        "fp8bq_quant_weight_block": (I32, [P, I64, I64, I64, P, P, P]),
+        "fp8bq_absmax_scale": (I32, [P, I64, I64, I64, P, P]),
+    }
+    for name, (res, args) in sigs.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+_lib = _load()
+
+
+# ---------------------------------------------------------------- marshalling
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return ctypes.c_void_p(t)
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ld(x) -> int:
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("expected a 2-D tensor with unit stride in the last dimension")
+    return x.stride(0)
+
+
+def _nbytes(t) -> int:
+    return t.numel() * t.element_size()
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        raise Fp8bqError(status, what)
+
+
+# ---------------------------------------------------------------- utility
+
+def fp8bq_version() -> int:
+    return _lib.fp8bq_version()
+
+
+def fp8bq_status_string(status: int) -> str:
+    return _lib.fp8bq_status_string(status).decode()
+
+
+def fp8bq_last_cuda_error() -> int:
+    return _lib.fp8bq_last_cuda_error()
+
+
+def fp8bq_workspace_bytes(op: int, M: int, N: int, K: int) -> int:
+    return _lib.fp8bq_workspace_bytes(op, M, N, K)
+
+
+def fp8bq_workspace_init(ws, stream=None):
+    _check(_lib.fp8bq_workspace_init(_ptr(ws), _nbytes(ws), _stream(stream)),
+           "fp8bq_workspace_init")
+
+
+def fp8bq_poll_status(ws, stream=None) -> int:
+    """Synchronises the stream; returns 0, or 8 (FP8BQ_ERR_TIMEOUT)."""
+    return _lib.fp8bq_poll_status(_ptr(ws), _stream(stream))
+
+
+def new_workspace(op: int, M: int, N: int, K: int, device="cuda", stream=None):
+    """A zero-initialised workspace (torch-owned device memory) for `op` at this shape."""
+    ws = torch.empty(fp8bq_workspace_bytes(op, M, N, K), dtype=torch.uint8, device=device)
+    fp8bq_workspace_init(ws, stream)
+    return ws
+
+
+# ---------------------------------------------------------------- block path
+
+def fp8bq_quant_act(x, q, s, s_layout: int = SCALE_ROW_MAJOR, stream=None):
+    M, K = x.shape
+    _check(_lib.fp8bq_quant_act(_ptr(x), M, K, _ld(x), _ptr(q), _ptr(s), s_layout,
+                                _stream(stream)), "fp8bq_quant_act")
+
+
+def fp8bq_gemm(q, s_x, w, s_w, y, ws, bias=None, s_layout: int = SCALE_ROW_MAJOR,
+               stream=None):
+    M, K = q.shape
+    N = w.shape[0]
+    _check(_lib.fp8bq_gemm(_ptr(q), _ptr(s_x), s_layout, _ptr(w), _ptr(s_w), _ptr(bias),
+                           _ptr(y), M, N, K, _ptr(ws), _nbytes(ws), _stream(stream)),
+           "fp8bq_gemm")
+
+
+def fp8bq_linear(x, w, s_w, y, ws, bias=None, stream=None):
+    M, K = x.shape
+    N = w.shape[0]
+    _check(_lib.fp8bq_linear(_ptr(x), _ld(x), _ptr(w), _ptr(s_w), _ptr(bias), _ptr(y),
+                             M, N, K, _ptr(ws), _nbytes(ws), _stream(stream)),
+           "fp8bq_linear")
+
+
+# ---------------------------------------------------------------- MX path
+
+def fp8bq_mx_quant_act(x, q, s, stream=None):
+    M, K = x.shape
+    _check(_lib.fp8bq_mx_quant_act(_ptr(x), M, K, _ld(x), _ptr(q), _ptr(s),
+                                   _stream(stream)), "fp8bq_mx_quant_act")
+
+
+def fp8bq_mx_gemm(q, s_x, w, s_w, y, ws, bias=None, stream=None):
+    M, K = q.shape
+    N = w.shape[0]
+    _check(_lib.fp8bq_mx_gemm(_ptr(q), _ptr(s_x), _ptr(w), _ptr(s_w), _ptr(bias), _ptr(y),
+                              M, N, K, _ptr(ws), _nbytes(ws), _stream(stream)),
+           "fp8bq_mx_gemm")
+
+
+def fp8bq_mx_linear(x, w, s_w, y, ws, bias=None, stream=None):
+    M, K = x.shape
+    N = w.shape[0]
+    _check(_lib.fp8bq_mx_linear(_ptr(x), _ld(x), _ptr(w), _ptr(s_w), _ptr(bias), _ptr(y),
+                                M, N, K, _ptr(ws), _nbytes(ws), _stream(stream)),
+           "fp8bq_mx_linear")
+
+
+# ---------------------------------------------------------------- static path
+
+def _parts(part_sizes):
+    arr = (ctypes.c_int64 * len(part_sizes))(*[int(p) for p in part_sizes])
+    return arr, len(part_sizes)
+
+
+def fp8bq_static_quant_act(x, s_x, q, stream=None):
+    M, K = x.shape
+    _check(_lib.fp8bq_static_quant_act(_ptr(x), M, K, _ld(x), _ptr(s_x), _ptr(q),
+                                       _stream(stream)), "fp8bq_static_quant_act")
+
+
+def fp8bq_static_gemm(q, s_x, w, s_w_part, part_sizes, y, ws, bias=None, stream=None):
+    M, K = q.shape
+    N = w.shape[0]
+    arr, n = _parts(part_sizes)
+    _check(_lib.fp8bq_static_gemm(_ptr(q), _ptr(s_x), _ptr(w), _ptr(s_w_part), arr, n,
+                                  _ptr(bias), _ptr(y), M, N, K, _ptr(ws), _nbytes(ws),
+                                  _stream(stream)), "fp8bq_static_gemm")
+
+
+def fp8bq_static_linear(x, s_x, w, s_w_part, part_sizes, y, ws, bias=None, stream=None):
+    M, K = x.shape
+    N = w.shape[0]
+    arr, n = _parts(part_sizes)
+    _check(_lib.fp8bq_static_linear(_ptr(x), _ld(x), _ptr(s_x), _ptr(w), _ptr(s_w_part),
+                                    arr, n, _ptr(bias), _ptr(y), M, N, K, _ptr(ws),
+                                    _nbytes(ws), _stream(stream)), "fp8bq_static_linear")
+
+
+# ---------------------------------------------------------------- set-up helpers
+
+def fp8bq_quant_weight_block(w, q, s_w, stream=None):
+    N, K = w.shape
+    _check(_lib.fp8bq_quant_weight_block(_ptr(w), N, K, _ld(w), _ptr(q), _ptr(s_w),
+                                         _stream(stream)), "fp8bq_quant_weight_block")
+
+
+def fp8bq_absmax_scale(x, s, stream=None):
+    rows, K = x.shape
+    _check(_lib.fp8bq_absmax_scale(_ptr(x), rows, K, _ld(x), _ptr(s), _stream(stream)),
+           "fp8bq_absmax_scale")

@@ -1,0 +1,107 @@
+// common.cuh -- shared definitions of the CUDA library (host and device).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+namespace fp8bq {
+
+constexpr int kBlockK = 128;  // K width of one scale block / one pipeline stage
+constexpr int kBlockN = 128;  // rows of W sharing one weight scale
+constexpr int kMxGroup = 32;  // K elements per UE8M0 scale
+constexpr int kMaxParts = 64; // static path: maximum number of output partitions
+
+// Status values stored in the workspace status word (same numbers as fp8bq_status).
+constexpr uint32_t kStatusTimeout = 8;
+
+// ---------------------------------------------------------------- quant kernels
+
+void launch_quant_group(const void *x, int64_t M, int64_t K, int64_t ldx, void *q, float *s,
+                        int s_layout, cudaStream_t st);
+void launch_quant_mx(const void *x, int64_t M, int64_t K, int64_t ldx, void *q, uint8_t *s,
+                     cudaStream_t st);
+void launch_quant_static(const void *x, int64_t M, int64_t K, int64_t ldx, const float *s,
+                         void *q, cudaStream_t st);
+void launch_quant_weight_block(const void *w, int64_t N, int64_t K, int64_t ldw, void *q,
+                               float *s, cudaStream_t st);
+void launch_absmax_scale(const void *x, int64_t rows, int64_t K, int64_t ldx, float *s,
+                         int num_sms, cudaStream_t st);
+
+// ---------------------------------------------------------------- GEMM
+
+enum GemmMode : int { kModeBlock = 0, kModeTensor = 1, kModeMx = 2 };
+
+// Everything a GEMM launch needs besides the two tensor maps.
+struct GemmArgs {
+  int mode;
+  int M, N, K;
+  // block path
+  const float *sx;
+  int sx_layout;  // 0 row-major [M][KB], 1 column-major [KB][ldsx]
+  int ldsx;       // KB for row-major, round_up(M,4) for column-major
+  const float *sw;
+  // static path
+  const float *sx_scalar;
+  const float *sw_part;
+  int n_parts;
+  int part_end[kMaxParts];
+  // MX path
+  const uint8_t *ux;
+  const uint8_t *uw;
+  // epilogue
+  const void *bias;
+  void *y;
+  // workspace
+  uint32_t *status;
+  uint32_t *counters;
+  float *partials;
+  uint64_t wait_limit_ns;
+};
+
+struct DeviceInfo {
+  int num_sms;
+  int cc_major, cc_minor;
+  size_t max_smem_optin;
+};
+
+// Workspace layout (byte offsets), shared by the host entry points.
+struct WorkspaceLayout {
+  size_t status, counters, partials, q, s, total;
+};
+WorkspaceLayout workspace_layout(int op, int64_t M, int64_t N, int64_t K);
+
+// Work decomposition of one GEMM launch.
+struct LaunchShape {
+  int units;        // work units (output tiles, times splits in the swapped form)
+  int num_a_tiles;  // 128-row tiles of the A operand
+  int splits;       // K splits per tile (swapped form only)
+  int kps;          // K blocks per split
+  int KB;           // ceil(K / 128)
+  int sx_stage;     // floats of shared memory staging s_x (swapped block form)
+};
+
+// K-major E4M3 matrix [rows, K] (pitch K bytes) as a TMA map with a
+// [box_rows x 128 B] box and 128-byte swizzling.
+bool make_kmajor_map(CUtensorMap *m, const void *base, int64_t rows, int64_t K, int box_rows);
+
+// Kernel variants, one translation unit each (instantiated from gemm_kernel.cuh).
+// `bn` selects the token tile of the swapped (decode) form: 16, 32 or 64.
+cudaError_t run_block_normal(const GemmArgs &a, const void *q, const void *w,
+                             const LaunchShape &sh, int grid, cudaStream_t st, int *status);
+cudaError_t run_block_swap(int bn, const GemmArgs &a, const void *q, const void *w,
+                           const LaunchShape &sh, int grid, cudaStream_t st, int *status);
+cudaError_t run_tensor_normal(const GemmArgs &a, const void *q, const void *w,
+                              const LaunchShape &sh, int grid, cudaStream_t st, int *status);
+cudaError_t run_tensor_swap(int bn, const GemmArgs &a, const void *q, const void *w,
+                            const LaunchShape &sh, int grid, cudaStream_t st, int *status);
+cudaError_t run_mx_normal(const GemmArgs &a, const void *q, const void *w,
+                          const LaunchShape &sh, int grid, cudaStream_t st, int *status);
+
+// Chooses the kernel variant for the shape and launches it.  Returns 0 or an
+// fp8bq status; a CUDA error is returned through `cuda_err`.
+int launch_gemm(const GemmArgs &a, const void *q_act, const void *w, const DeviceInfo &dev,
+                cudaStream_t st, cudaError_t *cuda_err);
+
+}  // namespace fp8bq

@@ -1,0 +1,446 @@
+// fp8bq_api.cu -- the C ABI (include/fp8bq.h): host-side validation, per-device
+// attribute cache, workspace bookkeeping and kernel launches.  Nothing here
+// computes on the host; every step of the path runs in the kernels of quant.cu
+// and gemm_*.cu.
+#include <cuda_runtime.h>
+
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/fp8bq.h"
+#include "common.cuh"
+
+using namespace fp8bq;
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+constexpr int kMaxDevices = 64;
+struct DevSlot {
+  std::once_flag once;
+  DeviceInfo info;
+  cudaError_t err;
+};
+DevSlot g_dev[kMaxDevices];
+
+uint64_t wait_limit_ns() {
+  static uint64_t v = [] {
+    uint64_t ms = 1000;
+    if (const char *e = std::getenv("FP8BQ_WAIT_LIMIT_MS")) {
+      char *end = nullptr;
+      unsigned long long x = std::strtoull(e, &end, 10);
+      if (end != e && x > 0) ms = x;
+    }
+    return ms * 1000000ull;
+  }();
+  return v;
+}
+
+int cuda_fail(cudaError_t e) {
+  g_last_cuda_error = static_cast<int>(e);
+  return FP8BQ_ERR_CUDA;
+}
+
+// Current device must be compute capability 10.3 (GB300).
+int device_info(DeviceInfo *out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kMaxDevices) return FP8BQ_ERR_ARCH;
+  DevSlot &s = g_dev[dev];
+  std::call_once(s.once, [&] {
+    s.err = cudaSuccess;
+    int v = 0;
+    cudaError_t r;
+    if ((r = cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) s.err = r;
+    s.info.num_sms = v;
+    if ((r = cudaDeviceGetAttribute(&v, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess) s.err = r;
+    s.info.cc_major = v;
+    if ((r = cudaDeviceGetAttribute(&v, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess) s.err = r;
+    s.info.cc_minor = v;
+    if ((r = cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess) s.err = r;
+    s.info.max_smem_optin = static_cast<size_t>(v);
+  });
+  if (s.err != cudaSuccess) return cuda_fail(s.err);
+  if (s.info.cc_major != 10 || s.info.cc_minor != 3) return FP8BQ_ERR_ARCH;
+  *out = s.info;
+  return FP8BQ_OK;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// Common checks for an activation matrix [M, K] with pitch ldx.
+int check_act(const void *x, int64_t M, int64_t K, int64_t ldx, int kmod) {
+  if (!x) return FP8BQ_ERR_NULL;
+  if (M < 0 || K < 1 || ldx < K || M > (int64_t(1) << 31) - 1 || K > (int64_t(1) << 30))
+    return FP8BQ_ERR_SHAPE;
+  if (!aligned(x, 16) || (ldx % 8) != 0 || (K % kmod) != 0) return FP8BQ_ERR_ALIGN;
+  return FP8BQ_OK;
+}
+
+int check_gemm_shape(int64_t M, int64_t N, int64_t K, int kmod) {
+  if (M < 0 || N < 1 || K < 1) return FP8BQ_ERR_SHAPE;
+  if (M > (int64_t(1) << 31) - 1 || N > (int64_t(1) << 31) - 1 || K > (int64_t(1) << 30))
+    return FP8BQ_ERR_SHAPE;
+  if (K % kmod) return FP8BQ_ERR_ALIGN;
+  return FP8BQ_OK;
+}
+
+int check_ws(void *ws, size_t ws_bytes, int op, int64_t M, int64_t N, int64_t K) {
+  if (!ws) return FP8BQ_ERR_WORKSPACE;
+  if (!aligned(ws, 256)) return FP8BQ_ERR_ALIGN;
+  if (ws_bytes < workspace_layout(op, M, N, K).total) return FP8BQ_ERR_WORKSPACE;
+  return FP8BQ_OK;
+}
+
+GemmArgs base_args(int mode, int64_t M, int64_t N, int64_t K, const void *bias, void *y,
+                   void *ws, int op) {
+  GemmArgs a;
+  std::memset(&a, 0, sizeof a);
+  a.mode = mode;
+  a.M = static_cast<int>(M);
+  a.N = static_cast<int>(N);
+  a.K = static_cast<int>(K);
+  a.bias = bias;
+  a.y = y;
+  const WorkspaceLayout L = workspace_layout(op, M, N, K);
+  uint8_t *w = static_cast<uint8_t *>(ws);
+  a.status = reinterpret_cast<uint32_t *>(w + L.status);
+  a.counters = reinterpret_cast<uint32_t *>(w + L.counters);
+  a.partials = reinterpret_cast<float *>(w + L.partials);
+  a.wait_limit_ns = wait_limit_ns();
+  return a;
+}
+
+int finish_launch(int st, cudaError_t e) {
+  if (st != 0) return st;
+  if (e != cudaSuccess) return cuda_fail(e);
+  return FP8BQ_OK;
+}
+
+#define RETURN_IF(x)            \
+  do {                          \
+    int _r = (x);               \
+    if (_r != FP8BQ_OK) return _r; \
+  } while (0)
+
+// ------------------------------------------------------------------ shared bodies
+
+int gemm_block_impl(const void *q, const float *s_x, int s_layout, const void *w,
+                    const float *s_w, const void *bias, void *y, int64_t M, int64_t N, int64_t K,
+                    void *ws, int op, cudaStream_t st, const DeviceInfo &dev) {
+  GemmArgs a = base_args(kModeBlock, M, N, K, bias, y, ws, op);
+  a.sx = s_x;
+  a.sx_layout = s_layout;
+  a.ldsx = s_layout == FP8BQ_SCALE_ROW_MAJOR ? static_cast<int>((K + 127) / 128)
+                                             : static_cast<int>((M + 3) / 4 * 4);
+  a.sw = s_w;
+  cudaError_t e;
+  int r = launch_gemm(a, q, w, dev, st, &e);
+  return finish_launch(r, e);
+}
+
+int gemm_mx_impl(const void *q, const uint8_t *s_x, const void *w, const uint8_t *s_w,
+                 const void *bias, void *y, int64_t M, int64_t N, int64_t K, void *ws, int op,
+                 cudaStream_t st, const DeviceInfo &dev) {
+  GemmArgs a = base_args(kModeMx, M, N, K, bias, y, ws, op);
+  a.ux = s_x;
+  a.uw = s_w;
+  cudaError_t e;
+  int r = launch_gemm(a, q, w, dev, st, &e);
+  return finish_launch(r, e);
+}
+
+int gemm_static_impl(const void *q, const float *s_x, const void *w, const float *s_w_part,
+                     const int64_t *parts, int n_parts, const void *bias, void *y, int64_t M,
+                     int64_t N, int64_t K, void *ws, int op, cudaStream_t st,
+                     const DeviceInfo &dev) {
+  GemmArgs a = base_args(kModeTensor, M, N, K, bias, y, ws, op);
+  a.sx_scalar = s_x;
+  a.sw_part = s_w_part;
+  a.n_parts = n_parts;
+  int64_t end = 0;
+  for (int p = 0; p < n_parts; ++p) {
+    end += parts[p];
+    a.part_end[p] = static_cast<int>(end);
+  }
+  cudaError_t e;
+  int r = launch_gemm(a, q, w, dev, st, &e);
+  return finish_launch(r, e);
+}
+
+// An empty batch (M == 0) launches nothing; only the other extents are checked
+// and pointers may be NULL.
+int empty_batch(int64_t K, int64_t N) { return (K >= 1 && N >= 1) ? FP8BQ_OK : FP8BQ_ERR_SHAPE; }
+
+int check_parts(const int64_t *parts, int n_parts, int64_t N) {
+  if (!parts) return FP8BQ_ERR_NULL;
+  if (n_parts < 1 || n_parts > kMaxParts) return FP8BQ_ERR_SHAPE;
+  int64_t sum = 0;
+  for (int p = 0; p < n_parts; ++p) {
+    if (parts[p] < 1) return FP8BQ_ERR_SHAPE;
+    sum += parts[p];
+  }
+  return sum == N ? FP8BQ_OK : FP8BQ_ERR_SHAPE;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fp8bq_version(void) { return 10000; }
+
+const char *fp8bq_status_string(int s) {
+  switch (s) {
+    case FP8BQ_OK: return "ok";
+    case FP8BQ_ERR_NULL: return "a required pointer is NULL";
+    case FP8BQ_ERR_SHAPE: return "invalid shape";
+    case FP8BQ_ERR_ALIGN: return "pointer or pitch misaligned";
+    case FP8BQ_ERR_UNSUPPORTED: return "unsupported argument";
+    case FP8BQ_ERR_ARCH: return "device is not compute capability 10.3";
+    case FP8BQ_ERR_WORKSPACE: return "workspace missing or too small";
+    case FP8BQ_ERR_CUDA: return "CUDA runtime error";
+    case FP8BQ_ERR_TIMEOUT: return "a device-side wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int fp8bq_last_cuda_error(void) { return g_last_cuda_error; }
+
+size_t fp8bq_workspace_bytes(int op, int64_t M, int64_t N, int64_t K) {
+  if (op < FP8BQ_OP_GEMM || op > FP8BQ_OP_STATIC_LINEAR || M < 0 || N < 1 || K < 1) return 256;
+  return workspace_layout(op, M, N, K).total;
+}
+
+int fp8bq_workspace_init(void *ws, size_t ws_bytes, void *stream) {
+  if (!ws) return FP8BQ_ERR_NULL;
+  if (!aligned(ws, 256)) return FP8BQ_ERR_ALIGN;
+  cudaError_t e = cudaMemsetAsync(ws, 0, ws_bytes, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FP8BQ_OK : cuda_fail(e);
+}
+
+int fp8bq_poll_status(void *ws, void *stream) {
+  if (!ws) return FP8BQ_ERR_NULL;
+  if (!aligned(ws, 256)) return FP8BQ_ERR_ALIGN;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t word = 0;
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e);
+  e = cudaMemcpy(&word, ws, sizeof word, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (word != 0) {
+    e = cudaMemset(ws, 0, sizeof word);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return FP8BQ_ERR_TIMEOUT;
+  }
+  return FP8BQ_OK;
+}
+
+// ------------------------------------------------------------------ block path
+
+int fp8bq_quant_act(const void *x, int64_t M, int64_t K, int64_t ldx, void *q, float *s,
+                    int s_layout, void *stream) {
+  if (M == 0) return empty_batch(K, 1);
+  if (!q || !s) return FP8BQ_ERR_NULL;
+  RETURN_IF(check_act(x, M, K, ldx, 16));
+  if (s_layout != FP8BQ_SCALE_ROW_MAJOR && s_layout != FP8BQ_SCALE_COL_MAJOR)
+    return FP8BQ_ERR_UNSUPPORTED;
+  if (!aligned(q, 16) || !aligned(s, 4)) return FP8BQ_ERR_ALIGN;
+  if (M == 0) return FP8BQ_OK;
+  DeviceInfo dev;
+  RETURN_IF(device_info(&dev));
+  launch_quant_group(x, M, K, ldx, q, s, s_layout, static_cast<cudaStream_t>(stream));
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? FP8BQ_OK : cuda_fail(e);
+}
+
+int fp8bq_gemm(const void *q, const float *s_x, int s_layout, const void *w, const float *s_w,
+               const void *bias, void *y, int64_t M, int64_t N, int64_t K, void *ws,
+               size_t ws_bytes, void *stream) {
+  if (M == 0) return empty_batch(K, N);
+  if (!q || !s_x || !w || !s_w || !y) return FP8BQ_ERR_NULL;
+  RETURN_IF(check_gemm_shape(M, N, K, 16));
+  if (s_layout != FP8BQ_SCALE_ROW_MAJOR && s_layout != FP8BQ_SCALE_COL_MAJOR)
+    return FP8BQ_ERR_UNSUPPORTED;
+  if (!aligned(q, 16) || !aligned(w, 16) || !aligned(y, 16) || !aligned(s_x, 4) ||
+      !aligned(s_w, 4) || !aligned(bias, 2))
+    return FP8BQ_ERR_ALIGN;
+  RETURN_IF(check_ws(ws, ws_bytes, FP8BQ_OP_GEMM, M, N, K));
+  if (M == 0) return FP8BQ_OK;
+  DeviceInfo dev;
+  RETURN_IF(device_info(&dev));
+  return gemm_block_impl(q, s_x, s_layout, w, s_w, bias, y, M, N, K, ws, FP8BQ_OP_GEMM,
+                         static_cast<cudaStream_t>(stream), dev);
+}
+
+int fp8bq_linear(const void *x, int64_t ldx, const void *w, const float *s_w, const void *bias,
+                 void *y, int64_t M, int64_t N, int64_t K, void *ws, size_t ws_bytes,
+                 void *stream) {
+  if (M == 0) return empty_batch(K, N);
+  if (!w || !s_w || !y) return FP8BQ_ERR_NULL;
+  RETURN_IF(check_act(x, M, K, ldx, 16));
+  RETURN_IF(check_gemm_shape(M, N, K, 16));
+  if (!aligned(w, 16) || !aligned(y, 16) || !aligned(s_w, 4) || !aligned(bias, 2))
+    return FP8BQ_ERR_ALIGN;
+  RETURN_IF(check_ws(ws, ws_bytes, FP8BQ_OP_LINEAR, M, N, K));
+  if (M == 0) return FP8BQ_OK;
+  DeviceInfo dev;
+  RETURN_IF(device_info(&dev));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const WorkspaceLayout L = workspace_layout(FP8BQ_OP_LINEAR, M, N, K);
+  uint8_t *q = static_cast<uint8_t *>(ws) + L.q;
+  float *s = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + L.s);
+  // column-major scales: per K block the 128 rows of a tile are contiguous
+  launch_quant_group(x, M, K, ldx, q, s, FP8BQ_SCALE_COL_MAJOR, st);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e);
+  return gemm_block_impl(q, s, FP8BQ_SCALE_COL_MAJOR, w, s_w, bias, y, M, N, K, ws,
+                         FP8BQ_OP_LINEAR, st, dev);
+}
+
+// ------------------------------------------------------------------ MX path
+
+int fp8bq_mx_quant_act(const void *x, int64_t M, int64_t K, int64_t ldx, void *q, uint8_t *s,
+                       void *stream) {
+  if (M == 0) return empty_batch(K, 1);
+  if (!q || !s) return FP8BQ_ERR_NULL;
+  RETURN_IF(check_act(x, M, K, ldx, 32));
+  if (!aligned(q, 16)) return FP8BQ_ERR_ALIGN;
+  if (M == 0) return FP8BQ_OK;
+  DeviceInfo dev;
+  RETURN_IF(device_info(&dev));
+  launch_quant_mx(x, M, K, ldx, q, s, static_cast<cudaStream_t>(stream));
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? FP8BQ_OK : cuda_fail(e);
+}
+
+int fp8bq_mx_gemm(const void *q, const uint8_t *s_x, const void *w, const uint8_t *s_w,
+                  const void *bias, void *y, int64_t M, int64_t N, int64_t K, void *ws,
+                  size_t ws_bytes, void *stream) {
+  if (M == 0) return empty_batch(K, N);
+  if (!q || !s_x || !w || !s_w || !y) return FP8BQ_ERR_NULL;
+  RETURN_IF(check_gemm_shape(M, N, K, 32));
+  if (!aligned(q, 16) || !aligned(w, 16) || !aligned(y, 16) || !aligned(bias, 2))
+    return FP8BQ_ERR_ALIGN;
+  RETURN_IF(check_ws(ws, ws_bytes, FP8BQ_OP_MX_GEMM, M, N, K));
+  if (M == 0) return FP8BQ_OK;
+  DeviceInfo dev;
+  RETURN_IF(device_info(&dev));
+  return gemm_mx_impl(q, s_x, w, s_w, bias, y, M, N, K, ws, FP8BQ_OP_MX_GEMM,
+                      static_cast<cudaStream_t>(stream), dev);
+}
+
+int fp8bq_mx_linear(const void *x, int64_t ldx, const void *w, const uint8_t *s_w,
+                    const void *bias, void *y, int64_t M, int64_t N, int64_t K, void *ws,
+                    size_t ws_bytes, void *stream) {
+  if (M == 0) return empty_batch(K, N);
+  if (!w || !s_w || !y) return FP8BQ_ERR_NULL;
+  RETURN_IF(check_act(x, M, K, ldx, 32));
+  RETURN_IF(check_gemm_shape(M, N, K, 32));
+  if (!aligned(w, 16) || !aligned(y, 16) || !aligned(bias, 2)) return FP8BQ_ERR_ALIGN;
+  RETURN_IF(check_ws(ws, ws_bytes, FP8BQ_OP_MX_LINEAR, M, N, K));
+  if (M == 0) return FP8BQ_OK;
+  DeviceInfo dev;
+  RETURN_IF(device_info(&dev));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const WorkspaceLayout L = workspace_layout(FP8BQ_OP_MX_LINEAR, M, N, K);
+  uint8_t *q = static_cast<uint8_t *>(ws) + L.q;
+  uint8_t *s = static_cast<uint8_t *>(ws) + L.s;
+  launch_quant_mx(x, M, K, ldx, q, s, st);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e);
+  return gemm_mx_impl(q, s, w, s_w, bias, y, M, N, K, ws, FP8BQ_OP_MX_LINEAR, st, dev);
+}
+
+// ------------------------------------------------------------------ static path
+
+int fp8bq_static_quant_act(const void *x, int64_t M, int64_t K, int64_t ldx, const float *s_x,
+                           void *q, void *stream) {
+  if (M == 0) return empty_batch(K, 1);
+  if (!q || !s_x) return FP8BQ_ERR_NULL;
+  RETURN_IF(check_act(x, M, K, ldx, 16));
+  if (!aligned(q, 16) || !aligned(s_x, 4)) return FP8BQ_ERR_ALIGN;
+  if (M == 0) return FP8BQ_OK;
+  DeviceInfo dev;
+  RETURN_IF(device_info(&dev));
+  launch_quant_static(x, M, K, ldx, s_x, q, static_cast<cudaStream_t>(stream));
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? FP8BQ_OK : cuda_fail(e);
+}
+
+int fp8bq_static_gemm(const void *q, const float *s_x, const void *w, const float *s_w_part,
+                      const int64_t *part_sizes_host, int n_parts, const void *bias, void *y,
+                      int64_t M, int64_t N, int64_t K, void *ws, size_t ws_bytes, void *stream) {
+  if (M == 0) return empty_batch(K, N);
+  if (!q || !s_x || !w || !s_w_part || !y) return FP8BQ_ERR_NULL;
+  RETURN_IF(check_gemm_shape(M, N, K, 16));
+  RETURN_IF(check_parts(part_sizes_host, n_parts, N));
+  if (!aligned(q, 16) || !aligned(w, 16) || !aligned(y, 16) || !aligned(s_x, 4) ||
+      !aligned(s_w_part, 4) || !aligned(bias, 2))
+    return FP8BQ_ERR_ALIGN;
+  RETURN_IF(check_ws(ws, ws_bytes, FP8BQ_OP_STATIC_GEMM, M, N, K));
+  if (M == 0) return FP8BQ_OK;
+  DeviceInfo dev;
+  RETURN_IF(device_info(&dev));
+  return gemm_static_impl(q, s_x, w, s_w_part, part_sizes_host, n_parts, bias, y, M, N, K, ws,
+                          FP8BQ_OP_STATIC_GEMM, static_cast<cudaStream_t>(stream), dev);
+}
+
+int fp8bq_static_linear(const void *x, int64_t ldx, const float *s_x, const void *w,
+                        const float *s_w_part, const int64_t *part_sizes_host, int n_parts,
+                        const void *bias, void *y, int64_t M, int64_t N, int64_t K, void *ws,
+                        size_t ws_bytes, void *stream) {
+  if (M == 0) return empty_batch(K, N);
+  if (!s_x || !w || !s_w_part || !y) return FP8BQ_ERR_NULL;
+  RETURN_IF(check_act(x, M, K, ldx, 16));
+  RETURN_IF(check_gemm_shape(M, N, K, 16));
+  RETURN_IF(check_parts(part_sizes_host, n_parts, N));
+  if (!aligned(w, 16) || !aligned(y, 16) || !aligned(s_x, 4) || !aligned(s_w_part, 4) ||
+      !aligned(bias, 2))
+    return FP8BQ_ERR_ALIGN;
+  RETURN_IF(check_ws(ws, ws_bytes, FP8BQ_OP_STATIC_LINEAR, M, N, K));
+  if (M == 0) return FP8BQ_OK;
+  DeviceInfo dev;
+  RETURN_IF(device_info(&dev));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const WorkspaceLayout L = workspace_layout(FP8BQ_OP_STATIC_LINEAR, M, N, K);
+  uint8_t *q = static_cast<uint8_t *>(ws) + L.q;
+  launch_quant_static(x, M, K, ldx, s_x, q, st);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e);
+  return gemm_static_impl(q, s_x, w, s_w_part, part_sizes_host, n_parts, bias, y, M, N, K, ws,
+                          FP8BQ_OP_STATIC_LINEAR, st, dev);
+}
+
+// ------------------------------------------------------------------ set-up helpers
+
+int fp8bq_quant_weight_block(const void *w, int64_t N, int64_t K, int64_t ldw, void *q,
+                             float *s_w, void *stream) {
+  if (!q || !s_w) return FP8BQ_ERR_NULL;
+  RETURN_IF(check_act(w, N, K, ldw, 16));
+  if (N < 1) return FP8BQ_ERR_SHAPE;
+  if (!aligned(q, 16) || !aligned(s_w, 4)) return FP8BQ_ERR_ALIGN;
+  if ((N + 127) / 128 > 65535) return FP8BQ_ERR_SHAPE;
+  DeviceInfo dev;
+  RETURN_IF(device_info(&dev));
+  launch_quant_weight_block(w, N, K, ldw, q, s_w, static_cast<cudaStream_t>(stream));
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? FP8BQ_OK : cuda_fail(e);
+}
+
+int fp8bq_absmax_scale(const void *x, int64_t rows, int64_t K, int64_t ldx, float *s,
+                       void *stream) {
+  if (!s) return FP8BQ_ERR_NULL;
+  RETURN_IF(check_act(x, rows, K, ldx, 16));
+  if (rows < 1) return FP8BQ_ERR_SHAPE;
+  if (!aligned(s, 4)) return FP8BQ_ERR_ALIGN;
+  DeviceInfo dev;
+  RETURN_IF(device_info(&dev));
+  launch_absmax_scale(x, rows, K, ldx, s, dev.num_sms, static_cast<cudaStream_t>(stream));
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? FP8BQ_OK : cuda_fail(e);
+}
+
+}  // extern "C"

@@ -1,0 +1,113 @@
+// gemm_launch.cu -- host side of the GEMMs: TMA tensor maps, workspace layout
+// and the choice of kernel variant and work decomposition for a shape.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+
+namespace fp8bq {
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+constexpr int kMaxSplits = 8;
+
+}  // namespace
+
+bool make_kmajor_map(CUtensorMap *m, const void *base, int64_t rows, int64_t K, int box_rows) {
+  auto enc = get_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(K)};
+  cuuint32_t box[2] = {128u, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// [status word | split-K tile counters | split-K FP32 partials | fused: Q | fused: scales]
+WorkspaceLayout workspace_layout(int op, int64_t M, int64_t N, int64_t K) {
+  auto up = [](size_t v) { return (v + 255) / 256 * 256; };
+  WorkspaceLayout L{};
+  const int64_t KB = (K + 127) / 128;
+  const int64_t NT = (N + 127) / 128;
+  L.status = 0;
+  L.counters = 256;
+  size_t off = L.counters + up(static_cast<size_t>(NT) * 4);
+  L.partials = off;
+  const bool mx = (op == 2 || op == 3);
+  if (M <= 64 && !mx) off += up(static_cast<size_t>(kMaxSplits) * M * N * 4);
+  L.q = off;
+  const bool fused = (op == 1 || op == 3 || op == 5);
+  if (fused) off += up(static_cast<size_t>(M) * K);
+  L.s = off;
+  if (op == 1) off += up(static_cast<size_t>(KB) * ((M + 3) / 4 * 4) * 4);
+  if (op == 3) off += up(static_cast<size_t>(M) * (K / 32));
+  L.total = off;
+  return L;
+}
+
+int launch_gemm(const GemmArgs &a, const void *q_act, const void *w, const DeviceInfo &dev,
+                cudaStream_t st, cudaError_t *cuda_err) {
+  *cuda_err = cudaSuccess;
+  int status = 0;
+  LaunchShape sh{};
+  sh.KB = (a.K + 127) / 128;
+  const bool swap = (a.mode != kModeMx) && a.M <= 64;
+  if (swap) {
+    // decode: weight rows on the MMA's M side, tokens on its N side, K split so
+    // that tiles x splits fills the SMs; partials reduced by the last CTA
+    const int tiles = (a.N + 127) / 128;
+    int splits = dev.num_sms / tiles;
+    if (splits < 1) splits = 1;
+    if (splits > kMaxSplits) splits = kMaxSplits;
+    if (splits > sh.KB) splits = sh.KB;
+    int kps = (sh.KB + splits - 1) / splits;
+    while (kps > 64 && splits < kMaxSplits) {  // bounds the s_x staging buffer
+      ++splits;
+      kps = (sh.KB + splits - 1) / splits;
+    }
+    if (kps > 64) return 4;  // FP8BQ_ERR_UNSUPPORTED: K too large for the decode tile
+    splits = (sh.KB + kps - 1) / kps;  // no empty split
+    sh.splits = splits;
+    sh.kps = kps;
+    sh.num_a_tiles = tiles;
+    sh.units = tiles * splits;
+    const int bn = a.M <= 16 ? 16 : a.M <= 32 ? 32 : 64;
+    sh.sx_stage = (a.mode == kModeBlock) ? bn * kps : 0;
+    *cuda_err = (a.mode == kModeBlock)
+                    ? run_block_swap(bn, a, q_act, w, sh, sh.units, st, &status)
+                    : run_tensor_swap(bn, a, q_act, w, sh, sh.units, st, &status);
+    return status;
+  }
+  // prefill: persistent CTAs over (M tiles x N tiles), M fastest
+  const int bn = (a.mode == kModeMx) ? 128 : 256;
+  sh.num_a_tiles = (a.M + 127) / 128;
+  const int n_tiles = (a.N + bn - 1) / bn;
+  sh.splits = 1;
+  sh.kps = sh.KB;
+  sh.units = sh.num_a_tiles * n_tiles;
+  sh.sx_stage = 0;
+  const int grid = sh.units < dev.num_sms ? sh.units : dev.num_sms;
+  if (a.mode == kModeBlock) *cuda_err = run_block_normal(a, q_act, w, sh, grid, st, &status);
+  else if (a.mode == kModeTensor) *cuda_err = run_tensor_normal(a, q_act, w, sh, grid, st, &status);
+  else *cuda_err = run_mx_normal(a, q_act, w, sh, grid, st, &status);
+  return status;
+}
+
+}  // namespace fp8bq

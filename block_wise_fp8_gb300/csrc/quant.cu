@@ -1,0 +1,287 @@
+// quant.cu -- activation / weight quantisation kernels (HBM-streaming).
+//
+// Every kernel reads BF16 with 16-byte vector loads, reduces |x| with warp
+// shuffles inside its group, and converts with the hardware's saturating
+// round-to-nearest-even FP32 -> E4M3 conversion.  Scales and quotients are
+// IEEE binary32 divisions (__fdiv_rn), so codes and scales are bit-identical
+// to the definitions on the pages ("SGLang 源码完全拆解(十九)", §从浮点到 FP8 的
+// 基本公式; "GLM-5.3 推理全链路(十七)", §第1站, s_g = max|x|/448, q = round(x/s_g)).
+#include <cuda_fp8.h>
+
+#include "common.cuh"
+
+namespace fp8bq {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr float kFloor = 1e-10f;  // amax floor (the pages' E8M0 rule; avoids 0/0)
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ void unpack16(const uint4 (&v)[2], float (&f)[16]) {
+  const uint32_t w[8] = {v[0].x, v[0].y, v[0].z, v[0].w, v[1].x, v[1].y, v[1].z, v[1].w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    f[2 * i] = bf16_lo(w[i]);
+    f[2 * i + 1] = bf16_hi(w[i]);
+  }
+}
+
+__device__ __forceinline__ uint4 ld_stream(const void *p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ float amax16(const float (&f)[16]) {
+  float m = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(f[i]));
+  return m;
+}
+
+// 16 binary32 values -> 16 E4M3 codes (RNE, saturating), packed little-endian.
+__device__ __forceinline__ uint4 to_e4m3x16(const float (&t)[16]) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(t[4 * i], t[4 * i + 1]),
+                                                 __NV_SATFINITE, __NV_E4M3);
+    const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(t[4 * i + 2], t[4 * i + 3]),
+                                                 __NV_SATFINITE, __NV_E4M3);
+    w[i] = (lo & 0xFFFFu) | (hi << 16);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// ---------------------------------------------------------------- group-128 activation quant
+// 8 threads per 128-channel group, 16 channels (32 bytes) per thread; a
+// partial last group masks whole 16-channel chunks (K % 16 == 0).
+__global__ void __launch_bounds__(kThreads) quant_group128_kernel(
+    const uint8_t *__restrict__ x, int64_t M, int K, int64_t ldx_bytes, int G,
+    uint8_t *__restrict__ q, float *__restrict__ s, int s_layout, int64_t lds) {
+  const int64_t gid = static_cast<int64_t>(blockIdx.x) * (kThreads / 8) + (threadIdx.x >> 3);
+  const int sub = threadIdx.x & 7;
+  const bool in_range = gid < M * G;
+  const int64_t row = in_range ? gid / G : 0;
+  const int g = in_range ? static_cast<int>(gid - row * G) : 0;
+  const int k = g * 128 + sub * 16;
+  const bool valid = in_range && k < K;
+
+  uint4 v[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+  if (valid) {
+    const uint8_t *p = x + row * ldx_bytes + static_cast<int64_t>(k) * 2;
+    v[0] = ld_stream(p);
+    v[1] = ld_stream(p + 16);
+  }
+  float f[16];
+  unpack16(v, f);
+  float amax = amax16(f);
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+  const float sg = __fdiv_rn(fmaxf(amax, kFloor), 448.0f);
+  float t[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) t[i] = __fdiv_rn(f[i], sg);
+  const uint4 out = to_e4m3x16(t);
+  if (valid) *reinterpret_cast<uint4 *>(q + row * K + k) = out;
+  if (in_range && sub == 0) {
+    if (s_layout == 0) s[row * lds + g] = sg;
+    else s[static_cast<int64_t>(g) * lds + row] = sg;
+  }
+}
+
+// ---------------------------------------------------------------- MXFP8 [1,32] quant
+// 2 threads per 32-channel group.  e = ceil(log2(r)), r = max(amax,1e-10)/448
+// read from r's bits (r is a positive normal float): biased exponent plus one
+// unless the mantissa is zero.  The UE8M0 code is e + 127.
+__global__ void __launch_bounds__(kThreads) quant_mx_kernel(const uint8_t *__restrict__ x,
+                                                            int64_t M, int K,
+                                                            int64_t ldx_bytes,
+                                                            uint8_t *__restrict__ q,
+                                                            uint8_t *__restrict__ s) {
+  const int G = K / 32;
+  const int64_t gid = static_cast<int64_t>(blockIdx.x) * (kThreads / 2) + (threadIdx.x >> 1);
+  const int sub = threadIdx.x & 1;
+  const bool valid = gid < M * G;
+  const int64_t row = valid ? gid / G : 0;
+  const int g = valid ? static_cast<int>(gid - row * G) : 0;
+  const int k = g * 32 + sub * 16;
+  uint4 v[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+  if (valid) {
+    const uint8_t *p = x + row * ldx_bytes + static_cast<int64_t>(k) * 2;
+    v[0] = ld_stream(p);
+    v[1] = ld_stream(p + 16);
+  }
+  float f[16];
+  unpack16(v, f);
+  float amax = amax16(f);
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  const float r = __fdiv_rn(fmaxf(amax, kFloor), 448.0f);
+  const uint32_t rb = __float_as_uint(r);
+  const uint32_t u = (rb >> 23) + ((rb & 0x7FFFFFu) != 0u ? 1u : 0u);  // e + 127
+  const float inv = __uint_as_float((254u - u) << 23);                 // 2^-e, exact
+  float t[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) t[i] = __fmul_rn(f[i], inv);
+  const uint4 out = to_e4m3x16(t);
+  if (valid) {
+    *reinterpret_cast<uint4 *>(q + row * K + k) = out;
+    if (sub == 0) s[row * G + g] = static_cast<uint8_t>(u);
+  }
+}
+
+// ---------------------------------------------------------------- static per-tensor quant
+__global__ void __launch_bounds__(kThreads) quant_static_kernel(const uint8_t *__restrict__ x,
+                                                                int64_t M, int K,
+                                                                int64_t ldx_bytes,
+                                                                const float *__restrict__ s_ptr,
+                                                                uint8_t *__restrict__ q) {
+  const int C = K / 16;
+  const int64_t cid = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+  if (cid >= M * C) return;
+  const int64_t row = cid / C;
+  const int k = static_cast<int>(cid - row * C) * 16;
+  const float sv = __ldg(s_ptr);
+  const uint8_t *p = x + row * ldx_bytes + static_cast<int64_t>(k) * 2;
+  uint4 v[2] = {ld_stream(p), ld_stream(p + 16)};
+  float f[16];
+  unpack16(v, f);
+  float t[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) t[i] = __fdiv_rn(f[i], sv);
+  *reinterpret_cast<uint4 *>(q + row * K + k) = to_e4m3x16(t);
+}
+
+// ---------------------------------------------------------------- 128x128 weight blocks
+// One CTA per block; thread t covers row t/2 of the block and 64 channels.
+__global__ void __launch_bounds__(kThreads) quant_weight_block_kernel(
+    const uint8_t *__restrict__ w, int N, int K, int64_t ldw_bytes, uint8_t *__restrict__ q,
+    float *__restrict__ s, int KB) {
+  __shared__ float red[kThreads / 32];
+  const int nb = blockIdx.y, kb = blockIdx.x;
+  const int r = nb * 128 + (threadIdx.x >> 1);
+  const int kbase = kb * 128 + (threadIdx.x & 1) * 64;
+  float f[4][16];
+  bool ok[4];
+  float amax = 0.0f;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const int k = kbase + c * 16;
+    ok[c] = r < N && k < K;
+    uint4 v[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+    if (ok[c]) {
+      const uint8_t *p = w + static_cast<int64_t>(r) * ldw_bytes + static_cast<int64_t>(k) * 2;
+      v[0] = ld_stream(p);
+      v[1] = ld_stream(p + 16);
+    }
+    unpack16(v, f[c]);
+    amax = fmaxf(amax, amax16(f[c]));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  amax = red[0];
+#pragma unroll
+  for (int i = 1; i < kThreads / 32; ++i) amax = fmaxf(amax, red[i]);
+  const float sb = __fdiv_rn(fmaxf(amax, kFloor), 448.0f);
+  if (threadIdx.x == 0) s[nb * KB + kb] = sb;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    float t[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) t[i] = __fdiv_rn(f[c][i], sb);
+    const uint4 out = to_e4m3x16(t);
+    if (ok[c])
+      *reinterpret_cast<uint4 *>(q + static_cast<int64_t>(r) * K + kbase + c * 16) = out;
+  }
+}
+
+// ---------------------------------------------------------------- per-tensor absmax scale
+// amax over the matrix via atomicMax on the bit patterns of non-negative floats
+// (their integer order equals their numeric order), then s = max(amax,1e-10)/448.
+__global__ void __launch_bounds__(kThreads) absmax_kernel(const uint8_t *__restrict__ x,
+                                                          int64_t rows, int K,
+                                                          int64_t ldx_bytes,
+                                                          uint32_t *__restrict__ acc) {
+  const int C = K / 16;
+  const int64_t total = rows * C;
+  float m = 0.0f;
+  for (int64_t cid = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; cid < total;
+       cid += static_cast<int64_t>(gridDim.x) * kThreads) {
+    const int64_t row = cid / C;
+    const int k = static_cast<int>(cid - row * C) * 16;
+    const uint8_t *p = x + row * ldx_bytes + static_cast<int64_t>(k) * 2;
+    uint4 v[2] = {ld_stream(p), ld_stream(p + 16)};
+    float f[16];
+    unpack16(v, f);
+    m = fmaxf(m, amax16(f));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((threadIdx.x & 31) == 0) atomicMax(acc, __float_as_uint(m));
+}
+
+__global__ void absmax_finalize_kernel(float *s) {
+  const float amax = __uint_as_float(*reinterpret_cast<uint32_t *>(s));
+  *s = __fdiv_rn(fmaxf(amax, kFloor), 448.0f);
+}
+
+inline unsigned blocks_for(int64_t work, int per_block) {
+  return static_cast<unsigned>((work + per_block - 1) / per_block);
+}
+
+}  // namespace
+
+void launch_quant_group(const void *x, int64_t M, int64_t K, int64_t ldx, void *q, float *s,
+                        int s_layout, cudaStream_t st) {
+  const int G = static_cast<int>((K + 127) / 128);
+  const int64_t lds = s_layout == 0 ? G : ((M + 3) / 4) * 4;
+  quant_group128_kernel<<<blocks_for(M * G, kThreads / 8), kThreads, 0, st>>>(
+      static_cast<const uint8_t *>(x), M, static_cast<int>(K), ldx * 2, G,
+      static_cast<uint8_t *>(q), s, s_layout, lds);
+}
+
+void launch_quant_mx(const void *x, int64_t M, int64_t K, int64_t ldx, void *q, uint8_t *s,
+                     cudaStream_t st) {
+  quant_mx_kernel<<<blocks_for(M * (K / 32), kThreads / 2), kThreads, 0, st>>>(
+      static_cast<const uint8_t *>(x), M, static_cast<int>(K), ldx * 2,
+      static_cast<uint8_t *>(q), s);
+}
+
+void launch_quant_static(const void *x, int64_t M, int64_t K, int64_t ldx, const float *s,
+                         void *q, cudaStream_t st) {
+  quant_static_kernel<<<blocks_for(M * (K / 16), kThreads), kThreads, 0, st>>>(
+      static_cast<const uint8_t *>(x), M, static_cast<int>(K), ldx * 2, s,
+      static_cast<uint8_t *>(q));
+}
+
+void launch_quant_weight_block(const void *w, int64_t N, int64_t K, int64_t ldw, void *q,
+                               float *s, cudaStream_t st) {
+  const int KB = static_cast<int>((K + 127) / 128);
+  const int NB = static_cast<int>((N + 127) / 128);
+  quant_weight_block_kernel<<<dim3(KB, NB), kThreads, 0, st>>>(
+      static_cast<const uint8_t *>(w), static_cast<int>(N), static_cast<int>(K), ldw * 2,
+      static_cast<uint8_t *>(q), s, KB);
+}
+
+void launch_absmax_scale(const void *x, int64_t rows, int64_t K, int64_t ldx, float *s,
+                         int num_sms, cudaStream_t st) {
+  cudaMemsetAsync(s, 0, sizeof(float), st);
+  const int64_t work = rows * (K / 16);
+  unsigned grid = blocks_for(work, kThreads);
+  const unsigned cap = static_cast<unsigned>(num_sms) * 8u;
+  if (grid > cap) grid = cap;
+  if (grid == 0) grid = 1;
+  absmax_kernel<<<grid, kThreads, 0, st>>>(static_cast<const uint8_t *>(x), rows,
+                                           static_cast<int>(K), ldx * 2,
+                                           reinterpret_cast<uint32_t *>(s));
+  absmax_finalize_kernel<<<1, 1, 0, st>>>(s);
+}
+
+}  // namespace fp8bq

@@ -1,0 +1,199 @@
+/*
+ * fp8bq.h -- C ABI of the block-wise FP8 W8A8 linear for one NVIDIA GB300 (sm_103a).
+ *
+ * The operation is the forward of an FP8 linear layer as the pages describe it
+ * (apply(layer, x, bias) -> y, with the layer's E4M3 weight and its scales):
+ *
+ *   1. activation quantisation: per token, per group of 128 channels,
+ *      s = max|x| / 448 and q = round_to_nearest_even(x / s), saturated to +-448
+ *      ("SGLang 源码完全拆解(十九)", §从浮点到 FP8 的基本公式 and
+ *      §Triton 分块内核在做什么; "GLM-5.3 推理全链路(十七)", §第1站 eq. for s_g, q_i);
+ *   2. block-scaled FP8 GEMM: y[i][j] = sum_b (sum_{k in block b} q[i][k] w[j][k])
+ *      * s_x[i][b] * s_w[j/128][b], FP32 accumulation, promoted once per 128-wide
+ *      K block, BF16 output ("SGLang 源码完全拆解(十九)", §一条 GEMM 的三种缩放组合,
+ *      the block-wise equation; §Triton 分块内核在做什么);
+ *   3. the two fused: BF16 in, BF16 out (same page, §一次前向的完整时序);
+ *   plus an MXFP8 variant ([1,32] blocks, UE8M0 scales; same page §checkpoint
+ *   里的量化元数据 and "[SGLang] FP8" §4) and a static per-tensor variant
+ *   (one activation scale, one weight scale per output partition; "SGLang 源码完全
+ *   拆解(十九)", §激活量化的三种选择 and "[SGLang] FP8" §5).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *    allocates nothing and keeps no per-call state.  Host pointers are named
+ *    `*_host`.
+ *  - Layouts are row-major.  X is BF16 [M, K] with row pitch `ldx` elements;
+ *    Q (E4M3 codes) is [M, K] with pitch K; W is E4M3 [N, K] with pitch K;
+ *    Y is BF16 [M, N] with pitch N.  bias, when not NULL, is BF16 [N].
+ *  - Block path scales: s_w is FP32 [ceil(N/128)][ceil(K/128)] ("weight_scale_inv",
+ *    the dequantisation multiplier); s_x is FP32 and either row-major
+ *    [M][ceil(K/128)] (FP8BQ_SCALE_ROW_MAJOR) or column-major
+ *    [ceil(K/128)][round_up(M,4)] (FP8BQ_SCALE_COL_MAJOR).
+ *  - MX path scales are UE8M0 codes (uint8, value 2^(u-127)), row-major
+ *    [rows][K/32] for both activations and weights.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    Calls are asynchronous and stream-ordered.
+ *  - Arguments are validated on the host before anything is launched; on an
+ *    error nothing is launched and no output is touched.  M == 0 is a valid
+ *    empty batch: FP8BQ_OK without launching, and the tensor pointers may be NULL.
+ *  - Requirements: x, q, w, y 16-byte aligned; ldx >= K and ldx % 8 == 0;
+ *    K % 16 == 0 for the E4M3 paths and K % 32 == 0 for MX; FP32 scale
+ *    pointers 4-byte aligned; bias 2-byte aligned.
+ *  - GEMM and linear entry points take a workspace `ws` of at least
+ *    fp8bq_workspace_bytes(op, M, N, K) bytes, 256-byte aligned, zeroed once
+ *    with fp8bq_workspace_init before its first use.  The library keeps it in a
+ *    valid state between calls.  Calls that share a workspace must not overlap
+ *    on the GPU (same stream, or ordered by events).
+ *  - Every device-side wait is bounded: a wait that runs out sets a status word
+ *    in the workspace, the kernel exits cleanly, and fp8bq_poll_status reports
+ *    FP8BQ_ERR_TIMEOUT.  The limit is 1 s per wait, or FP8BQ_WAIT_LIMIT_MS from
+ *    the environment, read once.  After a timeout the outputs are undefined.
+ *  - No C++ exception crosses this interface.
+ */
+#ifndef FP8BQ_H
+#define FP8BQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FP8BQ_API __attribute__((visibility("default")))
+
+/* Status codes returned by every int-returning entry point. */
+typedef enum fp8bq_status {
+  FP8BQ_OK = 0,
+  FP8BQ_ERR_NULL = 1,        /* a required pointer is NULL                          */
+  FP8BQ_ERR_SHAPE = 2,       /* M < 0, N < 1, K < 1, ldx < K, bad partitions         */
+  FP8BQ_ERR_ALIGN = 3,       /* pointer or pitch breaks the alignment rules above   */
+  FP8BQ_ERR_UNSUPPORTED = 4, /* bad enum value or a shape the kernels do not cover  */
+  FP8BQ_ERR_ARCH = 5,        /* current device is not compute capability 10.3       */
+  FP8BQ_ERR_WORKSPACE = 6,   /* workspace NULL or smaller than required             */
+  FP8BQ_ERR_CUDA = 7,        /* a CUDA runtime call failed; see fp8bq_last_cuda_error */
+  FP8BQ_ERR_TIMEOUT = 8      /* a device wait gave up (reported by fp8bq_poll_status) */
+} fp8bq_status;
+
+enum { FP8BQ_SCALE_ROW_MAJOR = 0, FP8BQ_SCALE_COL_MAJOR = 1 };
+
+/* Operation ids for fp8bq_workspace_bytes. */
+enum {
+  FP8BQ_OP_GEMM = 0,
+  FP8BQ_OP_LINEAR = 1,
+  FP8BQ_OP_MX_GEMM = 2,
+  FP8BQ_OP_MX_LINEAR = 3,
+  FP8BQ_OP_STATIC_GEMM = 4,
+  FP8BQ_OP_STATIC_LINEAR = 5
+};
+
+/* ---------------------------------------------------------------- utility */
+
+/* Library version, major*10000 + minor*100 + patch. */
+FP8BQ_API int fp8bq_version(void);
+
+/* Static string for a status code ("unknown status" for other values). */
+FP8BQ_API const char *fp8bq_status_string(int status);
+
+/* cudaError_t of the last FP8BQ_ERR_CUDA returned on the calling thread (0 if none). */
+FP8BQ_API int fp8bq_last_cuda_error(void);
+
+/* Workspace bytes needed by `op` at this shape (a multiple of 256; never 0). */
+FP8BQ_API size_t fp8bq_workspace_bytes(int op, int64_t M, int64_t N, int64_t K);
+
+/* Zeroes `ws_bytes` bytes of a workspace on `stream` (required once before first use). */
+FP8BQ_API int fp8bq_workspace_init(void *ws, size_t ws_bytes, void *stream);
+
+/* Synchronises `stream`, then returns and clears the workspace status word:
+ * FP8BQ_OK, or FP8BQ_ERR_TIMEOUT if a kernel's bounded wait ran out. */
+FP8BQ_API int fp8bq_poll_status(void *ws, void *stream);
+
+/* ------------------------------------------------ block path (group/block 128) */
+
+/* Per-token group-128 activation quantisation (per_token_group_quant_fp8).
+ * x: BF16 [M, K] pitch ldx.  q: E4M3 [M, K].  s: FP32 scales in `s_layout`.
+ * Bit-exact rule: amax = max|x| over the group (floored at 1e-10),
+ * s = amax / 448 and q = RNE_sat(x / s), both IEEE binary32 divisions. */
+FP8BQ_API int fp8bq_quant_act(const void *x, int64_t M, int64_t K, int64_t ldx,
+                              void *q, float *s, int s_layout, void *stream);
+
+/* Block-scaled FP8 GEMM: y = BF16(sum_b P_b * s_x[:, b] * s_w[n/128, b] + bias),
+ * P_b the FP32 tensor-core sum over K block b. */
+FP8BQ_API int fp8bq_gemm(const void *q, const float *s_x, int s_layout,
+                         const void *w, const float *s_w, const void *bias,
+                         void *y, int64_t M, int64_t N, int64_t K, void *ws,
+                         size_t ws_bytes, void *stream);
+
+/* Fused linear: fp8bq_quant_act into the workspace, then fp8bq_gemm. */
+FP8BQ_API int fp8bq_linear(const void *x, int64_t ldx, const void *w,
+                           const float *s_w, const void *bias, void *y,
+                           int64_t M, int64_t N, int64_t K, void *ws,
+                           size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------ MXFP8 path ([1,32], UE8M0) */
+
+/* MXFP8 activation quantisation: per 32-channel group, e = ceil(log2(max(amax,
+ * 1e-10) / 448)) (binary32 division), s = e + 127 (UE8M0), q = RNE_sat(x * 2^-e).
+ * s: uint8 [M][K/32].  Also quantises weights (rows = N). */
+FP8BQ_API int fp8bq_mx_quant_act(const void *x, int64_t M, int64_t K,
+                                 int64_t ldx, void *q, uint8_t *s,
+                                 void *stream);
+
+/* MXFP8 GEMM on the tensor cores' block-scaled MMA: s_x uint8 [M][K/32],
+ * s_w uint8 [N][K/32]; y = BF16(sum_g P_g * 2^(s_x-127) * 2^(s_w-127) + bias). */
+FP8BQ_API int fp8bq_mx_gemm(const void *q, const uint8_t *s_x, const void *w,
+                            const uint8_t *s_w, const void *bias, void *y,
+                            int64_t M, int64_t N, int64_t K, void *ws,
+                            size_t ws_bytes, void *stream);
+
+/* Fused MXFP8 linear: fp8bq_mx_quant_act into the workspace, then fp8bq_mx_gemm. */
+FP8BQ_API int fp8bq_mx_linear(const void *x, int64_t ldx, const void *w,
+                              const uint8_t *s_w, const void *bias, void *y,
+                              int64_t M, int64_t N, int64_t K, void *ws,
+                              size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------ static per-tensor path */
+
+/* Static quantisation with one device-resident FP32 scale s_x[0]:
+ * q = RNE_sat(x / s_x), binary32 division. */
+FP8BQ_API int fp8bq_static_quant_act(const void *x, int64_t M, int64_t K,
+                                     int64_t ldx, const float *s_x, void *q,
+                                     void *stream);
+
+/* Per-tensor FP8 GEMM: y = BF16((sum_k q w) * s_x[0] * s_w_part[p(j)] + bias),
+ * p(j) the output partition of row j.  part_sizes_host[n_parts] (host memory,
+ * 1 <= n_parts <= 64) must sum to N; s_w_part is a device FP32 [n_parts]. */
+FP8BQ_API int fp8bq_static_gemm(const void *q, const float *s_x, const void *w,
+                                const float *s_w_part,
+                                const int64_t *part_sizes_host, int n_parts,
+                                const void *bias, void *y, int64_t M, int64_t N,
+                                int64_t K, void *ws, size_t ws_bytes,
+                                void *stream);
+
+/* Fused static linear: fp8bq_static_quant_act into the workspace, then fp8bq_static_gemm. */
+FP8BQ_API int fp8bq_static_linear(const void *x, int64_t ldx, const float *s_x,
+                                  const void *w, const float *s_w_part,
+                                  const int64_t *part_sizes_host, int n_parts,
+                                  const void *bias, void *y, int64_t M,
+                                  int64_t N, int64_t K, void *ws,
+                                  size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------ weight / calibration set-up */
+
+/* 128x128 block quantisation of a BF16 weight [N, K] (pitch ldw) into E4M3
+ * [N, K] and FP32 s_w [ceil(N/128)][ceil(K/128)]; a partial edge block uses
+ * only its valid elements.  Same arithmetic as fp8bq_quant_act. */
+FP8BQ_API int fp8bq_quant_weight_block(const void *w, int64_t N, int64_t K,
+                                       int64_t ldw, void *q, float *s_w,
+                                       void *stream);
+
+/* One per-tensor scale s[0] = max(max|x|, 1e-10) / 448 over a BF16 [rows, K]
+ * matrix (pitch ldx): a calibration batch, or one weight partition. */
+FP8BQ_API int fp8bq_absmax_scale(const void *x, int64_t rows, int64_t K,
+                                 int64_t ldx, float *s, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FP8BQ_H */

@@ -16,6 +16,9 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a GB300 GPU and the CUDA library")
+    # build the CUDA library and the oracle in-tree if missing or stale (no-op otherwise)
+    import __graft_entry__
+    __graft_entry__.build()
 
 
 @pytest.fixture(scope="session")

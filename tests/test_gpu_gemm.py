@@ -1,0 +1,160 @@
+"""GPU parity of the block-scaled FP8 GEMM and the fused linear against the CPU
+oracle's binary64 result on the same quantised inputs.
+
+Tolerance (per element |y - ref| <= 1e-2 max(1,|ref|), relative Frobenius
+<= 4e-3) at sizes the oracle computes in full; at the prefill sizes on sampled
+outputs.  Covers both tile orientations (decode M <= 64 swaps operands and
+splits K), ragged M/N/K, both activation-scale layouts, bias, pitch > K,
+determinism of the split-K reduction and an exactly representable case."""
+import numpy as np
+import pytest
+import torch
+
+import block_wise_fp8_gb300 as fb
+import oracle
+import synthetic_inputs as si
+from gpu_util import check_close, dev, host, sample_indices
+
+pytestmark = pytest.mark.gpu
+
+
+def _weights(N, K):
+    return oracle.quant_weight_block(si.weights(N, K))
+
+
+def _gemm(qa, sa, qw, sw, bias=None, layout=fb.SCALE_ROW_MAJOR, ws=None):
+    M, K = qa.shape
+    N = qw.shape[0]
+    if layout == fb.SCALE_COL_MAJOR:
+        M4 = -(-M // 4) * 4
+        sa_dev = np.zeros((sa.shape[1], M4), np.float32)
+        sa_dev[:, :M] = sa.T
+    else:
+        sa_dev = sa
+    y = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    if ws is None:
+        ws = fb.new_workspace(fb.OP_GEMM, M, N, K)
+    fb.fp8bq_gemm(dev(qa), dev(sa_dev), dev(qw), dev(sw), y, ws,
+                  bias=None if bias is None else dev(bias), s_layout=layout)
+    assert fb.fp8bq_poll_status(ws) == 0
+    return host(y)
+
+
+@pytest.mark.parametrize("M,N,K", [(16, 384, 256), (5, 200, 208), (1, 128, 128),
+                                   (64, 384, 1024), (128, 256, 128), (200, 520, 384),
+                                   (256, 512, 2048), (131, 257 * 8, 144), (65, 136, 16)])
+@pytest.mark.parametrize("layout", [fb.SCALE_ROW_MAJOR, fb.SCALE_COL_MAJOR])
+def test_gemm_small_shapes(M, N, K, layout):
+    qa, sa = oracle.quant_group(si.activations(M, K))
+    qw, sw = _weights(N, K)
+    y = _gemm(qa, sa, qw, sw, layout=layout)
+    check_close(y, oracle.gemm_block(qa, sa, qw, sw), f"gemm {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M", [1, 8, 32, 64])
+def test_gemm_decode_full(M):
+    K = N = 6144
+    qa, sa = oracle.quant_group(si.activations(M, K))
+    qw, sw = _weights(N, K)
+    y = _gemm(qa, sa, qw, sw)
+    check_close(y, oracle.gemm_block(qa, sa, qw, sw), f"decode M={M}")
+
+
+@pytest.mark.parametrize("N", [6144, 24576])
+def test_gemm_prefill_sampled(N):
+    M, K = 4096, 6144
+    qa, sa = oracle.quant_group(si.activations(M, K))
+    qw, sw = _weights(N, K)
+    y = _gemm(qa, sa, qw, sw)
+    rows, cols = sample_indices(M, N, 3000)
+    ref = oracle.gemm_block_sampled(qa, sa, qw, sw, rows, cols)
+    check_close(y[rows, cols], ref, f"prefill N={N}")
+    # whole-output properties: finite everywhere, and the RMS matches the sample
+    assert np.all(np.isfinite(y))
+    assert abs(np.sqrt(np.mean(y ** 2)) / np.sqrt(np.mean(ref ** 2)) - 1) < 0.1
+
+
+def test_gemm_bias():
+    M, N, K = 48, 256, 384
+    qa, sa = oracle.quant_group(si.activations(M, K))
+    qw, sw = _weights(N, K)
+    bias = si.f32_to_bf16_bits(np.linspace(-4, 4, N).astype(np.float32))
+    for m in (48, 160):  # both orientations
+        qa_m, sa_m = oracle.quant_group(si.activations(m, K))
+        y = _gemm(qa_m, sa_m, qw, sw, bias=bias)
+        check_close(y, oracle.gemm_block(qa_m, sa_m, qw, sw, bias=bias), f"bias M={m}")
+    del qa, sa
+
+
+def test_gemm_integer_case_is_exact():
+    """Unit scales and codes in {0, +-0.5, +-1, +-2}: every partial sum is a
+    multiple of 1/4 below 2^10, exact in FP32, so the output must be exactly the
+    round-to-nearest-even BF16 value of the oracle's result."""
+    rng = np.random.default_rng(3)
+    small = np.array([0x00, 0x30, 0xB0, 0x38, 0xB8, 0x40, 0xC0], np.uint8)
+    for M in (7, 192):
+        N, K = 256, 256
+        qa = rng.choice(small, (M, K))
+        qw = rng.choice(small, (N, K))
+        sa = np.ones((M, 2), np.float32)
+        sw = np.ones((2, 2), np.float32)
+        y = _gemm(qa, sa, qw, sw)
+        ref = oracle.gemm_block(qa, sa, qw, sw)
+        assert np.all(np.abs(ref) <= 256)
+        ref_bf16 = torch.from_numpy(ref).to(torch.bfloat16).double().numpy()
+        assert np.array_equal(y, ref_bf16)
+
+
+def test_split_k_reduction_is_deterministic():
+    M, N, K = 8, 6144, 6144
+    qa, sa = oracle.quant_group(si.activations(M, K))
+    qw, sw = _weights(N, K)
+    ws = fb.new_workspace(fb.OP_GEMM, M, N, K)
+    ys = [_gemm(qa, sa, qw, sw, ws=ws) for _ in range(3)]
+    assert np.array_equal(ys[0], ys[1]) and np.array_equal(ys[1], ys[2])
+
+
+@pytest.mark.parametrize("M,N,K", [(16, 384, 256), (1, 6144, 6144), (64, 6144, 6144),
+                                   (300, 384, 256), (4096, 6144, 6144)])
+def test_linear_matches_oracle(M, N, K):
+    x = si.activations(M, K)
+    qw, sw = _weights(N, K)
+    qa, sa = oracle.quant_group(x)
+    xd = dev(x)
+    y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    ws = fb.new_workspace(fb.OP_LINEAR, M, N, K)
+    fb.fp8bq_linear(xd, dev(qw), dev(sw), y, ws)
+    assert fb.fp8bq_poll_status(ws) == 0
+    yh = host(y)
+    if M * N * K <= 64 * 6144 * 6144:
+        check_close(yh, oracle.gemm_block(qa, sa, qw, sw), f"linear {M}x{N}x{K}")
+    else:
+        rows, cols = sample_indices(M, N, 2000)
+        check_close(yh[rows, cols], oracle.gemm_block_sampled(qa, sa, qw, sw, rows, cols),
+                    f"linear {M}x{N}x{K}")
+
+
+def test_linear_with_pitch_and_bias():
+    M, N, K = 40, 256, 512
+    x = si.activations(M, K)
+    qw, sw = _weights(N, K)
+    bias = si.f32_to_bf16_bits(np.linspace(-1, 1, N).astype(np.float32))
+    wide = torch.zeros(M, K + 128, dtype=torch.bfloat16, device="cuda")
+    wide[:, :K] = dev(x)
+    y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    ws = fb.new_workspace(fb.OP_LINEAR, M, N, K)
+    fb.fp8bq_linear(wide[:, :K], dev(qw), dev(sw), y, ws, bias=dev(bias))
+    assert fb.fp8bq_poll_status(ws) == 0
+    qa, sa = oracle.quant_group(x)
+    check_close(host(y), oracle.gemm_block(qa, sa, qw, sw, bias=bias), "linear pitch+bias")
+
+
+def test_empty_batch():
+    ws = fb.new_workspace(fb.OP_GEMM, 0, 256, 256)
+    y = torch.empty(0, 256, dtype=torch.bfloat16, device="cuda")
+    q = torch.empty(0, 256, dtype=torch.uint8, device="cuda")
+    s = torch.empty(0, 2, dtype=torch.float32, device="cuda")
+    w = torch.zeros(256, 256, dtype=torch.uint8, device="cuda")
+    sw = torch.ones(2, 2, dtype=torch.float32, device="cuda")
+    fb.fp8bq_gemm(q, s, w, sw, y, ws)
+    torch.cuda.synchronize()

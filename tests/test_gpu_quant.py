@@ -1,0 +1,163 @@
+"""GPU parity of the quantisation kernels against the CPU oracle: E4M3 codes and
+scales must be bit-identical, on the five workloads' shapes, ragged K, both
+scale layouts, a row pitch wider than K, and every finite BF16 input."""
+import numpy as np
+import pytest
+import torch
+
+import block_wise_fp8_gb300 as fb
+import oracle
+import synthetic_inputs as si
+from gpu_util import dev, host
+
+pytestmark = pytest.mark.gpu
+
+
+def _gpu_quant_group(x, layout=fb.SCALE_ROW_MAJOR, ldx_pad=0):
+    M, K = x.shape
+    xd = dev(x)
+    if ldx_pad:
+        wide = torch.zeros(M, K + ldx_pad, dtype=torch.bfloat16, device="cuda")
+        wide[:, :K] = xd
+        xd = wide[:, :K]
+    G = -(-K // 128)
+    q = torch.empty(M, K, dtype=torch.uint8, device="cuda")
+    if layout == fb.SCALE_ROW_MAJOR:
+        s = torch.full((M, G), -1.0, dtype=torch.float32, device="cuda")
+    else:
+        s = torch.full((G, -(-M // 4) * 4), -1.0, dtype=torch.float32, device="cuda")
+    fb.fp8bq_quant_act(xd, q, s, layout)
+    torch.cuda.synchronize()
+    return host(q), host(s)
+
+
+@pytest.mark.parametrize("M,K", [(16, 256), (5, 208), (1, 6144), (8, 6144), (32, 6144),
+                                 (64, 6144), (4096, 6144), (2048, 7168), (4096, 4096),
+                                 (3, 16), (7, 144)])
+def test_quant_group_bit_exact(M, K):
+    x = si.activations(M, K)
+    q, s = _gpu_quant_group(x)
+    qr, sr = oracle.quant_group(x)
+    assert np.array_equal(s.view(np.uint32), sr.view(np.uint32))
+    assert np.array_equal(q, qr)
+
+
+def test_quant_group_col_major_and_pitch():
+    M, K = 37, 6144
+    x = si.activations(M, K)
+    q, s = _gpu_quant_group(x, fb.SCALE_COL_MAJOR, ldx_pad=64)
+    qr, sr = oracle.quant_group(x)
+    assert np.array_equal(q, qr)
+    assert np.array_equal(s[:, :M].view(np.uint32), sr.T.view(np.uint32))
+
+
+def test_quant_group_special_values():
+    """zero groups, negative zero, tiny and subnormal BF16 values, exact powers."""
+    K = 512
+    x = np.zeros((4, K), np.uint16)
+    x[1, :128] = 0x8000                                              # -0.0
+    x[1, 128:256] = si.f32_to_bf16_bits(np.linspace(-1e-38, 1e-38, 128).astype(np.float32))
+    x[2] = si.f32_to_bf16_bits((np.arange(K) - 256).astype(np.float32) * 2.0 ** -20)
+    x[3] = np.arange(K, dtype=np.uint16) * 127                        # assorted patterns
+    x[3][((x[3] >> 7) & 0xFF) == 0xFF] = 0                            # no inf/nan
+    q, s = _gpu_quant_group(x)
+    qr, sr = oracle.quant_group(x)
+    assert np.array_equal(s.view(np.uint32), sr.view(np.uint32))
+    assert np.array_equal(q, qr)
+
+
+def test_static_quant_every_finite_bf16_value():
+    """s = 1: q = RNE_sat(x) for all 2^16 BF16 patterns except Inf/NaN, which checks
+    the hardware conversion (saturation, subnormals, ties, signed zero) against
+    the oracle's encoder exhaustively over BF16 inputs."""
+    pats = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    pats = pats[((pats >> 7) & 0xFF) != 0xFF]
+    pats = np.concatenate([pats, np.zeros((-len(pats)) % 16, np.uint16)])
+    x = pats.reshape(-1, 16 * 64) if len(pats) % (16 * 64) == 0 else pats.reshape(-1, 16)
+    sx = torch.ones(1, dtype=torch.float32, device="cuda")
+    q = torch.empty(x.shape, dtype=torch.uint8, device="cuda")
+    fb.fp8bq_static_quant_act(dev(x), sx, q)
+    torch.cuda.synchronize()
+    assert np.array_equal(host(q), oracle.quant_static(x, 1.0))
+
+
+@pytest.mark.parametrize("M,K", [(2048, 7168), (5, 96), (64, 7168), (1, 32)])
+def test_quant_mx_bit_exact(M, K):
+    x = si.activations(M, K)
+    q = torch.empty(M, K, dtype=torch.uint8, device="cuda")
+    s = torch.empty(M, K // 32, dtype=torch.uint8, device="cuda")
+    fb.fp8bq_mx_quant_act(dev(x), q, s)
+    torch.cuda.synchronize()
+    qr, ur = oracle.quant_mx(x)
+    assert np.array_equal(host(s), ur)
+    assert np.array_equal(host(q), qr)
+
+
+def test_quant_mx_special_groups():
+    row = np.zeros((3, 64), np.float32)
+    row[1, 5] = 448.0 * 2.0 ** -7
+    row[1, 40] = 450.0 * 2.0 ** 9
+    row[2] = np.linspace(-3e-39, 3e-39, 64)
+    x = si.f32_to_bf16_bits(row)
+    q = torch.empty(3, 64, dtype=torch.uint8, device="cuda")
+    s = torch.empty(3, 2, dtype=torch.uint8, device="cuda")
+    fb.fp8bq_mx_quant_act(dev(x), q, s)
+    torch.cuda.synchronize()
+    qr, ur = oracle.quant_mx(x)
+    assert np.array_equal(host(s), ur) and np.array_equal(host(q), qr)
+
+
+@pytest.mark.parametrize("M", [1, 512, 4096])
+def test_static_scale_and_quant_bit_exact(M):
+    K = 4096
+    calib = si.calibration(256, K)
+    s_gpu = torch.empty(1, dtype=torch.float32, device="cuda")
+    fb.fp8bq_absmax_scale(dev(calib), s_gpu)
+    s_ref = oracle.absmax_scale(calib)
+    torch.cuda.synchronize()
+    assert host(s_gpu).view(np.uint32)[0] == np.float32(s_ref).view(np.uint32)
+    x = si.activations(M, K)              # outlier channels exceed the calibration range
+    q = torch.empty(M, K, dtype=torch.uint8, device="cuda")
+    fb.fp8bq_static_quant_act(dev(x), s_gpu, q)
+    torch.cuda.synchronize()
+    qr = oracle.quant_static(x, s_ref)
+    assert np.array_equal(host(q), qr)
+    if M > 1:
+        assert np.any(qr == 0x7E)          # saturation is exercised
+
+
+@pytest.mark.parametrize("N,K", [(384, 256), (200, 208), (6144, 6144), (130, 16)])
+def test_weight_block_quant_bit_exact(N, K):
+    w = si.weights(N, K)
+    q = torch.empty(N, K, dtype=torch.uint8, device="cuda")
+    s = torch.empty(-(-N // 128), -(-K // 128), dtype=torch.float32, device="cuda")
+    fb.fp8bq_quant_weight_block(dev(w), q, s)
+    torch.cuda.synchronize()
+    qr, sr = oracle.quant_weight_block(w)
+    assert np.array_equal(host(s).view(np.uint32), sr.view(np.uint32))
+    assert np.array_equal(host(q), qr)
+
+
+def test_weight_partition_scales_bit_exact():
+    w = si.weights(14336, 4096)
+    parts = [4096, 4096, 6144]
+    qr, spr = oracle.quant_weight_static(w, parts)
+    wd = dev(w)
+    sp = torch.empty(3, dtype=torch.float32, device="cuda")
+    q = torch.empty(14336, 4096, dtype=torch.uint8, device="cuda")
+    r0 = 0
+    for p, n in enumerate(parts):
+        fb.fp8bq_absmax_scale(wd[r0:r0 + n], sp[p:p + 1])
+        fb.fp8bq_static_quant_act(wd[r0:r0 + n], sp[p:p + 1], q[r0:r0 + n])
+        r0 += n
+    torch.cuda.synchronize()
+    assert np.array_equal(host(sp).view(np.uint32), spr.view(np.uint32))
+    assert np.array_equal(host(q), qr)
+
+
+def test_empty_batch_is_a_no_op():
+    x = torch.empty(0, 256, dtype=torch.bfloat16, device="cuda")
+    q = torch.empty(0, 256, dtype=torch.uint8, device="cuda")
+    s = torch.empty(0, 2, dtype=torch.float32, device="cuda")
+    fb.fp8bq_quant_act(x, q, s)
+    fb.fp8bq_mx_quant_act(x, q, s.view(torch.uint8))
