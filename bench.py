@@ -337,40 +337,51 @@ def run_e2e(fb, torch, dev, stream, layers, x, args, world, rank):
             "ms_per_step": round(ms_max / steps, 4)}
 
 
-def _time_ms(torch, stream, fn, reps, flush=None):
-    """Mean ms of fn() over reps launches, each timed alone with CUDA events."""
+def _time_back_to_back(torch, stream, fns, reps):
+    """Mean ms per launch of `reps` launches issued back to back, cycling through
+    `fns` (one per independent copy of the inputs, so that together they exceed
+    L2 and every launch streams its operands from HBM)."""
+    for f in fns:
+        f()
     for _ in range(3):
-        fn()
+        fns[0]()
     torch.cuda.synchronize()
-    tot = 0.0
-    for _ in range(reps):
-        if flush is not None:
-            flush.zero_()
-        s = torch.cuda.Event(enable_timing=True)
-        e = torch.cuda.Event(enable_timing=True)
-        s.record(stream)
-        fn()
-        e.record(stream)
-        e.synchronize()
-        tot += s.elapsed_time(e)
-    return tot / reps
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for i in range(reps):
+        fns[i % len(fns)]()
+    e.record(stream)
+    e.synchronize()
+    return s.elapsed_time(e) / reps
+
+
+def _copies(t, n):
+    return [t] + [t.clone() for _ in range(n - 1)]
 
 
 def run_extra(fb, torch, dev, stream, hbm_peak, fp8_peak):
-    """Decode and quantiser GB/s, MXFP8 and static TFLOPS (informational)."""
+    """Decode and quantiser GB/s, MXFP8 and static TFLOPS (informational).  Each
+    figure is the mean over back-to-back launches rotating through enough input
+    copies to exceed 1.5x the L2 size."""
     out = {}
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
 
     def to_dev(bits):
         return torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
 
-    # decode GEMM: weights streamed from HBM each launch
+    def n_sets(bytes_per_set):
+        return max(2, int(np.ceil(1.5 * l2 / bytes_per_set)))
+
+    # decode GEMM and linear: weights streamed from HBM each launch
     K = N = si.DECODE["K"]
     wb = to_dev(si.weights(N, K))
     qw = torch.empty(N, K, dtype=torch.uint8, device=dev)
     sw = torch.empty(N // 128, K // 128, dtype=torch.float32, device=dev)
     fb.fp8bq_quant_weight_block(wb, qw, sw)
     del wb
+    ns = n_sets(N * K)
+    qws, sws = _copies(qw, ns), _copies(sw, ns)
     dec = {}
     for M in si.DECODE["M_list"]:
         x = to_dev(si.activations(M, K))
@@ -379,37 +390,48 @@ def run_extra(fb, torch, dev, stream, hbm_peak, fp8_peak):
         fb.fp8bq_quant_act(x, q, sx)
         y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
         ws = fb.new_workspace(fb.OP_LINEAR, M, N, K, device=dev)
-        t = _time_ms(torch, stream, lambda: fb.fp8bq_gemm(q, sx, qw, sw, y, ws), 50, flush)
-        tl = _time_ms(torch, stream, lambda: fb.fp8bq_linear(x, qw, sw, y, ws), 50, flush)
+        g = [lambda i=i: fb.fp8bq_gemm(q, sx, qws[i], sws[i], y, ws) for i in range(ns)]
+        l = [lambda i=i: fb.fp8bq_linear(x, qws[i], sws[i], y, ws) for i in range(ns)]
+        t = _time_back_to_back(torch, stream, g, 60)
+        tl = _time_back_to_back(torch, stream, l, 60)
         gemm_bytes = N * K + sw.numel() * 4 + M * (K + K // 128 * 4) + 2 * M * N
         lin_bytes = N * K + sw.numel() * 4 + 2 * M * K + 2 * M * N
         dec[str(M)] = {"gemm_us": round(t * 1e3, 2),
                        "gemm_gbs": round(gemm_bytes / (t * 1e-3) / 1e9, 1),
                        "gemm_frac_hbm": round(gemm_bytes / (t * 1e-3) / 1e9 / hbm_peak, 4),
                        "linear_us": round(tl * 1e3, 2),
-                       "linear_gbs": round(lin_bytes / (tl * 1e-3) / 1e9, 1)}
+                       "linear_gbs": round(lin_bytes / (tl * 1e-3) / 1e9, 1),
+                       "linear_frac_hbm": round(lin_bytes / (tl * 1e-3) / 1e9 / hbm_peak, 4)}
     out["decode_N6144_K6144"] = dec
-    del qw, sw
+    del qw, sw, qws, sws
 
-    # quantisers at the three workload shapes
+    # quantisers at the workload shapes
     quant = {}
-    for name, (M, K) in {"group128_4096x6144": (4096, 6144)}.items():
-        x = to_dev(si.activations(M, K))
-        q = torch.empty(M, K, dtype=torch.uint8, device=dev)
-        sx = torch.empty(M, K // 128, dtype=torch.float32, device=dev)
-        t = _time_ms(torch, stream, lambda: fb.fp8bq_quant_act(x, q, sx), 50, flush)
-        b = M * K * 2 + M * K + M * (K // 128) * 4
-        quant[name] = {"us": round(t * 1e3, 2), "gbs": round(b / (t * 1e-3) / 1e9, 1),
-                       "frac_hbm": round(b / (t * 1e-3) / 1e9 / hbm_peak, 4)}
+    M, K = 4096, 6144
+    b = M * K * 2 + M * K + M * (K // 128) * 4
+    ns = n_sets(b)
+    xs = _copies(to_dev(si.activations(M, K)), ns)
+    qs = [torch.empty(M, K, dtype=torch.uint8, device=dev) for _ in range(ns)]
+    ss = [torch.empty(M, K // 128, dtype=torch.float32, device=dev) for _ in range(ns)]
+    t = _time_back_to_back(torch, stream, [lambda i=i: fb.fp8bq_quant_act(xs[i], qs[i], ss[i])
+                                           for i in range(ns)], 60)
+    quant["group128_4096x6144"] = {"us": round(t * 1e3, 2), "gbs": round(b / (t * 1e-3) / 1e9, 1),
+                                   "frac_hbm": round(b / (t * 1e-3) / 1e9 / hbm_peak, 4)}
+    del xs, qs, ss
     M, K = si.MXFP8["M"], si.MXFP8["K"]
-    xm = to_dev(si.activations(M, K))
-    qm = torch.empty(M, K, dtype=torch.uint8, device=dev)
-    um = torch.empty(M, K // 32, dtype=torch.uint8, device=dev)
-    t = _time_ms(torch, stream, lambda: fb.fp8bq_mx_quant_act(xm, qm, um), 50, flush)
     b = M * K * 3 + M * K // 32
+    ns = n_sets(b)
+    xm = to_dev(si.activations(M, K))
+    xms = _copies(xm, ns)
+    qms = [torch.empty(M, K, dtype=torch.uint8, device=dev) for _ in range(ns)]
+    ums = [torch.empty(M, K // 32, dtype=torch.uint8, device=dev) for _ in range(ns)]
+    t = _time_back_to_back(torch, stream, [lambda i=i: fb.fp8bq_mx_quant_act(xms[i], qms[i], ums[i])
+                                           for i in range(ns)], 60)
     quant["mx_2048x7168"] = {"us": round(t * 1e3, 2), "gbs": round(b / (t * 1e-3) / 1e9, 1),
                              "frac_hbm": round(b / (t * 1e-3) / 1e9 / hbm_peak, 4)}
     out["quant"] = quant
+    qm, um = qms[0], ums[0]
+    del xms
 
     # MXFP8 GEMM 2048 x 4096 x 7168
     N = si.MXFP8["N"]
@@ -418,16 +440,12 @@ def run_extra(fb, torch, dev, stream, hbm_peak, fp8_peak):
     uwm = torch.empty(N, K // 32, dtype=torch.uint8, device=dev)
     fb.fp8bq_mx_quant_act(wb, qwm, uwm)
     del wb
-    fb.fp8bq_mx_quant_act(xm, qm, um)
     ym = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
     wsm = fb.new_workspace(fb.OP_MX_GEMM, M, N, K, device=dev)
-    try:
-        t = _time_ms(torch, stream, lambda: fb.fp8bq_mx_gemm(qm, um, qwm, uwm, ym, wsm), 30, flush)
-        tf = 2.0 * M * N * K / (t * 1e-3) / 1e12
-        out["mx_gemm_2048x4096x7168"] = {"us": round(t * 1e3, 2), "tflops": round(tf, 1),
-                                         "frac_fp8": round(tf / fp8_peak, 4)}
-    except Exception as ex:  # reported, not hidden
-        out["mx_gemm_2048x4096x7168"] = {"error": str(ex)}
+    t = _time_back_to_back(torch, stream, [lambda: fb.fp8bq_mx_gemm(qm, um, qwm, uwm, ym, wsm)], 30)
+    tf = 2.0 * M * N * K / (t * 1e-3) / 1e12
+    out["mx_gemm_2048x4096x7168"] = {"us": round(t * 1e3, 2), "tflops": round(tf, 1),
+                                     "frac_fp8": round(tf / fp8_peak, 4)}
     del qwm, uwm
 
     # static per-tensor GEMM, N = 14336 (4096/4096/6144), K = 4096
@@ -441,6 +459,8 @@ def run_extra(fb, torch, dev, stream, hbm_peak, fp8_peak):
         fb.fp8bq_static_quant_act(wb[r0:r0 + n], sp[p:p + 1], qws[r0:r0 + n])
         r0 += n
     del wb
+    ns = n_sets(N * K)
+    qwss = _copies(qws, ns)
     s_x = torch.empty(1, dtype=torch.float32, device=dev)
     fb.fp8bq_absmax_scale(to_dev(si.calibration(si.STATIC["calib_rows"], K)), s_x)
     st = {}
@@ -450,8 +470,10 @@ def run_extra(fb, torch, dev, stream, hbm_peak, fp8_peak):
         fb.fp8bq_static_quant_act(xs, s_x, qs)
         ys = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
         wss = fb.new_workspace(fb.OP_STATIC_GEMM, M, N, K, device=dev)
-        t = _time_ms(torch, stream,
-                     lambda: fb.fp8bq_static_gemm(qs, s_x, qws, sp, parts, ys, wss), 30, flush)
+        t = _time_back_to_back(
+            torch, stream,
+            [lambda i=i: fb.fp8bq_static_gemm(qs, s_x, qwss[i], sp, parts, ys, wss)
+             for i in range(ns)], 30)
         tf = 2.0 * M * N * K / (t * 1e-3) / 1e12
         b = N * K + M * K + 2 * M * N
         st[str(M)] = {"us": round(t * 1e3, 2), "tflops": round(tf, 2),

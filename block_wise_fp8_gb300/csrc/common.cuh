@@ -75,7 +75,7 @@ WorkspaceLayout workspace_layout(int op, int64_t M, int64_t N, int64_t K);
 // Work decomposition of one GEMM launch.
 struct LaunchShape {
   int units;        // work units (output tiles, times splits in the swapped form)
-  int num_a_tiles;  // 128-row tiles of the A operand
+  int num_a_tiles;  // A-operand row tiles (128 rows; 256 for pair tiles)
   int splits;       // K splits per tile (swapped form only)
   int kps;          // K blocks per split
   int KB;           // ceil(K / 128)
@@ -85,15 +85,20 @@ struct LaunchShape {
 // K-major E4M3 matrix [rows, K] (pitch K bytes) as a TMA map with a
 // [box_rows x 128 B] box and 128-byte swizzling.
 bool make_kmajor_map(CUtensorMap *m, const void *base, int64_t rows, int64_t K, int box_rows);
+// The same through a small per-process cache of recently encoded maps.
+bool cached_kmajor_map(CUtensorMap *m, const void *base, int64_t rows, int64_t K,
+                       int box_rows);
 
 // Kernel variants, one translation unit each (instantiated from gemm_kernel.cuh).
-// `bn` selects the token tile of the swapped (decode) form: 16, 32 or 64.
-cudaError_t run_block_normal(const GemmArgs &a, const void *q, const void *w,
-                             const LaunchShape &sh, int grid, cudaStream_t st, int *status);
+// Pair (prefill) forms: `bn` is the weight-row tile, 192 or 256, and `grid` the
+// number of CTA pairs.  Swapped (decode) forms: `bn` is the token tile, 16, 32
+// or 64, and `grid` the number of CTAs.
+cudaError_t run_block_pair(int bn, const GemmArgs &a, const void *q, const void *w,
+                           const LaunchShape &sh, int grid, cudaStream_t st, int *status);
 cudaError_t run_block_swap(int bn, const GemmArgs &a, const void *q, const void *w,
                            const LaunchShape &sh, int grid, cudaStream_t st, int *status);
-cudaError_t run_tensor_normal(const GemmArgs &a, const void *q, const void *w,
-                              const LaunchShape &sh, int grid, cudaStream_t st, int *status);
+cudaError_t run_tensor_pair(int bn, const GemmArgs &a, const void *q, const void *w,
+                            const LaunchShape &sh, int grid, cudaStream_t st, int *status);
 cudaError_t run_tensor_swap(int bn, const GemmArgs &a, const void *q, const void *w,
                             const LaunchShape &sh, int grid, cudaStream_t st, int *status);
 cudaError_t run_mx_normal(const GemmArgs &a, const void *q, const void *w,

@@ -7,9 +7,10 @@
 //                1x128 activation groups).  The tensor core produces P_b, the FP32
 //                sum over one 128-wide K block, into TMEM; the epilogue warps read
 //                it back and promote it into FP32 registers with one FMA per
-//                element and K block (the per-128-K promotion of "GLM-5.3 推理全链路
-//                (十七)", DeepSeek-V3 Fig. 7 paragraph).  TMEM holds two partial
-//                buffers so the MMA of block b+1 overlaps the promotion of block b.
+//                element and K block (paired FP32 FMAs, two elements per
+//                instruction) -- the per-128-K promotion of "GLM-5.3 推理全链路
+//                (十七)", DeepSeek-V3 Fig. 7 paragraph.  TMEM holds ACCB partial
+//                buffers so the MMA runs up to ACCB K blocks ahead of the promotion.
 //   kModeTensor  y = (sum_k q w) * s_x * s_w[p(j)]: full-K accumulation in TMEM,
 //                one scale product per column in the epilogue.
 //   kModeMx      y = sum_g P_g * 2^(ua-127) * 2^(uw-127) with the block-scaled MMA
@@ -20,11 +21,18 @@
 // Roles (warp index):
 //   0            TMA producer: A and B tiles, 128 K per stage, 128B-swizzled.
 //   1            TMEM allocator and single-thread MMA issuer.
-//   2 .. 2+SFW   (MX only) scale-factor writers, one per TMEM lane quarter.
+//   2 .. 2+SFW   (MX only) scale-factor writers, one per TMEM lane quarter,
+//                loading the UE8M0 codes a few stages ahead.
 //   rest         epilogue: TMEM -> registers -> promotion -> BF16 -> global.
 //
-// Two tile orientations:
-//   normal  UMMA M = 128 tokens, UMMA N = BN weight rows (prefill).
+// Tile forms:
+//   pair    (prefill) a cluster of two CTAs on two SMs computes a 256 x BN tile
+//           with the pair MMA (tcgen05 cta_group::2): each CTA TMA-loads its own
+//           128 token rows and half of the BN weight rows, the even CTA issues the
+//           MMAs, each CTA's TMEM receives its 128 rows of the result and its own
+//           epilogue promotes and stores them.  Persistent clusters walk the tiles
+//           M-fastest so concurrent clusters share weight tiles in L2.
+//   normal  the same with one CTA: UMMA M = 128 tokens, UMMA N = BN weight rows.
 //   swap    UMMA M = 128 weight rows, UMMA N = BN tokens (decode, M <= 64), with
 //           split-K across CTAs and a deterministic last-CTA reduction in
 //           ascending split order.
@@ -34,6 +42,8 @@
 // TMEM and exits.
 #pragma once
 #include <cuda_bf16.h>
+
+#include <mutex>
 
 #include "common.cuh"
 #include "ptx.cuh"
@@ -50,23 +60,31 @@ constexpr uint32_t pow2_at_least(uint32_t v) {
   return p;
 }
 
-template <int MODE, bool SWAP, int BN, int STAGES, int EPI_WARPS>
+template <int MODE, bool SWAP, int BN, int STAGES, int EPI_WARPS, int ACCB, bool PAIR>
 struct Cfg {
+  static constexpr int kMmaM = PAIR ? 256 : 128;     // rows of the MMA (both CTAs)
+  static constexpr int kBrows = PAIR ? BN / 2 : BN;  // weight rows loaded by this CTA
   static constexpr int kSfWarps = (MODE == kModeMx) ? 4 : 0;
   static constexpr int kSfSlots = 4;
-  static constexpr int kSfColsA = 4;            // 128 rows / 32
+  static constexpr int kSfPrefetch = 4;          // stages of UE8M0 codes loaded ahead
+  static constexpr int kSfColsA = 4;             // 128 rows / 32
   static constexpr int kSfColsB = (MODE == kModeMx) ? BN / 32 : 4;
-  static constexpr int kSfSlotCols = 16;        // A at +0, B at +8
-  static constexpr int kThreads = 64 + 32 * (kSfWarps + EPI_WARPS);
+  static constexpr int kSfSlotCols = 16;         // A at +0, B at +8
+  // block tiles: two MMA-issuing warps take alternate K blocks (disjoint TMEM
+  // partial buffers), so one issues while the other waits on its barriers
+  static constexpr int kIssuers = (MODE == kModeBlock) ? 2 : 1;
+  static constexpr int kThreads = 32 * (1 + kIssuers + kSfWarps + EPI_WARPS);
   static constexpr int kEpiThreads = 32 * EPI_WARPS;
-  static constexpr int kEpiBase = 2 + kSfWarps;  // first epilogue warp
+  static constexpr int kEpiBase = 1 + kIssuers + kSfWarps;  // first epilogue warp
   static constexpr int kColGroups = EPI_WARPS / 4;
-  static constexpr int kCPT = BN / kColGroups;    // columns per epilogue thread
-  static constexpr int kCW = (kCPT % 32 == 0) ? 32 : 16;  // tcgen05.ld chunk width
-  static constexpr int kBatch = (kCPT < 64) ? kCPT : 64;  // columns per wait::ld
-  static constexpr int kBbytes = BN * 128;
+  static constexpr int kCPT = BN / kColGroups;   // columns per epilogue thread
+  // tcgen05.ld chunk width: 16 columns where a large FP32 accumulator lives in
+  // registers (block tiles with more than 64 columns per thread), otherwise 32
+  static constexpr int kCW =
+      (MODE == kModeBlock && !SWAP && kCPT > 64) ? 16 : (kCPT % 32 == 0) ? 32 : 16;
+  static constexpr int kBbytes = kBrows * 128;
   static constexpr int kStageBytes = kAbytes + kBbytes;
-  static constexpr int kAccCols = 2 * BN;  // double-buffered accumulators / partials
+  static constexpr int kAccCols = ACCB * BN;     // accumulators / partials
   static constexpr int kSfBase = kAccCols;
   static constexpr uint32_t kTmemCols =
       pow2_at_least(kAccCols + (MODE == kModeMx ? kSfSlots * kSfSlotCols : 0));
@@ -76,14 +94,21 @@ struct Cfg {
 
   static_assert(EPI_WARPS % 4 == 0, "epilogue warps must cover the 4 TMEM lane quarters");
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M = 128");
-  static_assert(kCPT % kCW == 0 && kBatch % kCW == 0 && kCPT % kBatch == 0, "chunking");
+  static_assert(kCPT % kCW == 0 && kCPT % 2 == 0, "chunking");
   static_assert(kTmemCols <= 512, "TMEM columns");
+  static_assert(STAGES <= 8 && ACCB <= 8, "barrier arrays");
+  static_assert(kIssuers == 1 || ACCB % kIssuers == 0, "each issuer owns whole buffers");
   static_assert(MODE != kModeMx || (!SWAP && BN % 32 == 0 && kSfColsB <= 8), "MX tiles");
+  static_assert(!PAIR || (!SWAP && MODE != kModeMx && kBrows % 8 == 0), "pair tiles");
+  static_assert(MODE != kModeBlock || SWAP || (128 % kCPT == 0 && BN % kCPT == 0),
+                "block tiles: each thread's columns lie in one 128-row weight block");
+  static_assert(!SWAP || (kCPT <= 64 && EPI_WARPS == 4),
+                "swapped tiles keep all token columns of a weight row in one thread");
 };
 
 struct SmemBarriers {
   uint64_t full[8], empty[8];
-  uint64_t tfull[2], tempty[2];
+  uint64_t tfull[8], tempty[8];
   uint64_t sf_full[4], sf_empty[4];
   uint64_t drain;
   uint32_t tmem_base;
@@ -100,6 +125,30 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   return *reinterpret_cast<uint32_t *>(&h);
 }
 
+// (c0, c1) = (a0 * b0 + c0, a1 * b1 + c1): one paired FP32 FMA, each lane an
+// IEEE round-to-nearest fused multiply-add.
+__device__ __forceinline__ void ffma2(float &c0, float &c1, float a0, float a1, float b0,
+                                      float b1) {
+  asm("{\n\t.reg .b64 ra, rb, rc;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "mov.b64 rc, {%0, %1};\n\t"
+      "fma.rn.f32x2 rc, ra, rb, rc;\n\t"
+      "mov.b64 {%0, %1}, rc;\n\t}"
+      : "+f"(c0), "+f"(c1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
+__device__ __forceinline__ void fmul2(float &a0, float &a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 ra, rb;\n\t"
+      "mov.b64 ra, {%0, %1};\n\t"
+      "mov.b64 rb, {%2, %3};\n\t"
+      "mul.rn.f32x2 ra, ra, rb;\n\t"
+      "mov.b64 {%0, %1}, ra;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "f"(b0), "f"(b1));
+}
+
 __device__ __forceinline__ void record_timeout(const GemmArgs &a) {
   if (a.status) atomicExch(a.status, kStatusTimeout);
 }
@@ -111,15 +160,36 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volati
   return __all_sync(0xffffffffu, ok);
 }
 
+template <int CW>
+__device__ __forceinline__ void tmem_ld_chunk(uint32_t taddr, uint32_t *r) {
+  if (CW == 32) tmem_ld32(taddr, r);
+  else tmem_ld16(taddr, r);
+}
+
 // Work unit -> (row0 of A, row0 of B, kb range, split, tile id for counters).
 struct Unit {
-  int a_row0, b_row0, kb0, kb1, split, tile;
+  int a_row0;       // first A row of this CTA (tokens, or weight rows when swapped)
+  int b_row0;       // first B row of the tile (the epilogue's first weight column)
+  int b_load_row0;  // first B row this CTA loads (pair tiles: its half)
+  int kb0, kb1, split, tile;
 };
 
-template <bool SWAP>
+template <bool SWAP, bool PAIR>
 __device__ __forceinline__ Unit decode_unit(int u, int num_a_tiles, int splits, int kps, int KB,
-                                            int bn) {
+                                            int bn, uint32_t rank) {
   Unit r;
+  if (PAIR) {
+    // A = tokens (256 per pair tile, 128 per CTA), B = bn weight rows (bn/2 per CTA)
+    const int mt = u % num_a_tiles, nt = u / num_a_tiles;
+    r.tile = u;
+    r.split = 0;
+    r.a_row0 = mt * 2 * kBM + static_cast<int>(rank) * kBM;
+    r.b_row0 = nt * bn;
+    r.b_load_row0 = r.b_row0 + static_cast<int>(rank) * (bn / 2);
+    r.kb0 = 0;
+    r.kb1 = KB;
+    return r;
+  }
   if (SWAP) {
     // A = weight rows (128 per tile), B = all tokens; units = tiles x splits
     r.tile = u / splits;
@@ -135,17 +205,60 @@ __device__ __forceinline__ Unit decode_unit(int u, int num_a_tiles, int splits, 
     r.a_row0 = mt * kBM;
     r.b_row0 = nt * bn;
   }
+  r.b_load_row0 = r.b_row0;
   r.kb0 = r.split * kps;
   r.kb1 = min(KB, r.kb0 + kps);
   return r;
 }
 
-template <int MODE, bool SWAP, int BN, int STAGES, int EPI_WARPS>
-__global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS>::kThreads, 1)
+// Four UE8M0 codes (K groups 4kb..4kb+3) of one row, packed little-endian.
+__device__ __forceinline__ uint32_t sf_word(const uint8_t *base, int row, int rows, int G,
+                                            int kb) {
+  if (row >= rows) return 0u;
+  const uint8_t *p = base + static_cast<int64_t>(row) * G + 4 * kb;
+  if ((G & 3) == 0) return __ldg(reinterpret_cast<const uint32_t *>(p));
+  uint32_t v = 0;
+#pragma unroll
+  for (int g = 0; g < 4; ++g)
+    if (4 * kb + g < G) v |= static_cast<uint32_t>(__ldg(p + g)) << (8 * g);
+  return v;
+}
+
+// Store `n` (multiple of 8 unless ragged) BF16 values of row m starting at column c0.
+template <int CNT>
+__device__ __forceinline__ void store_row(uint16_t *y, const float *v, int m, int c0,
+                                          const GemmArgs &a) {
+  uint16_t *yr = y + static_cast<int64_t>(m) * a.N;
+  if ((a.N & 7) == 0) {
+#pragma unroll
+    for (int j = 0; j < CNT; j += 8) {
+      if (c0 + j < a.N) {
+        uint4 q;
+        q.x = pack_bf16x2(v[j], v[j + 1]);
+        q.y = pack_bf16x2(v[j + 2], v[j + 3]);
+        q.z = pack_bf16x2(v[j + 4], v[j + 5]);
+        q.w = pack_bf16x2(v[j + 6], v[j + 7]);
+        *reinterpret_cast<uint4 *>(yr + c0 + j) = q;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < CNT; ++j)
+      if (c0 + j < a.N) {
+        __nv_bfloat16 h = __float2bfloat16_rn(v[j]);
+        yr[c0 + j] = *reinterpret_cast<uint16_t *>(&h);
+      }
+  }
+}
+
+// One CTA per SM.  Registers are split over the SM's four schedulers, so the
+// per-thread budget is set by the scheduler holding the most warps.
+template <int MODE, bool SWAP, int BN, int STAGES, int EPI_WARPS, int ACCB, bool PAIR>
+__global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, PAIR>::kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ GemmArgs args, const LaunchShape shape) {
-  using C = Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS>;
+  using C = Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, PAIR>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -158,21 +271,26 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS>::kThrea
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint64_t limit = args.wait_limit_ns;
+  // pair tiles: rank in the CTA pair; work is distributed per cluster
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const bool leader = rank == 0u;
+  const int cl_id = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int cl_num = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&bars->full[s], 1);
       mbar_init(&bars->empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < ACCB; ++b) {
       mbar_init(&bars->tfull[b], 1);
-      mbar_init(&bars->tempty[b], EPI_WARPS);
+      mbar_init(&bars->tempty[b], PAIR ? 2 * EPI_WARPS : EPI_WARPS);
     }
     for (int s = 0; s < C::kSfSlots; ++s) {
       mbar_init(&bars->sf_full[s], C::kSfWarps > 0 ? C::kSfWarps : 1);
       mbar_init(&bars->sf_empty[s], 1);
     }
-    mbar_init(&bars->drain, 1);
+    mbar_init(&bars->drain, C::kIssuers);
     bars->abort = 0;
     bars->is_last = 0;
     fence_mbar_init();
@@ -182,11 +300,17 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS>::kThrea
     tma_prefetch_desc(&tmB);
   }
   if (warp == 1) {
-    tmem_alloc(&bars->tmem_base, C::kTmemCols);
-    tmem_relinquish();
+    if (PAIR) {
+      tmem_alloc_pair(&bars->tmem_base, C::kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(&bars->tmem_base, C::kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync();  // the peer's barriers are initialised before any use
   tc_fence_after();
   const uint32_t tmem_base = bars->tmem_base;
 
@@ -195,44 +319,57 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS>::kThrea
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      int last_phase[STAGES];
-      for (int s = 0; s < STAGES; ++s) last_phase[s] = -1;
+      uint32_t issued = 0, phase_bits = 0;  // per stage: ever issued, last phase
       uint32_t it = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < shape.units; u += gridDim.x) {
-        const Unit w = decode_unit<SWAP>(u, shape.num_a_tiles, shape.splits, shape.kps, KB, BN);
+      for (int u = cl_id; ok && u < shape.units; u += cl_num) {
+        const Unit w = decode_unit<SWAP, PAIR>(u, shape.num_a_tiles, shape.splits, shape.kps, KB, BN, rank);
         for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
           if (!mbar_wait(&bars->empty[s], ph ^ 1u, abort_flag, limit)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&bars->full[s], C::kStageBytes);
-          tma_load_2d(sA + s * kAbytes, &tmA, &bars->full[s], kb * 128, w.a_row0);
-          tma_load_2d(sB + s * C::kBbytes, &tmB, &bars->full[s], kb * 128, w.b_row0);
-          last_phase[s] = static_cast<int>(ph);
+          if (PAIR) {
+            // both CTAs' bytes complete on the even CTA's barrier
+            if (leader) mbar_arrive_expect_tx(&bars->full[s], 2 * C::kStageBytes);
+            const uint32_t bar0 = mapa_shared(smem_u32(&bars->full[s]), 0);
+            tma_load_2d_pair(sA + s * kAbytes, &tmA, bar0, kb * 128, w.a_row0);
+            tma_load_2d_pair(sB + s * C::kBbytes, &tmB, bar0, kb * 128, w.b_load_row0);
+          } else {
+            mbar_arrive_expect_tx(&bars->full[s], C::kStageBytes);
+            tma_load_2d(sA + s * kAbytes, &tmA, &bars->full[s], kb * 128, w.a_row0);
+            tma_load_2d(sB + s * C::kBbytes, &tmB, &bars->full[s], kb * 128, w.b_load_row0);
+          }
+          issued |= 1u << s;
+          phase_bits = (phase_bits & ~(1u << s)) | (ph << s);
         }
       }
       if (!ok) {
         record_timeout(args);
-        // let every copy this thread issued land before the CTA's smem goes away
-        for (int s = 0; s < STAGES; ++s)
-          if (last_phase[s] >= 0) {
+        // let every copy issued land before shared memory goes away (pair tiles:
+        // the even CTA's barriers count both CTAs' copies; the odd CTA stays
+        // resident until the closing cluster barrier)
+        for (int s = 0; s < STAGES && (!PAIR || leader); ++s)
+          if ((issued >> s) & 1u) {
             uint32_t dummy = 0;
-            mbar_wait(&bars->full[s], static_cast<uint32_t>(last_phase[s]), &dummy, limit);
+            mbar_wait(&bars->full[s], (phase_bits >> s) & 1u, &dummy, limit);
           }
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      uint32_t it = 0, kit = 0, uit = 0, sfit = 0;
+  } else if (warp <= C::kIssuers) {
+    // ------------------------------------------------------------ MMA issuers
+    // Issuer `me` takes the K blocks with it % kIssuers == me (block tiles; every
+    // K block has its own TMEM partial buffer) -- with one issuer, all of them.
+    const uint32_t me = static_cast<uint32_t>(warp - 1);
+    if (lane == 0 && (!PAIR || leader)) {
+      uint32_t it = 0, uit = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < shape.units; u += gridDim.x, ++uit) {
-        const Unit w = decode_unit<SWAP>(u, shape.num_a_tiles, shape.splits, shape.kps, KB, BN);
+      for (int u = cl_id; ok && u < shape.units; u += cl_num, ++uit) {
+        const Unit w = decode_unit<SWAP, PAIR>(u, shape.num_a_tiles, shape.splits, shape.kps, KB, BN, rank);
         if (MODE != kModeBlock) {
-          const uint32_t b = uit & 1u, ph = (uit >> 1) & 1u;
+          const uint32_t b = uit % ACCB, ph = (uit / ACCB) & 1u;
           if (!mbar_wait(&bars->tempty[b], ph ^ 1u, abort_flag, limit)) {
             ok = false;
             break;
@@ -240,16 +377,17 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS>::kThrea
           tc_fence_after();
         }
         for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
+          if (C::kIssuers > 1 && it % C::kIssuers != me) continue;
           uint32_t d_tmem;
           if (MODE == kModeBlock) {
-            const uint32_t b = kit & 1u, ph = (kit >> 1) & 1u;
+            const uint32_t b = it % ACCB, ph = (it / ACCB) & 1u;
             if (!mbar_wait(&bars->tempty[b], ph ^ 1u, abort_flag, limit)) {
               ok = false;
               break;
             }
             d_tmem = tmem_base + b * BN;
           } else {
-            d_tmem = tmem_base + (uit & 1u) * BN;
+            d_tmem = tmem_base + (uit % ACCB) * BN;
           }
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
           if (!mbar_wait(&bars->full[s], ph, abort_flag, limit)) {
@@ -258,9 +396,8 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS>::kThrea
           }
           uint32_t sfslot = 0;
           if (MODE == kModeMx) {
-            sfslot = sfit % C::kSfSlots;
-            if (!mbar_wait(&bars->sf_full[sfslot], (sfit / C::kSfSlots) & 1u, abort_flag,
-                           limit)) {
+            sfslot = it % C::kSfSlots;
+            if (!mbar_wait(&bars->sf_full[sfslot], (it / C::kSfSlots) & 1u, abort_flag, limit)) {
               ok = false;
               break;
             }
@@ -276,86 +413,89 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS>::kThrea
               const uint32_t sfcol = tmem_base + C::kSfBase + sfslot * C::kSfSlotCols;
               umma_mxf8f6f4(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc_mxf8_e4m3(kBM, BN, k, k),
                             sfcol, sfcol + 8, acc);
+            } else if (PAIR) {
+              umma_f8f6f4_pair(d_tmem, adesc + 2 * k, bdesc + 2 * k,
+                               idesc_f8f6f4_e4m3(C::kMmaM, BN), acc);
             } else {
               umma_f8f6f4(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc_f8f6f4_e4m3(kBM, BN), acc);
             }
           }
-          umma_commit(&bars->empty[s]);
-          if (MODE == kModeMx) {
-            umma_commit(&bars->sf_empty[sfslot]);
-            ++sfit;
-          }
+          if (PAIR) umma_commit_pair(&bars->empty[s], 0x3);
+          else umma_commit(&bars->empty[s]);
+          if (MODE == kModeMx) umma_commit(&bars->sf_empty[sfslot]);
           if (MODE == kModeBlock) {
-            umma_commit(&bars->tfull[kit & 1u]);
-            ++kit;
+            if (PAIR) umma_commit_pair(&bars->tfull[it % ACCB], 0x3);
+            else umma_commit(&bars->tfull[it % ACCB]);
           }
         }
         if (!ok) break;
-        if (MODE != kModeBlock) umma_commit(&bars->tfull[uit & 1u]);
+        if (MODE != kModeBlock) {
+          if (PAIR) umma_commit_pair(&bars->tfull[uit % ACCB], 0x3);
+          else umma_commit(&bars->tfull[uit % ACCB]);
+        }
       }
       if (!ok) record_timeout(args);
-      // every MMA issued by this thread has completed once `drain` flips
-      umma_commit(&bars->drain);
+      // every MMA issued by both issuers has completed once `drain` flips
+      if (PAIR) umma_commit_pair(&bars->drain, 0x1);
+      else umma_commit(&bars->drain);
       uint32_t dummy = 0;
       mbar_wait(&bars->drain, 0, &dummy, limit);
     }
     __syncwarp();
   } else if (warp < C::kEpiBase) {
     // ------------------------------------------------------------ MX scale-factor writers
+    // (warps 1 + kIssuers .. kEpiBase - 1)
     // Warp with lane quarter q writes TMEM lanes 32q..32q+31.  Layout (replicated in
     // every quarter): lane i, column c of a slot holds the four UE8M0 codes of stage
     // kb (K groups 4kb..4kb+3, one byte per MMA, selected by the sf id) of tile row
-    // i + 32c.
+    // i + 32c.  The codes are loaded kSfPrefetch stages before they are written.
     if (MODE == kModeMx) {
+      constexpr int PD = C::kSfPrefetch;
+      constexpr int NA = C::kSfColsA, NB = C::kSfColsB;
       const int q = warp & 3;
       const int G = args.K / 32;
       uint32_t sfit = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < shape.units; u += gridDim.x) {
-        const Unit w = decode_unit<SWAP>(u, shape.num_a_tiles, shape.splits, shape.kps, KB, BN);
-        for (int kb = w.kb0; kb < w.kb1; ++kb, ++sfit) {
-          uint32_t va[C::kSfColsA], vb[C::kSfColsB];
+      uint32_t ring[PD][NA + NB];
+      for (int u = cl_id; ok && u < shape.units; u += cl_num) {
+        const Unit w = decode_unit<SWAP, PAIR>(u, shape.num_a_tiles, shape.splits, shape.kps, KB, BN, rank);
+        auto load = [&](int kb, uint32_t *dst) {
 #pragma unroll
-          for (int c = 0; c < C::kSfColsA; ++c) {
-            const int r = w.a_row0 + lane + 32 * c;
-            uint32_t v = 0;
-            if (r < args.M) {
-              const uint8_t *p = args.ux + static_cast<int64_t>(r) * G + 4 * kb;
+          for (int c = 0; c < NA; ++c) dst[c] = sf_word(args.ux, w.a_row0 + lane + 32 * c, args.M, G, kb);
 #pragma unroll
-              for (int g = 0; g < 4; ++g)
-                if (4 * kb + g < G) v |= static_cast<uint32_t>(__ldg(p + g)) << (8 * g);
+          for (int c = 0; c < NB; ++c)
+            dst[NA + c] = sf_word(args.uw, w.b_row0 + lane + 32 * c, args.N, G, kb);
+        };
+#pragma unroll
+        for (int i = 0; i < PD; ++i)
+          if (w.kb0 + i < w.kb1) load(w.kb0 + i, ring[i]);
+        for (int kb = w.kb0; ok && kb < w.kb1; kb += PD) {
+#pragma unroll
+          for (int i = 0; i < PD; ++i) {
+            const int k = kb + i;
+            if (k < w.kb1 && ok) {
+              const uint32_t slot = sfit % C::kSfSlots;
+              if (!warp_wait(&bars->sf_empty[slot], ((sfit / C::kSfSlots) & 1u) ^ 1u,
+                             abort_flag, limit)) {
+                ok = false;
+              } else {
+                tc_fence_after();
+                const uint32_t col = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
+                                     C::kSfBase + slot * C::kSfSlotCols;
+                tmem_st4(col, ring[i][0], ring[i][1], ring[i][2], ring[i][3]);
+#pragma unroll
+                for (int c = 0; c < NB; c += 4)
+                  tmem_st4(col + 8 + c, ring[i][NA + c], ring[i][NA + c + 1],
+                           ring[i][NA + c + 2], ring[i][NA + c + 3]);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->sf_full[slot]);
+                ++sfit;
+                if (k + PD < w.kb1) load(k + PD, ring[i]);
+              }
             }
-            va[c] = v;
           }
-#pragma unroll
-          for (int c = 0; c < C::kSfColsB; ++c) {
-            const int r = w.b_row0 + lane + 32 * c;
-            uint32_t v = 0;
-            if (r < args.N) {
-              const uint8_t *p = args.uw + static_cast<int64_t>(r) * G + 4 * kb;
-#pragma unroll
-              for (int g = 0; g < 4; ++g)
-                if (4 * kb + g < G) v |= static_cast<uint32_t>(__ldg(p + g)) << (8 * g);
-            }
-            vb[c] = v;
-          }
-          const uint32_t slot = sfit % C::kSfSlots;
-          if (!warp_wait(&bars->sf_empty[slot], ((sfit / C::kSfSlots) & 1u) ^ 1u, abort_flag,
-                         limit)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t col =
-              tmem_base + (static_cast<uint32_t>(32 * q) << 16) + C::kSfBase + slot * C::kSfSlotCols;
-          tmem_st4(col, va[0], va[1], va[2], va[3]);
-#pragma unroll
-          for (int c = 0; c < C::kSfColsB; c += 4)
-            tmem_st4(col + 8 + c, vb[c], vb[c + 1], vb[c + 2], vb[c + 3]);
-          tmem_st_wait();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bars->sf_full[slot]);
         }
       }
       if (!ok && lane == 0) record_timeout(args);
@@ -365,207 +505,225 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS>::kThrea
     // ------------------------------------------------------------ epilogue
     const int ew = warp - C::kEpiBase;
     const int quarter = warp & 3;
+    // tell the MMA issuer (the even CTA for pair tiles) that an accumulator is drained
+    auto release_acc = [&](uint64_t *bar) {
+      if (PAIR && !leader) mbar_arrive_cluster(mapa_shared(smem_u32(bar), 0));
+      else mbar_arrive(bar);
+    };
     const int cg = ew >> 2;  // column group
     const int et = ew * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(32 * quarter) << 16;
-    const int NB = (args.N + kBlockN - 1) / kBlockN;
+    const int NBLK = (args.N + kBlockN - 1) / kBlockN;
+    uint16_t *y = static_cast<uint16_t *>(args.y);
+    const uint16_t *bias = static_cast<const uint16_t *>(args.bias);
     uint32_t kit = 0, uit = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < shape.units; u += gridDim.x, ++uit) {
-      const Unit w = decode_unit<SWAP>(u, shape.num_a_tiles, shape.splits, shape.kps, KB, BN);
+    for (int u = cl_id; u < shape.units; u += cl_num, ++uit) {
+      const Unit w = decode_unit<SWAP, PAIR>(u, shape.num_a_tiles, shape.splits, shape.kps, KB, BN, rank);
       const int d_row = w.a_row0 + 32 * quarter + lane;  // row of D held by this thread
       const int col0 = cg * C::kCPT;                     // first D column of this thread
-      float acc[C::kCPT];
+
+      if (!SWAP) {
+        // ---------------- normal orientation: thread = one token row, kCPT weight columns
+        const int m = d_row;
+        const int nbase = w.b_row0 + col0;
+        if (MODE == kModeBlock) {
+          float acc[C::kCPT];
 #pragma unroll
-      for (int j = 0; j < C::kCPT; ++j) acc[j] = 0.0f;
-
-      if (MODE == kModeBlock && SWAP) {
-        // stage s_x[token][kb] for this unit's K range: sx_stage[(kb-kb0)*BN + token]
-        const int nkb = w.kb1 - w.kb0;
-        for (int e = et; e < nkb * BN; e += C::kEpiThreads) {
-          const int kb = w.kb0 + e / BN, t = e % BN;
-          float v = 0.0f;
-          if (t < args.M)
-            v = __ldg(args.sx + (args.sx_layout == 0
-                                     ? static_cast<int64_t>(t) * args.ldsx + kb
-                                     : static_cast<int64_t>(kb) * args.ldsx + t));
-          sx_stage[e] = v;
-        }
-        named_bar_sync(1, C::kEpiThreads);
-      }
-
-      if (MODE == kModeBlock) {
-        const bool row_ok = d_row < (SWAP ? args.N : args.M);
-        auto sx_at = [&](int kb) -> float {
-          if (!row_ok || kb >= w.kb1) return 0.0f;
-          return __ldg(args.sx + (args.sx_layout == 0
-                                      ? static_cast<int64_t>(d_row) * args.ldsx + kb
-                                      : static_cast<int64_t>(kb) * args.ldsx + d_row));
-        };
-        float sx_next = SWAP ? 0.0f : sx_at(w.kb0);
-        for (int kb = w.kb0; kb < w.kb1 && ok; ++kb, ++kit) {
-          const uint32_t b = kit & 1u, ph = (kit >> 1) & 1u;
-          const float sx_cur = sx_next;
-          if (!SWAP) sx_next = sx_at(kb + 1);
-          if (!warp_wait(&bars->tfull[b], ph, abort_flag, limit)) {
+          for (int j = 0; j < C::kCPT; ++j) acc[j] = 0.0f;
+          const bool row_ok = m < args.M;
+          // every column of this thread lies in one 128-row weight block (kCPT
+          // divides 128 and tiles start on multiples of kCPT), so the promotion
+          // factor of a K block is s_x[m][kb] * s_w[nb][kb]; both are fetched one
+          // K block ahead so no global load sits on the per-block critical path
+          const int nb = min(nbase / kBlockN, NBLK - 1);
+          const float *swrow = args.sw + static_cast<int64_t>(nb) * KB;
+          auto sx_at = [&](int kb) -> float {
+            if (!row_ok || kb >= w.kb1) return 0.0f;
+            return __ldg(args.sx + (args.sx_layout == 0
+                                        ? static_cast<int64_t>(m) * args.ldsx + kb
+                                        : static_cast<int64_t>(kb) * args.ldsx + m));
+          };
+          auto sw_at = [&](int kb) -> float { return kb < w.kb1 ? __ldg(swrow + kb) : 0.0f; };
+          float sx_next = sx_at(w.kb0), sw_next = sw_at(w.kb0);
+          for (int kb = w.kb0; kb < w.kb1 && ok; ++kb, ++kit) {
+            const uint32_t b = kit % ACCB, ph = (kit / ACCB) & 1u;
+            const float f = sx_next * sw_next;
+            if (!warp_wait(&bars->tfull[b], ph, abort_flag, limit)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t tbase = tmem_base + lane_base + b * BN + col0;
+#pragma unroll
+            for (int c = 0; c < C::kCPT / C::kCW; ++c) {
+              uint32_t r[C::kCW];
+              tmem_ld_chunk<C::kCW>(tbase + c * C::kCW, r);
+              tmem_ld_wait();
+              if (c == C::kCPT / C::kCW - 1) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) release_acc(&bars->tempty[b]);
+                // the next K block's scales are requested only after the release,
+                // which would otherwise wait for these loads to complete
+                sx_next = sx_at(kb + 1);
+                sw_next = sw_at(kb + 1);
+              }
+#pragma unroll
+              for (int j = 0; j < C::kCW; j += 2)
+                ffma2(acc[c * C::kCW + j], acc[c * C::kCW + j + 1], __uint_as_float(r[j]),
+                      __uint_as_float(r[j + 1]), f, f);
+            }
+          }
+          // all epilogue warps agree on the outcome before anything is stored
+          named_bar_sync(2, C::kEpiThreads);
+          if (*abort_flag) {
+            ok = false;
+            break;
+          }
+          if (m < args.M) {
+            if (bias) {
+#pragma unroll
+              for (int j = 0; j < C::kCPT; ++j)
+                if (nbase + j < args.N) acc[j] += bf16_bits_to_float(bias[nbase + j]);
+            }
+            store_row<C::kCPT>(y, acc, m, nbase, args);
+          }
+        } else {
+          // kModeTensor / kModeMx: one pass over the full-K accumulator
+          const uint32_t b = uit % ACCB, ph = (uit / ACCB) & 1u;
+          if (!warp_wait(&bars->tfull[b], ph, abort_flag, limit)) ok = false;
+          named_bar_sync(2, C::kEpiThreads);
+          if (*abort_flag || !ok) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t tbase = tmem_base + lane_base + b * BN + col0;
+          const float sxs = (MODE == kModeTensor) ? __ldg(args.sx_scalar) : 1.0f;
 #pragma unroll
-          for (int bt = 0; bt < C::kCPT / C::kBatch; ++bt) {
-            uint32_t r[C::kBatch];
-#pragma unroll
-            for (int c = 0; c < C::kBatch / C::kCW; ++c) {
-              if (C::kCW == 32) tmem_ld32(tbase + bt * C::kBatch + c * 32, r + c * 32);
-              else tmem_ld16(tbase + bt * C::kBatch + c * 16, r + c * 16);
-            }
+          for (int c = 0; c < C::kCPT / C::kCW; ++c) {
+            uint32_t r[C::kCW];
+            tmem_ld_chunk<C::kCW>(tbase + c * C::kCW, r);
             tmem_ld_wait();
-            if (bt == C::kCPT / C::kBatch - 1) {
+            if (c == C::kCPT / C::kCW - 1) {
               tc_fence_before();
               __syncwarp();
-              if (lane == 0) mbar_arrive(&bars->tempty[b]);
+              if (lane == 0) release_acc(&bars->tempty[b]);
             }
-            if (SWAP) {
-              // lanes are weight rows of one 128-row block: one s_w per K block
-              const float swv = __ldg(args.sw + static_cast<int64_t>(w.a_row0 / kBlockN) * KB + kb);
-              const float *sxk = sx_stage + (kb - w.kb0) * BN;
+            float v[C::kCW];
 #pragma unroll
-              for (int j = 0; j < C::kBatch; ++j) {
-                const int jj = bt * C::kBatch + j;
-                acc[jj] = fmaf(__uint_as_float(r[j]), sxk[col0 + jj] * swv, acc[jj]);
-              }
-            } else {
-#pragma unroll
-              for (int c = 0; c < C::kBatch / C::kCW; ++c) {
-                const int n = w.b_row0 + col0 + bt * C::kBatch + c * C::kCW;
-                const int nb = min(n / kBlockN, NB - 1);
-                const float f = sx_cur * __ldg(args.sw + static_cast<int64_t>(nb) * KB + kb);
-#pragma unroll
-                for (int j = 0; j < C::kCW; ++j) {
-                  const int jj = bt * C::kBatch + c * C::kCW + j;
-                  acc[jj] = fmaf(__uint_as_float(r[c * C::kCW + j]), f, acc[jj]);
-                }
-              }
-            }
-          }
-        }
-      } else if (ok) {
-        // kModeTensor / kModeMx: one read of the full-K accumulator
-        const uint32_t b = uit & 1u, ph = (uit >> 1) & 1u;
-        if (!warp_wait(&bars->tfull[b], ph, abort_flag, limit)) {
-          ok = false;
-        } else {
-          tc_fence_after();
-          const uint32_t tbase = tmem_base + lane_base + b * BN + col0;
-#pragma unroll
-          for (int bt = 0; bt < C::kCPT / C::kBatch; ++bt) {
-            uint32_t r[C::kBatch];
-#pragma unroll
-            for (int c = 0; c < C::kBatch / C::kCW; ++c) {
-              if (C::kCW == 32) tmem_ld32(tbase + bt * C::kBatch + c * 32, r + c * 32);
-              else tmem_ld16(tbase + bt * C::kBatch + c * 16, r + c * 16);
-            }
-            tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < C::kBatch; ++j) acc[bt * C::kBatch + j] = __uint_as_float(r[j]);
-          }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bars->tempty[b]);
-          if (MODE == kModeTensor) {
-            const float sxs = __ldg(args.sx_scalar);
-            if (SWAP) {
-              // one output partition per lane (weight row)
-              int p = 0;
-              while (p < args.n_parts - 1 && d_row >= args.part_end[p]) ++p;
-              const float f = sxs * __ldg(args.sw_part + p);
-#pragma unroll
-              for (int j = 0; j < C::kCPT; ++j) acc[j] *= f;
-            } else {
-#pragma unroll
-              for (int j = 0; j < C::kCPT; ++j) {
-                const int n = w.b_row0 + col0 + j;
+            for (int j = 0; j < C::kCW; ++j) {
+              v[j] = __uint_as_float(r[j]);
+              const int n = nbase + c * C::kCW + j;
+              if (MODE == kModeTensor) {
                 int p = 0;
                 while (p < args.n_parts - 1 && n >= args.part_end[p]) ++p;
-                acc[j] *= sxs * __ldg(args.sw_part + p);
+                v[j] *= sxs * __ldg(args.sw_part + p);
               }
+              if (bias && n < args.N) v[j] += bf16_bits_to_float(bias[n]);
             }
-          }
-        }
-      }
-
-      // all epilogue warps agree on the outcome before anything is stored
-      named_bar_sync(2, C::kEpiThreads);
-      if (*abort_flag) {
-        ok = false;
-        break;
-      }
-
-      const __nv_bfloat16 *bias = static_cast<const __nv_bfloat16 *>(args.bias);
-      uint16_t *y = static_cast<uint16_t *>(args.y);
-      if (!SWAP) {
-        // thread holds row d_row, columns b_row0 + col0 + [0, kCPT)
-        const int m = d_row;
-        const int nbase = w.b_row0 + col0;
-        if (m < args.M) {
-          if (bias) {
-#pragma unroll
-            for (int j = 0; j < C::kCPT; ++j)
-              if (nbase + j < args.N)
-                acc[j] += bf16_bits_to_float(reinterpret_cast<const uint16_t *>(bias)[nbase + j]);
-          }
-          uint16_t *yr = y + static_cast<int64_t>(m) * args.N;
-          if ((args.N & 7) == 0) {
-#pragma unroll
-            for (int j = 0; j < C::kCPT; j += 8) {
-              if (nbase + j < args.N) {
-                uint4 v;
-                v.x = pack_bf16x2(acc[j], acc[j + 1]);
-                v.y = pack_bf16x2(acc[j + 2], acc[j + 3]);
-                v.z = pack_bf16x2(acc[j + 4], acc[j + 5]);
-                v.w = pack_bf16x2(acc[j + 6], acc[j + 7]);
-                *reinterpret_cast<uint4 *>(yr + nbase + j) = v;
-              }
-            }
-          } else {
-#pragma unroll
-            for (int j = 0; j < C::kCPT; ++j)
-              if (nbase + j < args.N) {
-                __nv_bfloat16 h = __float2bfloat16_rn(acc[j]);
-                yr[nbase + j] = *reinterpret_cast<uint16_t *>(&h);
-              }
+            if (m < args.M) store_row<C::kCW>(y, v, m, nbase + c * C::kCW, args);
           }
         }
       } else {
-        // swap: thread holds weight row n = d_row, tokens col0 + [0, kCPT)
+        // ---------------- swapped orientation: thread = one weight row, all tokens
+        float acc[C::kCPT];
+#pragma unroll
+        for (int j = 0; j < C::kCPT; ++j) acc[j] = 0.0f;
+        if (MODE == kModeBlock) {
+          // stage s_x[token][kb] for this unit's K range: sx_stage[(kb-kb0)*BN + token]
+          const int nkb = w.kb1 - w.kb0;
+          for (int e = et; e < nkb * BN; e += C::kEpiThreads) {
+            const int kb = w.kb0 + e / BN, t = e % BN;
+            float v = 0.0f;
+            if (t < args.M)
+              v = __ldg(args.sx + (args.sx_layout == 0
+                                       ? static_cast<int64_t>(t) * args.ldsx + kb
+                                       : static_cast<int64_t>(kb) * args.ldsx + t));
+            sx_stage[e] = v;
+          }
+          named_bar_sync(1, C::kEpiThreads);
+          // lanes are weight rows of one 128-row block: one s_w per K block,
+          // fetched one K block ahead
+          const float *swrow = args.sw + static_cast<int64_t>(w.a_row0 / kBlockN) * KB;
+          float sw_next = __ldg(swrow + w.kb0);
+          for (int kb = w.kb0; kb < w.kb1 && ok; ++kb, ++kit) {
+            const uint32_t b = kit % ACCB, ph = (kit / ACCB) & 1u;
+            const float swv = sw_next;
+            if (!warp_wait(&bars->tfull[b], ph, abort_flag, limit)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t tbase = tmem_base + lane_base + b * BN;
+            uint32_t r[C::kCPT];
+#pragma unroll
+            for (int c = 0; c < C::kCPT / C::kCW; ++c)
+              tmem_ld_chunk<C::kCW>(tbase + c * C::kCW, r + c * C::kCW);
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) release_acc(&bars->tempty[b]);
+            if (kb + 1 < w.kb1) sw_next = __ldg(swrow + kb + 1);  // after the release
+            const float *sxk = sx_stage + (kb - w.kb0) * BN;
+#pragma unroll
+            for (int j = 0; j < C::kCPT; j += 2) {
+              float f0 = sxk[j], f1 = sxk[j + 1];
+              fmul2(f0, f1, swv, swv);
+              ffma2(acc[j], acc[j + 1], __uint_as_float(r[j]), __uint_as_float(r[j + 1]), f0,
+                    f1);
+            }
+          }
+        } else if (ok) {
+          const uint32_t b = uit % ACCB, ph = (uit / ACCB) & 1u;
+          if (!warp_wait(&bars->tfull[b], ph, abort_flag, limit)) {
+            ok = false;
+          } else {
+            tc_fence_after();
+            const uint32_t tbase = tmem_base + lane_base + b * BN;
+            uint32_t r[C::kCPT];
+#pragma unroll
+            for (int c = 0; c < C::kCPT / C::kCW; ++c)
+              tmem_ld_chunk<C::kCW>(tbase + c * C::kCW, r + c * C::kCW);
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) release_acc(&bars->tempty[b]);
+            // one output partition per lane (weight row)
+            int p = 0;
+            while (p < args.n_parts - 1 && d_row >= args.part_end[p]) ++p;
+            const float f = __ldg(args.sx_scalar) * __ldg(args.sw_part + p);
+#pragma unroll
+            for (int j = 0; j < C::kCPT; ++j) acc[j] = __uint_as_float(r[j]) * f;
+          }
+        }
+
+        named_bar_sync(2, C::kEpiThreads);
+        if (*abort_flag) {
+          ok = false;
+          break;
+        }
         const int n = d_row;
         const bool n_ok = n < args.N;
-        const float bv = (bias && n_ok)
-                             ? bf16_bits_to_float(reinterpret_cast<const uint16_t *>(bias)[n])
-                             : 0.0f;
+        const float bv = (bias && n_ok) ? bf16_bits_to_float(bias[n]) : 0.0f;
         if (shape.splits == 1) {
           if (n_ok) {
 #pragma unroll
-            for (int j = 0; j < C::kCPT; ++j) {
-              const int m = col0 + j;
-              if (m < args.M) {
+            for (int j = 0; j < C::kCPT; ++j)
+              if (j < args.M) {
                 __nv_bfloat16 h = __float2bfloat16_rn(acc[j] + bv);
-                y[static_cast<int64_t>(m) * args.N + n] = *reinterpret_cast<uint16_t *>(&h);
+                y[static_cast<int64_t>(j) * args.N + n] = *reinterpret_cast<uint16_t *>(&h);
               }
-            }
           }
         } else {
           // split-K: publish FP32 partials, the last CTA of the tile reduces them
           float *part = args.partials;
           if (n_ok) {
 #pragma unroll
-            for (int j = 0; j < C::kCPT; ++j) {
-              const int m = col0 + j;
-              if (m < args.M)
-                __stcg(part + (static_cast<int64_t>(w.split) * args.M + m) * args.N + n, acc[j]);
-            }
+            for (int j = 0; j < C::kCPT; ++j)
+              if (j < args.M)
+                __stcg(part + (static_cast<int64_t>(w.split) * args.M + j) * args.N + n, acc[j]);
           }
           __threadfence();
           named_bar_sync(2, C::kEpiThreads);
@@ -577,19 +735,30 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS>::kThrea
           if (bars->is_last) {
             __threadfence();
             if (n_ok) {
+              // ascending split order; all of one split's loads are in flight at once
+              float sum[C::kCPT];
 #pragma unroll
-              for (int j = 0; j < C::kCPT; ++j) {
-                const int m = col0 + j;
-                if (m < args.M) {
-                  float sum = 0.0f;
-                  for (int sp = 0; sp < shape.splits; ++sp)
-                    sum += (sp == w.split)
-                               ? acc[j]
-                               : __ldcg(part + (static_cast<int64_t>(sp) * args.M + m) * args.N + n);
-                  __nv_bfloat16 h = __float2bfloat16_rn(sum + bv);
-                  y[static_cast<int64_t>(m) * args.N + n] = *reinterpret_cast<uint16_t *>(&h);
+              for (int j = 0; j < C::kCPT; ++j) sum[j] = 0.0f;
+              for (int sp = 0; sp < shape.splits; ++sp) {
+                if (sp == w.split) {
+#pragma unroll
+                  for (int j = 0; j < C::kCPT; ++j) sum[j] += acc[j];
+                } else {
+                  const float *src = part + static_cast<int64_t>(sp) * args.M * args.N + n;
+                  float v[C::kCPT];
+#pragma unroll
+                  for (int j = 0; j < C::kCPT; ++j)
+                    v[j] = (j < args.M) ? __ldcg(src + static_cast<int64_t>(j) * args.N) : 0.0f;
+#pragma unroll
+                  for (int j = 0; j < C::kCPT; ++j) sum[j] += v[j];
                 }
               }
+#pragma unroll
+              for (int j = 0; j < C::kCPT; ++j)
+                if (j < args.M) {
+                  __nv_bfloat16 h = __float2bfloat16_rn(sum[j] + bv);
+                  y[static_cast<int64_t>(j) * args.N + n] = *reinterpret_cast<uint16_t *>(&h);
+                }
             }
             if (et == 0) args.counters[w.tile] = 0u;  // ready for the next call
           }
@@ -603,32 +772,71 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS>::kThrea
   // ------------------------------------------------------------ teardown
   tc_fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync();  // no CTA leaves while its peer may still signal it
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, C::kTmemCols);
+    if (PAIR) tmem_dealloc_pair(tmem_base, C::kTmemCols);
+    else tmem_dealloc(tmem_base, C::kTmemCols);
   }
 }
 
-template <int MODE, bool SWAP, int BN, int STAGES, int EPI_WARPS>
+// Launches one variant.  `grid` counts CTAs for single-CTA tiles and clusters
+// for pair tiles; for pair tiles it is clamped to the clusters the device can
+// hold at once, so the persistent grid is a single wave.
+template <int MODE, bool SWAP, int BN, int STAGES, int EPI_WARPS, int ACCB, bool PAIR>
 cudaError_t run(const GemmArgs &a, const void *q_act, const void *w, const LaunchShape &sh,
                 int grid, cudaStream_t st, int *status) {
-  using C = Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS>;
+  using C = Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, PAIR>;
   CUtensorMap ta, tb;
   const void *a_ptr = SWAP ? w : q_act;
   const void *b_ptr = SWAP ? q_act : w;
   const int64_t a_rows = SWAP ? a.N : a.M;
   const int64_t b_rows = SWAP ? a.M : a.N;
-  if (!make_kmajor_map(&ta, a_ptr, a_rows, a.K, kBM) ||
-      !make_kmajor_map(&tb, b_ptr, b_rows, a.K, BN)) {
+  if (!cached_kmajor_map(&ta, a_ptr, a_rows, a.K, kBM) ||
+      !cached_kmajor_map(&tb, b_ptr, b_rows, a.K, C::kBrows)) {
     *status = 4;  // FP8BQ_ERR_UNSUPPORTED: tensor map rejected
     return cudaSuccess;
   }
   const size_t smem = C::kFixedSmem + static_cast<size_t>(sh.sx_stage) * sizeof(float);
-  auto kern = fp8_gemm_kernel<MODE, SWAP, BN, STAGES, EPI_WARPS>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  auto kern = fp8_gemm_kernel<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, PAIR>;
+  // the opt-in shared-memory limit is raised once per variant (to the largest
+  // request it can see: the fixed part plus the biggest s_x staging buffer)
+  static std::once_flag attr_once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(attr_once, [&] {
+    const size_t max_smem = C::kFixedSmem + (SWAP ? size_t(BN) * 64 * sizeof(float) : 0);
+    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(max_smem));
+  });
+  cudaError_t e = attr_err;
   if (e != cudaSuccess) return e;
-  kern<<<grid, C::kThreads, smem, st>>>(ta, tb, a, sh);
+  if (!PAIR) {
+    kern<<<grid, C::kThreads, smem, st>>>(ta, tb, a, sh);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(C::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  static int max_clusters = 0;  // per variant; the library targets one device type
+  if (max_clusters == 0) {
+    cfg.gridDim = dim3(2 * grid, 1, 1);
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+    if (e != cudaSuccess) return e;
+    max_clusters = n > 0 ? n : 1;
+  }
+  const int clusters = grid < max_clusters ? grid : max_clusters;
+  cfg.gridDim = dim3(2 * clusters, 1, 1);
+  e = cudaLaunchKernelEx(&cfg, kern, ta, tb, a, sh);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

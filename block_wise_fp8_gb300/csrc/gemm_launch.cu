@@ -40,6 +40,42 @@ bool make_kmajor_map(CUtensorMap *m, const void *base, int64_t rows, int64_t K, 
   return r == CUDA_SUCCESS;
 }
 
+// Small cache of encoded tensor maps keyed by (base, rows, K, box rows): repeated
+// calls on the same tensors (every forward of a layer) skip the host-side encode.
+bool cached_kmajor_map(CUtensorMap *m, const void *base, int64_t rows, int64_t K,
+                       int box_rows) {
+  struct Entry {
+    const void *base;
+    int64_t rows, K;
+    int box;
+    CUtensorMap map;
+  };
+  constexpr int kEntries = 32;
+  static Entry cache[kEntries];
+  static int used = 0, next = 0;
+  static std::mutex mu;
+  {
+    std::lock_guard<std::mutex> g(mu);
+    for (int i = 0; i < used; ++i)
+      if (cache[i].base == base && cache[i].rows == rows && cache[i].K == K &&
+          cache[i].box == box_rows) {
+        *m = cache[i].map;
+        return true;
+      }
+  }
+  if (!make_kmajor_map(m, base, rows, K, box_rows)) return false;
+  std::lock_guard<std::mutex> g(mu);
+  Entry &e = cache[next];
+  e.base = base;
+  e.rows = rows;
+  e.K = K;
+  e.box = box_rows;
+  e.map = *m;
+  next = (next + 1) % kEntries;
+  if (used < kEntries) ++used;
+  return true;
+}
+
 // [status word | split-K tile counters | split-K FP32 partials | fused: Q | fused: scales]
 WorkspaceLayout workspace_layout(int op, int64_t M, int64_t N, int64_t K) {
   auto up = [](size_t v) { return (v + 255) / 256 * 256; };
@@ -95,18 +131,39 @@ int launch_gemm(const GemmArgs &a, const void *q_act, const void *w, const Devic
                     : run_tensor_swap(bn, a, q_act, w, sh, sh.units, st, &status);
     return status;
   }
-  // prefill: persistent CTAs over (M tiles x N tiles), M fastest
-  const int bn = (a.mode == kModeMx) ? 128 : 256;
-  sh.num_a_tiles = (a.M + 127) / 128;
-  const int n_tiles = (a.N + bn - 1) / bn;
+  if (a.mode == kModeMx) {
+    // MXFP8: single-CTA 128 x 128 tiles, persistent CTAs, M fastest
+    sh.num_a_tiles = (a.M + 127) / 128;
+    sh.splits = 1;
+    sh.kps = sh.KB;
+    sh.units = sh.num_a_tiles * ((a.N + 127) / 128);
+    sh.sx_stage = 0;
+    const int grid = sh.units < dev.num_sms ? sh.units : dev.num_sms;
+    *cuda_err = run_mx_normal(a, q_act, w, sh, grid, st, &status);
+    return status;
+  }
+  // prefill: CTA pairs over 256 x bn tiles, persistent clusters, M fastest.  The
+  // weight tile width bn is the one with the least (waves x bn), i.e. the
+  // smallest tail when the tiles are dealt to the pairs.
+  const int pairs = dev.num_sms / 2;
+  sh.num_a_tiles = (a.M + 255) / 256;
+  int best_bn = 256;
+  long best_cost = -1;
+  for (int bn : {256, 192}) {
+    const long units = static_cast<long>(sh.num_a_tiles) * ((a.N + bn - 1) / bn);
+    const long cost = (units + pairs - 1) / pairs * bn;
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best_bn = bn;
+    }
+  }
   sh.splits = 1;
   sh.kps = sh.KB;
-  sh.units = sh.num_a_tiles * n_tiles;
+  sh.units = sh.num_a_tiles * ((a.N + best_bn - 1) / best_bn);
   sh.sx_stage = 0;
-  const int grid = sh.units < dev.num_sms ? sh.units : dev.num_sms;
-  if (a.mode == kModeBlock) *cuda_err = run_block_normal(a, q_act, w, sh, grid, st, &status);
-  else if (a.mode == kModeTensor) *cuda_err = run_tensor_normal(a, q_act, w, sh, grid, st, &status);
-  else *cuda_err = run_mx_normal(a, q_act, w, sh, grid, st, &status);
+  const int grid = sh.units < pairs ? sh.units : pairs;
+  *cuda_err = (a.mode == kModeBlock) ? run_block_pair(best_bn, a, q_act, w, sh, grid, st, &status)
+                                     : run_tensor_pair(best_bn, a, q_act, w, sh, grid, st, &status);
   return status;
 }
 

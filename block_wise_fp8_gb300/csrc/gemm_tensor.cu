@@ -3,17 +3,18 @@
 
 namespace fp8bq {
 
-cudaError_t run_tensor_normal(const GemmArgs &a, const void *q, const void *w,
-                              const LaunchShape &sh, int grid, cudaStream_t st, int *status) {
-  return run<kModeTensor, false, 256, 4, 8>(a, q, w, sh, grid, st, status);
+cudaError_t run_tensor_pair(int bn, const GemmArgs &a, const void *q, const void *w,
+                            const LaunchShape &sh, int grid, cudaStream_t st, int *status) {
+  if (bn == 192) return run<kModeTensor, false, 192, 7, 8, 2, true>(a, q, w, sh, grid, st, status);
+  return run<kModeTensor, false, 256, 6, 8, 2, true>(a, q, w, sh, grid, st, status);
 }
 
 cudaError_t run_tensor_swap(int bn, const GemmArgs &a, const void *q, const void *w,
                             const LaunchShape &sh, int grid, cudaStream_t st, int *status) {
   switch (bn) {
-    case 16: return run<kModeTensor, true, 16, 8, 4>(a, q, w, sh, grid, st, status);
-    case 32: return run<kModeTensor, true, 32, 8, 4>(a, q, w, sh, grid, st, status);
-    default: return run<kModeTensor, true, 64, 8, 4>(a, q, w, sh, grid, st, status);
+    case 16: return run<kModeTensor, true, 16, 8, 4, 2, false>(a, q, w, sh, grid, st, status);
+    case 32: return run<kModeTensor, true, 32, 8, 4, 2, false>(a, q, w, sh, grid, st, status);
+    default: return run<kModeTensor, true, 64, 8, 4, 2, false>(a, q, w, sh, grid, st, status);
   }
 }
 

@@ -43,6 +43,23 @@ __device__ __forceinline__ float amax16(const float (&f)[16]) {
   return m;
 }
 
+// x / s rounded to binary32, bit-identical to __fdiv_rn(x, s), at the cost of one
+// multiply in almost every case.  r = RN(1/s), so t = RN(x * r) is within 2.5 ulp
+// of RN(x / s).  E4M3 rounding only changes at the midpoints between adjacent
+// E4M3 values, which in the E4M3 normal range (|t| >= 2^-6) are exactly the
+// binary32 values whose low 20 mantissa bits are 0x80000; binade edges are not
+// rounding boundaries.  So t and RN(x / s) encode to the same E4M3 code unless t
+// lies within 4 ulp of such a midpoint or in the E4M3 subnormal range, and only
+// then is the division performed.
+__device__ __forceinline__ float div_by_scale(float x, float s, float r) {
+  float t = __fmul_rn(x, r);
+  const uint32_t b = __float_as_uint(t) & 0x7FFFFFFFu;
+  const bool near_tie = ((b & 0xFFFFFu) - 0x7FFFCu) <= 8u;
+  const bool sub_e4m3 = b < 0x3C800000u && b != 0u;  // 0 < |t| < 2^-6
+  if (near_tie || sub_e4m3) t = __fdiv_rn(x, s);
+  return t;
+}
+
 // 16 binary32 values -> 16 E4M3 codes (RNE, saturating), packed little-endian.
 __device__ __forceinline__ uint4 to_e4m3x16(const float (&t)[16]) {
   uint32_t w[4];
@@ -84,9 +101,10 @@ __global__ void __launch_bounds__(kThreads) quant_group128_kernel(
   amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
   amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
   const float sg = __fdiv_rn(fmaxf(amax, kFloor), 448.0f);
+  const float rg = __frcp_rn(sg);
   float t[16];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) t[i] = __fdiv_rn(f[i], sg);
+  for (int i = 0; i < 16; ++i) t[i] = div_by_scale(f[i], sg, rg);
   const uint4 out = to_e4m3x16(t);
   if (valid) *reinterpret_cast<uint4 *>(q + row * K + k) = out;
   if (in_range && sub == 0) {
@@ -147,13 +165,14 @@ __global__ void __launch_bounds__(kThreads) quant_static_kernel(const uint8_t *_
   const int64_t row = cid / C;
   const int k = static_cast<int>(cid - row * C) * 16;
   const float sv = __ldg(s_ptr);
+  const float rv = __frcp_rn(sv);
   const uint8_t *p = x + row * ldx_bytes + static_cast<int64_t>(k) * 2;
   uint4 v[2] = {ld_stream(p), ld_stream(p + 16)};
   float f[16];
   unpack16(v, f);
   float t[16];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) t[i] = __fdiv_rn(f[i], sv);
+  for (int i = 0; i < 16; ++i) t[i] = div_by_scale(f[i], sv, rv);
   *reinterpret_cast<uint4 *>(q + row * K + k) = to_e4m3x16(t);
 }
 

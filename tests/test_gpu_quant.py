@@ -66,19 +66,46 @@ def test_quant_group_special_values():
     assert np.array_equal(q, qr)
 
 
-def test_static_quant_every_finite_bf16_value():
-    """s = 1: q = RNE_sat(x) for all 2^16 BF16 patterns except Inf/NaN, which checks
-    the hardware conversion (saturation, subnormals, ties, signed zero) against
-    the oracle's encoder exhaustively over BF16 inputs."""
+@pytest.mark.parametrize("amax", [3.0, 5.0, 7.0, 100.5, 0.3, 1e-30, 2.5e36])
+def test_quant_group_every_bf16_below_amax(amax):
+    """Every group has max |x| = amax (so the same non-power-of-two scale) and the
+    other 127 slots sweep every BF16 value of smaller magnitude, both signs: all
+    reachable quotients x / s, including those next to E4M3 rounding ties, must
+    give the codes of an IEEE binary32 division."""
+    a_bits = si.f32_to_bf16_bits(np.float32([amax]))[0]
+    a = si.bf16_bits_to_f32(np.array([a_bits]))[0]
+    pats = np.arange(1 << 15, dtype=np.uint32).astype(np.uint16)     # positive patterns
+    vals = si.bf16_bits_to_f32(pats)
+    pats = pats[np.isfinite(vals) & (vals <= a)]
+    pats = np.concatenate([pats, pats | 0x8000])
+    n_groups = -(-len(pats) // 127)
+    body = np.zeros(n_groups * 127, np.uint16)
+    body[:len(pats)] = pats
+    x = np.empty((n_groups, 128), np.uint16)
+    x[:, 0] = a_bits
+    x[:, 1:] = body.reshape(n_groups, 127)
+    x = x.reshape(-1, 1024) if n_groups % 8 == 0 else x
+    q, s = _gpu_quant_group(x)
+    qr, sr = oracle.quant_group(x)
+    assert np.array_equal(s.view(np.uint32), sr.view(np.uint32))
+    assert np.array_equal(q, qr)
+
+
+@pytest.mark.parametrize("scale", [1.0, 0.0137, 3.3])
+def test_static_quant_every_finite_bf16_value(scale):
+    """q = RNE_sat(x / s) for all 2^16 BF16 patterns except Inf/NaN.  With s = 1 this
+    checks the hardware conversion (saturation, subnormals, ties, signed zero)
+    against the oracle's encoder exhaustively over BF16 inputs; the other scales
+    check every quotient the division can produce."""
     pats = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
     pats = pats[((pats >> 7) & 0xFF) != 0xFF]
     pats = np.concatenate([pats, np.zeros((-len(pats)) % 16, np.uint16)])
     x = pats.reshape(-1, 16 * 64) if len(pats) % (16 * 64) == 0 else pats.reshape(-1, 16)
-    sx = torch.ones(1, dtype=torch.float32, device="cuda")
+    sx = torch.full((1,), scale, dtype=torch.float32, device="cuda")
     q = torch.empty(x.shape, dtype=torch.uint8, device="cuda")
     fb.fp8bq_static_quant_act(dev(x), sx, q)
     torch.cuda.synchronize()
-    assert np.array_equal(host(q), oracle.quant_static(x, 1.0))
+    assert np.array_equal(host(q), oracle.quant_static(x, np.float32(scale)))
 
 
 @pytest.mark.parametrize("M,K", [(2048, 7168), (5, 96), (64, 7168), (1, 32)])
