@@ -202,19 +202,19 @@ def run_ours(args):
         ws = fb.new_workspace(fb.OP_GEMM, M, N, K, device=dev)
         layers.append(dict(N=N, qw=qw, sw=sw, y=y, ws=ws))
     q = torch.empty(M, K, dtype=torch.uint8, device=dev)
-    sx = torch.empty(-(-K // 128), -(-M // 4) * 4, dtype=torch.float32, device=dev)
+    sx = torch.empty(M, -(-K // 128), dtype=torch.float32, device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     flops_step = sum(2.0 * M * K * L["N"] for L in layers)
 
     def step(ev=None):
-        # A1: group-128 activation quantisation, column-major scales
-        fb.fp8bq_quant_act(x, q, sx, fb.SCALE_COL_MAJOR)
+        # A1: group-128 activation quantisation (row-major scales)
+        fb.fp8bq_quant_act(x, q, sx, fb.SCALE_ROW_MAJOR)
         for i, L in enumerate(layers):
             if ev is not None:
                 ev[i][0].record(stream)
             # A2: block-scaled GEMM
             fb.fp8bq_gemm(q, sx, L["qw"], L["sw"], L["y"], L["ws"],
-                          s_layout=fb.SCALE_COL_MAJOR)
+                          s_layout=fb.SCALE_ROW_MAJOR)
             if ev is not None:
                 ev[i][1].record(stream)
 
@@ -281,7 +281,7 @@ def run_ours(args):
                 "W ~ N(0,0.02) quantised to E4M3 with 128x128 FP32 scales)",
         "config": {"workload": f"prefill block-FP8 linear: X[{M},{K}] BF16 -> N in "
                                f"{list(PREFILL_NS)}, BF16 out",
-                   "step": "group-128 quant (col-major scales) + block-scaled GEMM per N",
+                   "step": "group-128 quant (row-major scales) + block-scaled GEMM per N",
                    "global_batch": M * world, "per_gpu_tokens": M,
                    "parallelism": f"replicas x{world} (independent token batches)",
                    "l2": "flushed between timed steps (256 MiB write)"},

@@ -292,11 +292,12 @@ int fp8bq_linear(const void *x, int64_t ldx, const void *w, const float *s_w, co
   const WorkspaceLayout L = workspace_layout(FP8BQ_OP_LINEAR, M, N, K);
   uint8_t *q = static_cast<uint8_t *>(ws) + L.q;
   float *s = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + L.s);
-  // column-major scales: per K block the 128 rows of a tile are contiguous
-  launch_quant_group(x, M, K, ldx, q, s, FP8BQ_SCALE_COL_MAJOR, st);
+  // row-major scales: each epilogue thread walks its own row's scales, which
+  // stay in L1 across consecutive K blocks
+  launch_quant_group(x, M, K, ldx, q, s, FP8BQ_SCALE_ROW_MAJOR, st);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);
-  return gemm_block_impl(q, s, FP8BQ_SCALE_COL_MAJOR, w, s_w, bias, y, M, N, K, ws,
+  return gemm_block_impl(q, s, FP8BQ_SCALE_ROW_MAJOR, w, s_w, bias, y, M, N, K, ws,
                          FP8BQ_OP_LINEAR, st, dev);
 }
 

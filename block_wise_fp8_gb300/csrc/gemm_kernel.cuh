@@ -612,14 +612,29 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
               if (lane == 0) release_acc(&bars->tempty[b]);
             }
             float v[C::kCW];
+            // per-tensor scales: one output partition covers the whole chunk
+            // unless the chunk straddles a partition boundary (then per column)
+            const int n0c = nbase + c * C::kCW;
+            float fchunk = 1.0f;
+            bool uniform = true;
+            if (MODE == kModeTensor) {
+              int p = 0;
+              while (p < args.n_parts - 1 && n0c >= args.part_end[p]) ++p;
+              uniform = (p == args.n_parts - 1) || (n0c + C::kCW <= args.part_end[p]);
+              fchunk = sxs * __ldg(args.sw_part + p);
+            }
 #pragma unroll
             for (int j = 0; j < C::kCW; ++j) {
               v[j] = __uint_as_float(r[j]);
-              const int n = nbase + c * C::kCW + j;
+              const int n = n0c + j;
               if (MODE == kModeTensor) {
-                int p = 0;
-                while (p < args.n_parts - 1 && n >= args.part_end[p]) ++p;
-                v[j] *= sxs * __ldg(args.sw_part + p);
+                if (uniform) {
+                  v[j] *= fchunk;
+                } else {
+                  int p = 0;
+                  while (p < args.n_parts - 1 && n >= args.part_end[p]) ++p;
+                  v[j] *= sxs * __ldg(args.sw_part + p);
+                }
               }
               if (bias && n < args.N) v[j] += bf16_bits_to_float(bias[n]);
             }

@@ -92,7 +92,7 @@ WorkspaceLayout workspace_layout(int op, int64_t M, int64_t N, int64_t K) {
   const bool fused = (op == 1 || op == 3 || op == 5);
   if (fused) off += up(static_cast<size_t>(M) * K);
   L.s = off;
-  if (op == 1) off += up(static_cast<size_t>(KB) * ((M + 3) / 4 * 4) * 4);
+  if (op == 1) off += up(static_cast<size_t>(M) * KB * 4);
   if (op == 3) off += up(static_cast<size_t>(M) * (K / 32));
   L.total = off;
   return L;
