@@ -26,7 +26,8 @@ __all__ = [
     "OP_MX_GEMM", "OP_MX_LINEAR", "OP_STATIC_GEMM", "OP_STATIC_LINEAR", "library_path",
     "fp8bq_version", "fp8bq_status_string", "fp8bq_last_cuda_error",
     "fp8bq_workspace_bytes", "fp8bq_workspace_init", "fp8bq_poll_status",
-    "fp8bq_quant_act", "fp8bq_gemm", "fp8bq_linear", "fp8bq_mx_quant_act",
+    "fp8bq_quant_act", "fp8bq_gemm", "fp8bq_linear", "fp8bq_gemm_noalloc",
+    "NOALLOC_SCRATCH_BYTES", "fp8bq_mx_quant_act",
     "fp8bq_mx_gemm", "fp8bq_mx_linear", "fp8bq_static_quant_act", "fp8bq_static_gemm",
     "fp8bq_static_linear", "fp8bq_quant_weight_block", "fp8bq_absmax_scale",
     "new_workspace",
@@ -35,6 +36,7 @@ __all__ = [
 SCALE_ROW_MAJOR, SCALE_COL_MAJOR = 0, 1
 (OP_GEMM, OP_LINEAR, OP_MX_GEMM, OP_MX_LINEAR, OP_STATIC_GEMM,
  OP_STATIC_LINEAR) = range(6)
+NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024      # FP8BQ_NOALLOC_SCRATCH_BYTES
 
 STATUS_NAMES = {0: "FP8BQ_OK", 1: "FP8BQ_ERR_NULL", 2: "FP8BQ_ERR_SHAPE",
                 3: "FP8BQ_ERR_ALIGN", 4: "FP8BQ_ERR_UNSUPPORTED", 5: "FP8BQ_ERR_ARCH",
@@ -72,6 +74,7 @@ def _load():
         "fp8bq_quant_act": (I32, [P, I64, I64, I64, P, P, I32, P]),
         "fp8bq_gemm": (I32, [P, P, I32, P, P, P, P, I64, I64, I64, P, SZ, P]),
         "fp8bq_linear": (I32, [P, I64, P, P, P, P, I64, I64, I64, P, SZ, P]),
+        "fp8bq_gemm_noalloc": (I32, [P, P, I32, P, P, P, P, I64, I64, I64, P]),
         "fp8bq_mx_quant_act": (I32, [P, I64, I64, I64, P, P, P]),
         "fp8bq_mx_gemm": (I32, [P, P, P, P, P, P, I64, I64, I64, P, SZ, P]),
         "fp8bq_mx_linear": (I32, [P, I64, P, P, P, P, I64, I64, I64, P, SZ, P]),
@@ -175,6 +178,17 @@ def fp8bq_gemm(q, s_x, w, s_w, y, ws, bias=None, s_layout: int = SCALE_ROW_MAJOR
     _check(_lib.fp8bq_gemm(_ptr(q), _ptr(s_x), s_layout, _ptr(w), _ptr(s_w), _ptr(bias),
                            _ptr(y), M, N, K, _ptr(ws), _nbytes(ws), _stream(stream)),
            "fp8bq_gemm")
+
+
+def fp8bq_gemm_noalloc(q, s_x, w, s_w, y, bias=None, s_layout: int = SCALE_ROW_MAJOR,
+                       stream=None):
+    """fp8bq_gemm on the library's fixed device scratch instead of a workspace
+    (for callers that may not allocate device memory); see include/fp8bq.h."""
+    M, K = q.shape
+    N = w.shape[0]
+    _check(_lib.fp8bq_gemm_noalloc(_ptr(q), _ptr(s_x), s_layout, _ptr(w), _ptr(s_w),
+                                   _ptr(bias), _ptr(y), M, N, K, _stream(stream)),
+           "fp8bq_gemm_noalloc")
 
 
 def fp8bq_linear(x, w, s_w, y, ws, bias=None, stream=None):

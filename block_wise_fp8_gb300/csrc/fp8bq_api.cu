@@ -188,6 +188,39 @@ int check_parts(const int64_t *parts, int n_parts, int64_t N) {
 
 }  // namespace
 
+// ------------------------------------------------------------------ no-allocation scratch
+//
+// Scratch of fp8bq_gemm_noalloc: a fixed array in this library's device image.
+// Each device gets its own copy when the library's module is loaded on it, and
+// keeps it until the process exits.  On the host this name is only a handle
+// for cudaGetSymbolAddress, never an address to pass to a kernel.
+static __device__ __align__(256) uint8_t fp8bq_noalloc_scratch[FP8BQ_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+struct ScratchSlot {
+  std::once_flag once;
+  void *ptr;
+  cudaError_t err;
+};
+ScratchSlot g_scratch[kMaxDevices];
+
+// Device address of the scratch on device `dev`, looked up by the first call
+// on that device, with that device current (the caller's current device).
+// A failed look-up is remembered and returned by every later call.
+int noalloc_scratch(int dev, void **out) {
+  ScratchSlot &s = g_scratch[dev];
+  std::call_once(s.once, [&] {
+    s.ptr = nullptr;
+    s.err = cudaGetSymbolAddress(&s.ptr, fp8bq_noalloc_scratch);
+  });
+  if (s.err != cudaSuccess) return cuda_fail(s.err);
+  *out = s.ptr;
+  return FP8BQ_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 int fp8bq_version(void) { return 10000; }
@@ -442,6 +475,41 @@ int fp8bq_absmax_scale(const void *x, int64_t rows, int64_t K, int64_t ldx, floa
   launch_absmax_scale(x, rows, K, ldx, s, dev.num_sms, static_cast<cudaStream_t>(stream));
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? FP8BQ_OK : cuda_fail(e);
+}
+
+// ------------------------------------------------------------------ no-allocation GEMM
+
+// fp8bq_gemm with the library's fixed scratch array in place of a caller
+// workspace: same checks, same kernels, same results.  Allocates nothing.
+int fp8bq_gemm_noalloc(const void *q, const float *s_x, int s_layout, const void *w,
+                       const float *s_w, const void *bias, void *y, int64_t M, int64_t N,
+                       int64_t K, void *stream) {
+  if (M == 0) return empty_batch(K, N);
+  if (!q || !s_x || !w || !s_w || !y) return FP8BQ_ERR_NULL;
+  RETURN_IF(check_gemm_shape(M, N, K, 16));
+  if (s_layout != FP8BQ_SCALE_ROW_MAJOR && s_layout != FP8BQ_SCALE_COL_MAJOR)
+    return FP8BQ_ERR_UNSUPPORTED;
+  if (!aligned(q, 16) || !aligned(w, 16) || !aligned(y, 16) || !aligned(s_x, 4) ||
+      !aligned(s_w, 4) || !aligned(bias, 2))
+    return FP8BQ_ERR_ALIGN;
+  // the scratch is laid out exactly like an fp8bq_gemm workspace of this shape
+  const WorkspaceLayout L = workspace_layout(FP8BQ_OP_GEMM, M, N, K);
+  if (L.total > static_cast<size_t>(FP8BQ_NOALLOC_SCRATCH_BYTES)) return FP8BQ_ERR_WORKSPACE;
+  DeviceInfo dev;
+  RETURN_IF(device_info(&dev));
+  int d = 0;
+  cudaError_t e = cudaGetDevice(&d);
+  if (e != cudaSuccess) return cuda_fail(e);
+  void *scratch = nullptr;
+  RETURN_IF(noalloc_scratch(d, &scratch));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // The status word and the split-K tile counters must start at zero; the
+  // previous call may have left them set (a timed-out wait).  The FP32
+  // partials behind them are always written before they are read.
+  e = cudaMemsetAsync(scratch, 0, L.partials, st);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return gemm_block_impl(q, s_x, s_layout, w, s_w, bias, y, M, N, K, scratch, FP8BQ_OP_GEMM, st,
+                         dev);
 }
 
 }  // extern "C"

@@ -131,6 +131,43 @@ FP8BQ_API int fp8bq_linear(const void *x, int64_t ldx, const void *w,
                            int64_t M, int64_t N, int64_t K, void *ws,
                            size_t ws_bytes, void *stream);
 
+/* Size of the fixed scratch array behind fp8bq_gemm_noalloc (16 MiB per device). */
+#define FP8BQ_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+/* fp8bq_gemm without a caller workspace.  The pages have no counterpart: this
+ * entry point exists for callers that cannot hand the library device memory of
+ * its own -- an operator interface whose argument list is fixed and has no
+ * room for a workspace, or a runtime that plans all device memory ahead of time
+ * and forbids allocations (cudaMalloc, a framework's caching allocator) inside
+ * its operators.  Arguments, layouts, checks and results are those of
+ * fp8bq_gemm; the caller still owns q, s_x, w, s_w, bias and y.
+ *
+ * In place of `ws` it uses one array of FP8BQ_NOALLOC_SCRATCH_BYTES that the
+ * library holds in device memory on every GPU that loads it, until the process
+ * exits; it calls no allocating routine.
+ *  - Limit: shapes whose fp8bq_workspace_bytes(FP8BQ_OP_GEMM, M, N, K) exceeds
+ *    FP8BQ_NOALLOC_SCRATCH_BYTES are rejected with FP8BQ_ERR_WORKSPACE before
+ *    anything is launched.  For M > 64 that is a status word and one counter
+ *    per 128 output columns, so every N up to about 5 * 10^8 fits; for
+ *    M <= 64 it adds FP32 split-K partials (32 * M * N bytes), so M * N must
+ *    stay below about 524,000: every M <= 64 at N = 6144, M <= 16 at N = 24576.
+ *  - Set-up: the first call on a device, with that device current, looks up
+ *    the array's device address (cudaGetSymbolAddress) and keeps it; make that
+ *    first call before any stream capture begins.  A failed look-up returns
+ *    FP8BQ_ERR_CUDA then and on every later call on that device.
+ *  - Each call clears the array's status word and split-K counters on `stream`
+ *    (cudaMemsetAsync) before its kernel.  Every call on a device shares the one
+ *    array, which keeps what the last call left there: calls that may overlap
+ *    on the GPU (different streams without ordering between them) race on it
+ *    and give undefined results.  Calls on one stream are ordered and safe.
+ *  - A device-side wait that runs out leaves the outputs undefined and is not
+ *    reported to the host (there is no workspace to poll); the next call
+ *    clears the status word. */
+FP8BQ_API int fp8bq_gemm_noalloc(const void *q, const float *s_x, int s_layout,
+                                 const void *w, const float *s_w,
+                                 const void *bias, void *y, int64_t M,
+                                 int64_t N, int64_t K, void *stream);
+
 /* ------------------------------------------------ MXFP8 path ([1,32], UE8M0) */
 
 /* MXFP8 activation quantisation: per 32-channel group, e = ceil(log2(max(amax,

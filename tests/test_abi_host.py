@@ -93,6 +93,17 @@ def test_gemm_validation():
     assert call(M=0) == 0
 
 
+def test_gemm_noalloc_validation():
+    def call(q=P(A), lay=0, w=P(A), bias=None, M=16, N=384, K=256):
+        return L.fp8bq_gemm_noalloc(q, P(A), lay, w, P(A), bias, P(A), M, N, K, None)
+    assert call(q=None) == 1
+    assert call(K=100) == 3
+    assert call(lay=2) == 4
+    assert call(bias=P(A + 1)) == 3
+    assert call(M=64, N=24576, K=6144) == 6      # split-K partials exceed the scratch
+    assert call(M=0) == 0
+
+
 def test_mx_and_static_validation():
     assert L.fp8bq_mx_quant_act(P(A), 4, 48, 48, P(A), P(A), None) == 3    # K % 32
     assert L.fp8bq_mx_gemm(P(A), P(A), P(A), P(A), None, P(A), 4, 64, 80, P(A), 1 << 20,
