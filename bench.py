@@ -56,8 +56,9 @@ FP8_PER_BF16 = 2.0   # nominal dense FP8 / BF16 tensor rate
 # block-GEMM launch from an ncu capture, valid only for the kernel sources whose
 # digest is recorded; anything else reports null.
 NCU_TRAFFIC = {
-    "source_sha256": None,
-    "bytes_per_launch": None,
+    # profiles/block_gemm_prefill_4096x24576x6144.md (N = 24576 launch)
+    "source_sha256": "97122154c77436d657d4b13e89dcca4e72511b5fb1cce52869df340f47d0aa85",
+    "bytes_per_launch": 187026944 + 175159552,
 }
 
 
