@@ -57,8 +57,8 @@ FP8_PER_BF16 = 2.0   # nominal dense FP8 / BF16 tensor rate
 # digest is recorded; anything else reports null.
 NCU_TRAFFIC = {
     # profiles/block_gemm_prefill_4096x24576x6144.md (N = 24576 launch)
-    "source_sha256": "97122154c77436d657d4b13e89dcca4e72511b5fb1cce52869df340f47d0aa85",
-    "bytes_per_launch": 187026944 + 175159552,
+    "source_sha256": "3945102f9c819f420ea9225efd32bb2a26e0fc6ff5c8cedddbbb260d70bf04e9",
+    "bytes_per_launch": 182380800 + 173614080,
 }
 
 

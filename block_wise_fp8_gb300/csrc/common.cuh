@@ -58,6 +58,9 @@ struct GemmArgs {
   uint32_t *counters;
   float *partials;
   uint64_t wait_limit_ns;
+  // fault injection for the timeout tests (0 in normal use): CTA 0 issues no
+  // copy for its first K block, so the waits on that stage run out
+  int fault_skip_first_load;
 };
 
 struct DeviceInfo {

@@ -4,6 +4,7 @@
 // and gemm_*.cu.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -36,6 +37,22 @@ uint64_t wait_limit_ns() {
     return ms * 1000000ull;
   }();
   return v;
+}
+
+// Fault injection for the timeout tests, off unless the environment (read
+// once) has FP8BQ_FAULT_INJECT=skip_first_load:<n>: then CTA 0 of each of the
+// next n GEMM launches issues no copy for its first K block, the waits on that
+// stage run out after the wait limit, and the GEMM reports FP8BQ_ERR_TIMEOUT
+// through the workspace status word.  Later launches run normally.
+int fault_skip_first_load() {
+  static std::atomic<long> remaining{[] {
+    const char *e = std::getenv("FP8BQ_FAULT_INJECT");
+    const char *key = "skip_first_load:";
+    if (!e || std::strncmp(e, key, std::strlen(key)) != 0) return 0L;
+    return std::strtol(e + std::strlen(key), nullptr, 10);
+  }()};
+  if (remaining.load(std::memory_order_relaxed) <= 0) return 0;
+  return remaining.fetch_sub(1) > 0 ? 1 : 0;
 }
 
 int cuda_fail(cudaError_t e) {
@@ -111,6 +128,7 @@ GemmArgs base_args(int mode, int64_t M, int64_t N, int64_t K, const void *bias, 
   a.counters = reinterpret_cast<uint32_t *>(w + L.counters);
   a.partials = reinterpret_cast<float *>(w + L.partials);
   a.wait_limit_ns = wait_limit_ns();
+  a.fault_skip_first_load = fault_skip_first_load();
   return a;
 }
 

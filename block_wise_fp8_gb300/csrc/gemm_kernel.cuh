@@ -330,6 +330,7 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
             ok = false;
             break;
           }
+          if (args.fault_skip_first_load && blockIdx.x == 0 && it == 0) continue;
           if (PAIR) {
             // both CTAs' bytes complete on the even CTA's barrier
             if (leader) mbar_arrive_expect_tx(&bars->full[s], 2 * C::kStageBytes);
@@ -576,8 +577,7 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
             }
           }
           // all epilogue warps agree on the outcome before anything is stored
-          named_bar_sync(2, C::kEpiThreads);
-          if (*abort_flag) {
+          if (named_bar_any(2, C::kEpiThreads, !ok || *abort_flag)) {
             ok = false;
             break;
           }
@@ -593,8 +593,7 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
           // kModeTensor / kModeMx: one pass over the full-K accumulator
           const uint32_t b = uit % ACCB, ph = (uit / ACCB) & 1u;
           if (!warp_wait(&bars->tfull[b], ph, abort_flag, limit)) ok = false;
-          named_bar_sync(2, C::kEpiThreads);
-          if (*abort_flag || !ok) {
+          if (named_bar_any(2, C::kEpiThreads, !ok || *abort_flag)) {
             ok = false;
             break;
           }
@@ -714,8 +713,7 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
           }
         }
 
-        named_bar_sync(2, C::kEpiThreads);
-        if (*abort_flag) {
+        if (named_bar_any(2, C::kEpiThreads, !ok || *abort_flag)) {
           ok = false;
           break;
         }

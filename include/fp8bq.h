@@ -48,7 +48,10 @@
  *  - Every device-side wait is bounded: a wait that runs out sets a status word
  *    in the workspace, the kernel exits cleanly, and fp8bq_poll_status reports
  *    FP8BQ_ERR_TIMEOUT.  The limit is 1 s per wait, or FP8BQ_WAIT_LIMIT_MS from
- *    the environment, read once.  After a timeout the outputs are undefined.
+ *    the environment, read once.  After a timeout the outputs are undefined
+ *    and the workspace must be zeroed again (fp8bq_workspace_init).  For
+ *    tests, FP8BQ_FAULT_INJECT=skip_first_load:<n> (read once) makes the next
+ *    n GEMM launches skip one tile copy so that their waits run out.
  *  - No C++ exception crosses this interface.
  */
 #ifndef FP8BQ_H
