@@ -74,6 +74,10 @@ struct Cfg {
   // partial buffers), so one issues while the other waits on its barriers
   static constexpr int kIssuers = (MODE == kModeBlock) ? 2 : 1;
   static constexpr int kThreads = 32 * (1 + kIssuers + kSfWarps + EPI_WARPS);
+  // register budget: warps are dealt round-robin to the SM's four schedulers,
+  // each with a quarter of the register file, so the bound counts whole
+  // groups of four warps
+  static constexpr int kBoundThreads = (kThreads + 127) / 128 * 128;
   static constexpr int kEpiThreads = 32 * EPI_WARPS;
   static constexpr int kEpiBase = 1 + kIssuers + kSfWarps;  // first epilogue warp
   static constexpr int kColGroups = EPI_WARPS / 4;
@@ -97,7 +101,6 @@ struct Cfg {
   static_assert(kCPT % kCW == 0 && kCPT % 2 == 0, "chunking");
   static_assert(kTmemCols <= 512, "TMEM columns");
   static_assert(STAGES <= 8 && ACCB <= 8, "barrier arrays");
-  static_assert(kIssuers == 1 || ACCB % kIssuers == 0, "each issuer owns whole buffers");
   static_assert(MODE != kModeMx || (!SWAP && BN % 32 == 0 && kSfColsB <= 8), "MX tiles");
   static_assert(!PAIR || (!SWAP && MODE != kModeMx && kBrows % 8 == 0), "pair tiles");
   static_assert(MODE != kModeBlock || SWAP || (128 % kCPT == 0 && BN % kCPT == 0),
@@ -254,7 +257,7 @@ __device__ __forceinline__ void store_row(uint16_t *y, const float *v, int m, in
 // One CTA per SM.  Registers are split over the SM's four schedulers, so the
 // per-thread budget is set by the scheduler holding the most warps.
 template <int MODE, bool SWAP, int BN, int STAGES, int EPI_WARPS, int ACCB, bool PAIR>
-__global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, PAIR>::kThreads, 1)
+__global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, PAIR>::kBoundThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ GemmArgs args, const LaunchShape shape) {
@@ -316,200 +319,203 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
 
   const int KB = shape.KB;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      uint32_t issued = 0, phase_bits = 0;  // per stage: ever issued, last phase
-      uint32_t it = 0;
-      bool ok = true;
-      for (int u = cl_id; ok && u < shape.units; u += cl_num) {
-        const Unit w = decode_unit<SWAP, PAIR>(u, shape.num_a_tiles, shape.splits, shape.kps, KB, BN, rank);
-        for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
-          const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
-          if (!mbar_wait(&bars->empty[s], ph ^ 1u, abort_flag, limit)) {
-            ok = false;
-            break;
+  if (warp < C::kEpiBase) {
+    // producer, MMA issuers, MX scale-factor writers
+    if (warp == 0) {
+      // ------------------------------------------------------------ TMA producer
+      if (lane == 0) {
+        uint32_t issued = 0, phase_bits = 0;  // per stage: ever issued, last phase
+        uint32_t it = 0;
+        bool ok = true;
+        for (int u = cl_id; ok && u < shape.units; u += cl_num) {
+          const Unit w = decode_unit<SWAP, PAIR>(u, shape.num_a_tiles, shape.splits, shape.kps, KB, BN, rank);
+          for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
+            const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+            if (!mbar_wait(&bars->empty[s], ph ^ 1u, abort_flag, limit)) {
+              ok = false;
+              break;
+            }
+            if (args.fault_skip_first_load && blockIdx.x == 0 && it == 0) continue;
+            if (PAIR) {
+              // both CTAs' bytes complete on the even CTA's barrier
+              if (leader) mbar_arrive_expect_tx(&bars->full[s], 2 * C::kStageBytes);
+              const uint32_t bar0 = mapa_shared(smem_u32(&bars->full[s]), 0);
+              tma_load_2d_pair(sA + s * kAbytes, &tmA, bar0, kb * 128, w.a_row0);
+              tma_load_2d_pair(sB + s * C::kBbytes, &tmB, bar0, kb * 128, w.b_load_row0);
+            } else {
+              mbar_arrive_expect_tx(&bars->full[s], C::kStageBytes);
+              tma_load_2d(sA + s * kAbytes, &tmA, &bars->full[s], kb * 128, w.a_row0);
+              tma_load_2d(sB + s * C::kBbytes, &tmB, &bars->full[s], kb * 128, w.b_load_row0);
+            }
+            issued |= 1u << s;
+            phase_bits = (phase_bits & ~(1u << s)) | (ph << s);
           }
-          if (args.fault_skip_first_load && blockIdx.x == 0 && it == 0) continue;
-          if (PAIR) {
-            // both CTAs' bytes complete on the even CTA's barrier
-            if (leader) mbar_arrive_expect_tx(&bars->full[s], 2 * C::kStageBytes);
-            const uint32_t bar0 = mapa_shared(smem_u32(&bars->full[s]), 0);
-            tma_load_2d_pair(sA + s * kAbytes, &tmA, bar0, kb * 128, w.a_row0);
-            tma_load_2d_pair(sB + s * C::kBbytes, &tmB, bar0, kb * 128, w.b_load_row0);
-          } else {
-            mbar_arrive_expect_tx(&bars->full[s], C::kStageBytes);
-            tma_load_2d(sA + s * kAbytes, &tmA, &bars->full[s], kb * 128, w.a_row0);
-            tma_load_2d(sB + s * C::kBbytes, &tmB, &bars->full[s], kb * 128, w.b_load_row0);
-          }
-          issued |= 1u << s;
-          phase_bits = (phase_bits & ~(1u << s)) | (ph << s);
+        }
+        if (!ok) {
+          record_timeout(args);
+          // let every copy issued land before shared memory goes away (pair tiles:
+          // the even CTA's barriers count both CTAs' copies; the odd CTA stays
+          // resident until the closing cluster barrier)
+          for (int s = 0; s < STAGES && (!PAIR || leader); ++s)
+            if ((issued >> s) & 1u) {
+              uint32_t dummy = 0;
+              mbar_wait(&bars->full[s], (phase_bits >> s) & 1u, &dummy, limit);
+            }
         }
       }
-      if (!ok) {
-        record_timeout(args);
-        // let every copy issued land before shared memory goes away (pair tiles:
-        // the even CTA's barriers count both CTAs' copies; the odd CTA stays
-        // resident until the closing cluster barrier)
-        for (int s = 0; s < STAGES && (!PAIR || leader); ++s)
-          if ((issued >> s) & 1u) {
-            uint32_t dummy = 0;
-            mbar_wait(&bars->full[s], (phase_bits >> s) & 1u, &dummy, limit);
-          }
-      }
-    }
-    __syncwarp();
-  } else if (warp <= C::kIssuers) {
-    // ------------------------------------------------------------ MMA issuers
-    // Issuer `me` takes the K blocks with it % kIssuers == me (block tiles; every
-    // K block has its own TMEM partial buffer) -- with one issuer, all of them.
-    const uint32_t me = static_cast<uint32_t>(warp - 1);
-    if (lane == 0 && (!PAIR || leader)) {
-      uint32_t it = 0, uit = 0;
-      bool ok = true;
-      for (int u = cl_id; ok && u < shape.units; u += cl_num, ++uit) {
-        const Unit w = decode_unit<SWAP, PAIR>(u, shape.num_a_tiles, shape.splits, shape.kps, KB, BN, rank);
-        if (MODE != kModeBlock) {
-          const uint32_t b = uit % ACCB, ph = (uit / ACCB) & 1u;
-          if (!mbar_wait(&bars->tempty[b], ph ^ 1u, abort_flag, limit)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-        }
-        for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
-          if (C::kIssuers > 1 && it % C::kIssuers != me) continue;
-          uint32_t d_tmem;
-          if (MODE == kModeBlock) {
-            const uint32_t b = it % ACCB, ph = (it / ACCB) & 1u;
+      __syncwarp();
+    } else if (warp <= C::kIssuers) {
+      // ------------------------------------------------------------ MMA issuers
+      // Issuer `me` takes the K blocks with it % kIssuers == me (block tiles; every
+      // K block has its own TMEM partial buffer) -- with one issuer, all of them.
+      const uint32_t me = static_cast<uint32_t>(warp - 1);
+      if (lane == 0 && (!PAIR || leader)) {
+        uint32_t it = 0, uit = 0;
+        bool ok = true;
+        for (int u = cl_id; ok && u < shape.units; u += cl_num, ++uit) {
+          const Unit w = decode_unit<SWAP, PAIR>(u, shape.num_a_tiles, shape.splits, shape.kps, KB, BN, rank);
+          if (MODE != kModeBlock) {
+            const uint32_t b = uit % ACCB, ph = (uit / ACCB) & 1u;
             if (!mbar_wait(&bars->tempty[b], ph ^ 1u, abort_flag, limit)) {
               ok = false;
               break;
             }
-            d_tmem = tmem_base + b * BN;
-          } else {
-            d_tmem = tmem_base + (uit % ACCB) * BN;
+            tc_fence_after();
           }
-          const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
-          if (!mbar_wait(&bars->full[s], ph, abort_flag, limit)) {
-            ok = false;
-            break;
-          }
-          uint32_t sfslot = 0;
-          if (MODE == kModeMx) {
-            sfslot = it % C::kSfSlots;
-            if (!mbar_wait(&bars->sf_full[sfslot], (it / C::kSfSlots) & 1u, abort_flag, limit)) {
+          for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
+            if (C::kIssuers > 1 && it % C::kIssuers != me) continue;
+            uint32_t d_tmem;
+            if (MODE == kModeBlock) {
+              const uint32_t b = it % ACCB, ph = (it / ACCB) & 1u;
+              if (!mbar_wait(&bars->tempty[b], ph ^ 1u, abort_flag, limit)) {
+                ok = false;
+                break;
+              }
+              d_tmem = tmem_base + b * BN;
+            } else {
+              d_tmem = tmem_base + (uit % ACCB) * BN;
+            }
+            const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+            if (!mbar_wait(&bars->full[s], ph, abort_flag, limit)) {
               ok = false;
               break;
             }
-          }
-          tc_fence_after();
-          const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(sA + s * kAbytes));
-          const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(sB + s * C::kBbytes));
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            // advance 32 K-bytes inside the 128-byte swizzled row: +2 in the >>4 field
-            const uint32_t acc = (MODE == kModeBlock) ? (k > 0) : (kb > w.kb0 || k > 0);
+            uint32_t sfslot = 0;
             if (MODE == kModeMx) {
-              const uint32_t sfcol = tmem_base + C::kSfBase + sfslot * C::kSfSlotCols;
-              umma_mxf8f6f4(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc_mxf8_e4m3(kBM, BN, k, k),
-                            sfcol, sfcol + 8, acc);
-            } else if (PAIR) {
-              umma_f8f6f4_pair(d_tmem, adesc + 2 * k, bdesc + 2 * k,
-                               idesc_f8f6f4_e4m3(C::kMmaM, BN), acc);
-            } else {
-              umma_f8f6f4(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc_f8f6f4_e4m3(kBM, BN), acc);
+              sfslot = it % C::kSfSlots;
+              if (!mbar_wait(&bars->sf_full[sfslot], (it / C::kSfSlots) & 1u, abort_flag, limit)) {
+                ok = false;
+                break;
+              }
+            }
+            tc_fence_after();
+            const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(sA + s * kAbytes));
+            const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(sB + s * C::kBbytes));
+  #pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              // advance 32 K-bytes inside the 128-byte swizzled row: +2 in the >>4 field
+              const uint32_t acc = (MODE == kModeBlock) ? (k > 0) : (kb > w.kb0 || k > 0);
+              if (MODE == kModeMx) {
+                const uint32_t sfcol = tmem_base + C::kSfBase + sfslot * C::kSfSlotCols;
+                umma_mxf8f6f4(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc_mxf8_e4m3(kBM, BN, k, k),
+                              sfcol, sfcol + 8, acc);
+              } else if (PAIR) {
+                umma_f8f6f4_pair(d_tmem, adesc + 2 * k, bdesc + 2 * k,
+                                 idesc_f8f6f4_e4m3(C::kMmaM, BN), acc);
+              } else {
+                umma_f8f6f4(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc_f8f6f4_e4m3(kBM, BN), acc);
+              }
+            }
+            if (PAIR) umma_commit_pair(&bars->empty[s], 0x3);
+            else umma_commit(&bars->empty[s]);
+            if (MODE == kModeMx) umma_commit(&bars->sf_empty[sfslot]);
+            if (MODE == kModeBlock) {
+              if (PAIR) umma_commit_pair(&bars->tfull[it % ACCB], 0x3);
+              else umma_commit(&bars->tfull[it % ACCB]);
             }
           }
-          if (PAIR) umma_commit_pair(&bars->empty[s], 0x3);
-          else umma_commit(&bars->empty[s]);
-          if (MODE == kModeMx) umma_commit(&bars->sf_empty[sfslot]);
-          if (MODE == kModeBlock) {
-            if (PAIR) umma_commit_pair(&bars->tfull[it % ACCB], 0x3);
-            else umma_commit(&bars->tfull[it % ACCB]);
+          if (!ok) break;
+          if (MODE != kModeBlock) {
+            if (PAIR) umma_commit_pair(&bars->tfull[uit % ACCB], 0x3);
+            else umma_commit(&bars->tfull[uit % ACCB]);
           }
         }
-        if (!ok) break;
-        if (MODE != kModeBlock) {
-          if (PAIR) umma_commit_pair(&bars->tfull[uit % ACCB], 0x3);
-          else umma_commit(&bars->tfull[uit % ACCB]);
-        }
+        if (!ok) record_timeout(args);
+        // every MMA issued by both issuers has completed once `drain` flips
+        if (PAIR) umma_commit_pair(&bars->drain, 0x1);
+        else umma_commit(&bars->drain);
+        uint32_t dummy = 0;
+        mbar_wait(&bars->drain, 0, &dummy, limit);
       }
-      if (!ok) record_timeout(args);
-      // every MMA issued by both issuers has completed once `drain` flips
-      if (PAIR) umma_commit_pair(&bars->drain, 0x1);
-      else umma_commit(&bars->drain);
-      uint32_t dummy = 0;
-      mbar_wait(&bars->drain, 0, &dummy, limit);
-    }
-    __syncwarp();
-  } else if (warp < C::kEpiBase) {
-    // ------------------------------------------------------------ MX scale-factor writers
-    // (warps 1 + kIssuers .. kEpiBase - 1)
-    // Warp with lane quarter q writes TMEM lanes 32q..32q+31.  Layout (replicated in
-    // every quarter): lane i, column c of a slot holds the four UE8M0 codes of stage
-    // kb (K groups 4kb..4kb+3, one byte per MMA, selected by the sf id) of tile row
-    // i + 32c.  The codes are loaded kSfPrefetch stages before they are written.
-    if (MODE == kModeMx) {
-      constexpr int PD = C::kSfPrefetch;
-      constexpr int NA = C::kSfColsA, NB = C::kSfColsB;
-      const int q = warp & 3;
-      const int G = args.K / 32;
-      uint32_t sfit = 0;
-      bool ok = true;
-      uint32_t ring[PD][NA + NB];
-      for (int u = cl_id; ok && u < shape.units; u += cl_num) {
-        const Unit w = decode_unit<SWAP, PAIR>(u, shape.num_a_tiles, shape.splits, shape.kps, KB, BN, rank);
-        auto load = [&](int kb, uint32_t *dst) {
-#pragma unroll
-          for (int c = 0; c < NA; ++c) dst[c] = sf_word(args.ux, w.a_row0 + lane + 32 * c, args.M, G, kb);
-#pragma unroll
-          for (int c = 0; c < NB; ++c)
-            dst[NA + c] = sf_word(args.uw, w.b_row0 + lane + 32 * c, args.N, G, kb);
-        };
-#pragma unroll
-        for (int i = 0; i < PD; ++i)
-          if (w.kb0 + i < w.kb1) load(w.kb0 + i, ring[i]);
-        for (int kb = w.kb0; ok && kb < w.kb1; kb += PD) {
-#pragma unroll
-          for (int i = 0; i < PD; ++i) {
-            const int k = kb + i;
-            if (k < w.kb1 && ok) {
-              const uint32_t slot = sfit % C::kSfSlots;
-              if (!warp_wait(&bars->sf_empty[slot], ((sfit / C::kSfSlots) & 1u) ^ 1u,
-                             abort_flag, limit)) {
-                ok = false;
-              } else {
-                tc_fence_after();
-                const uint32_t col = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
-                                     C::kSfBase + slot * C::kSfSlotCols;
-                tmem_st4(col, ring[i][0], ring[i][1], ring[i][2], ring[i][3]);
-#pragma unroll
-                for (int c = 0; c < NB; c += 4)
-                  tmem_st4(col + 8 + c, ring[i][NA + c], ring[i][NA + c + 1],
-                           ring[i][NA + c + 2], ring[i][NA + c + 3]);
-                tmem_st_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars->sf_full[slot]);
-                ++sfit;
-                if (k + PD < w.kb1) load(k + PD, ring[i]);
+      __syncwarp();
+    } else if (warp < C::kEpiBase) {
+      // ------------------------------------------------------------ MX scale-factor writers
+      // (warps 1 + kIssuers .. kEpiBase - 1)
+      // Warp with lane quarter q writes TMEM lanes 32q..32q+31.  Layout (replicated in
+      // every quarter): lane i, column c of a slot holds the four UE8M0 codes of stage
+      // kb (K groups 4kb..4kb+3, one byte per MMA, selected by the sf id) of tile row
+      // i + 32c.  The codes are loaded kSfPrefetch stages before they are written.
+      if (MODE == kModeMx) {
+        constexpr int PD = C::kSfPrefetch;
+        constexpr int NA = C::kSfColsA, NB = C::kSfColsB;
+        const int q = warp & 3;
+        const int G = args.K / 32;
+        uint32_t sfit = 0;
+        bool ok = true;
+        uint32_t ring[PD][NA + NB];
+        for (int u = cl_id; ok && u < shape.units; u += cl_num) {
+          const Unit w = decode_unit<SWAP, PAIR>(u, shape.num_a_tiles, shape.splits, shape.kps, KB, BN, rank);
+          auto load = [&](int kb, uint32_t *dst) {
+  #pragma unroll
+            for (int c = 0; c < NA; ++c) dst[c] = sf_word(args.ux, w.a_row0 + lane + 32 * c, args.M, G, kb);
+  #pragma unroll
+            for (int c = 0; c < NB; ++c)
+              dst[NA + c] = sf_word(args.uw, w.b_row0 + lane + 32 * c, args.N, G, kb);
+          };
+  #pragma unroll
+          for (int i = 0; i < PD; ++i)
+            if (w.kb0 + i < w.kb1) load(w.kb0 + i, ring[i]);
+          for (int kb = w.kb0; ok && kb < w.kb1; kb += PD) {
+  #pragma unroll
+            for (int i = 0; i < PD; ++i) {
+              const int k = kb + i;
+              if (k < w.kb1 && ok) {
+                const uint32_t slot = sfit % C::kSfSlots;
+                if (!warp_wait(&bars->sf_empty[slot], ((sfit / C::kSfSlots) & 1u) ^ 1u,
+                               abort_flag, limit)) {
+                  ok = false;
+                } else {
+                  tc_fence_after();
+                  const uint32_t col = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
+                                       C::kSfBase + slot * C::kSfSlotCols;
+                  tmem_st4(col, ring[i][0], ring[i][1], ring[i][2], ring[i][3]);
+  #pragma unroll
+                  for (int c = 0; c < NB; c += 4)
+                    tmem_st4(col + 8 + c, ring[i][NA + c], ring[i][NA + c + 1],
+                             ring[i][NA + c + 2], ring[i][NA + c + 3]);
+                  tmem_st_wait();
+                  tc_fence_before();
+                  __syncwarp();
+                  if (lane == 0) mbar_arrive(&bars->sf_full[slot]);
+                  ++sfit;
+                  if (k + PD < w.kb1) load(k + PD, ring[i]);
+                }
               }
             }
           }
         }
+        if (!ok && lane == 0) record_timeout(args);
       }
-      if (!ok && lane == 0) record_timeout(args);
+      __syncwarp();
     }
-    __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
     const int ew = warp - C::kEpiBase;
     const int quarter = warp & 3;
-    // tell the MMA issuer (the even CTA for pair tiles) that an accumulator is drained
-    auto release_acc = [&](uint64_t *bar) {
-      if (PAIR && !leader) mbar_arrive_cluster(mapa_shared(smem_u32(bar), 0));
-      else mbar_arrive(bar);
+    // tell the MMA issuer (the even CTA for pair tiles) that accumulator b is drained
+    auto release_acc = [&](uint32_t b) {
+      if (PAIR && !leader) mbar_arrive_cluster(mapa_shared(smem_u32(&bars->tempty[b]), 0));
+      else mbar_arrive(&bars->tempty[b]);
     };
     const int cg = ew >> 2;  // column group
     const int et = ew * 32 + lane;
@@ -535,8 +541,9 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
           const bool row_ok = m < args.M;
           // every column of this thread lies in one 128-row weight block (kCPT
           // divides 128 and tiles start on multiples of kCPT), so the promotion
-          // factor of a K block is s_x[m][kb] * s_w[nb][kb]; both are fetched one
-          // K block ahead so no global load sits on the per-block critical path
+          // factor of a K block is s_x[m][kb] * s_w[nb][kb]; both are fetched two
+          // K blocks ahead so no global load sits on the per-block critical path
+          // (an arrive with release semantics also waits for loads still in flight)
           const int nb = min(nbase / kBlockN, NBLK - 1);
           const float *swrow = args.sw + static_cast<int64_t>(nb) * KB;
           auto sx_at = [&](int kb) -> float {
@@ -546,10 +553,13 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
                                         : static_cast<int64_t>(kb) * args.ldsx + m));
           };
           auto sw_at = [&](int kb) -> float { return kb < w.kb1 ? __ldg(swrow + kb) : 0.0f; };
-          float sx_next = sx_at(w.kb0), sw_next = sw_at(w.kb0);
+          float sx_cur = sx_at(w.kb0), sw_cur = sw_at(w.kb0);
+          float sx_nxt = sx_at(w.kb0 + 1), sw_nxt = sw_at(w.kb0 + 1);
           for (int kb = w.kb0; kb < w.kb1 && ok; ++kb, ++kit) {
             const uint32_t b = kit % ACCB, ph = (kit / ACCB) & 1u;
-            const float f = sx_next * sw_next;
+            const float f = sx_cur * sw_cur;
+            sx_cur = sx_nxt;
+            sw_cur = sw_nxt;
             if (!warp_wait(&bars->tfull[b], ph, abort_flag, limit)) {
               ok = false;
               break;
@@ -564,11 +574,9 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
               if (c == C::kCPT / C::kCW - 1) {
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) release_acc(&bars->tempty[b]);
-                // the next K block's scales are requested only after the release,
-                // which would otherwise wait for these loads to complete
-                sx_next = sx_at(kb + 1);
-                sw_next = sw_at(kb + 1);
+                if (lane == 0) release_acc(b);
+                sx_nxt = sx_at(kb + 2);
+                sw_nxt = sw_at(kb + 2);
               }
 #pragma unroll
               for (int j = 0; j < C::kCW; j += 2)
@@ -608,7 +616,7 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
             if (c == C::kCPT / C::kCW - 1) {
               tc_fence_before();
               __syncwarp();
-              if (lane == 0) release_acc(&bars->tempty[b]);
+              if (lane == 0) release_acc(b);
             }
             float v[C::kCW];
             // per-tensor scales: one output partition covers the whole chunk
@@ -678,7 +686,7 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
             tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) release_acc(&bars->tempty[b]);
+            if (lane == 0) release_acc(b);
             if (kb + 1 < w.kb1) sw_next = __ldg(swrow + kb + 1);  // after the release
             const float *sxk = sx_stage + (kb - w.kb0) * BN;
 #pragma unroll
@@ -703,7 +711,7 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
             tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) release_acc(&bars->tempty[b]);
+            if (lane == 0) release_acc(b);
             // one output partition per lane (weight row)
             int p = 0;
             while (p < args.n_parts - 1 && d_row >= args.part_end[p]) ++p;

@@ -143,15 +143,18 @@ int launch_gemm(const GemmArgs &a, const void *q_act, const void *w, const Devic
     return status;
   }
   // prefill: CTA pairs over 256 x bn tiles, persistent clusters, M fastest.  The
-  // weight tile width bn is the one with the least (waves x bn), i.e. the
-  // smallest tail when the tiles are dealt to the pairs.
+  // weight tile width bn is the one with the least (waves x bn x time per
+  // column), i.e. the smallest tail when the tiles are dealt to the pairs; for
+  // block scaling a 256-wide tile takes about 5 % less time per column than a
+  // 192-wide one (measured on GB300), for per-tensor scaling the same.
   const int pairs = dev.num_sms / 2;
   sh.num_a_tiles = (a.M + 255) / 256;
   int best_bn = 256;
   long best_cost = -1;
   for (int bn : {256, 192}) {
     const long units = static_cast<long>(sh.num_a_tiles) * ((a.N + bn - 1) / bn);
-    const long cost = (units + pairs - 1) / pairs * bn;
+    const long per_col = (a.mode == kModeBlock && bn == 256) ? 95 : 100;
+    const long cost = (units + pairs - 1) / pairs * bn * per_col;
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;
       best_bn = bn;
