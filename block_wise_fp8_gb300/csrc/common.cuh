@@ -42,6 +42,7 @@ struct GemmArgs {
   int sx_layout;  // 0 row-major [M][KB], 1 column-major [KB][ldsx]
   int ldsx;       // KB for row-major, round_up(M,4) for column-major
   const float *sw;
+  int sc_tma;     // set by the launcher: s_x and s_w reach the epilogue through TMA
   // static path
   const float *sx_scalar;
   const float *sw_part;
@@ -53,6 +54,7 @@ struct GemmArgs {
   // epilogue
   const void *bias;
   void *y;
+  int y_tma;  // set by the launcher: Y is written with TMA stores
   // workspace
   uint32_t *status;
   uint32_t *counters;
@@ -91,6 +93,15 @@ bool make_kmajor_map(CUtensorMap *m, const void *base, int64_t rows, int64_t K, 
 // The same through a small per-process cache of recently encoded maps.
 bool cached_kmajor_map(CUtensorMap *m, const void *base, int64_t rows, int64_t K,
                        int box_rows);
+// FP32 matrix [rows, cols] (row pitch `pitch` floats, a multiple of 4) as a TMA
+// map with a [box_rows x box_cols] box, no swizzle; through a small cache.
+bool cached_f32_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols,
+                    int64_t pitch, int box_cols, int box_rows);
+// Row-major BF16 matrix [rows, cols] (pitch 2*cols bytes, cols % 8 == 0) as a
+// TMA map with a [box_rows x box_cols] box, 128-byte swizzled (box_cols = 64),
+// through a small cache like the one above.
+bool cached_bf16_rows_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols,
+                          int box_cols, int box_rows);
 
 // Kernel variants, one translation unit each (instantiated from gemm_kernel.cuh).
 // Pair (prefill) forms: `bn` is the weight-row tile, 192 or 256, and `grid` the

@@ -43,6 +43,7 @@
 #pragma once
 #include <cuda_bf16.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "common.cuh"
@@ -73,28 +74,57 @@ struct Cfg {
   // block tiles: two MMA-issuing warps take alternate K blocks (disjoint TMEM
   // partial buffers), so one issues while the other waits on its barriers
   static constexpr int kIssuers = (MODE == kModeBlock) ? 2 : 1;
-  static constexpr int kThreads = 32 * (1 + kIssuers + kSfWarps + EPI_WARPS);
+  // block pair tiles keep the promoted FP32 accumulators in the epilogue warps'
+  // registers: warpgroup 0 (producer, the two issuers and one idle warp) hands
+  // registers to the epilogue warpgroups with setmaxnreg
+  static constexpr bool kRegSplit = (MODE == kModeBlock) && PAIR;
+  static constexpr int kEpiBase = kRegSplit ? 4 : 1 + kIssuers + kSfWarps;  // first epilogue warp
+  static constexpr int kThreads = 32 * (kEpiBase + EPI_WARPS);
   // register budget: warps are dealt round-robin to the SM's four schedulers,
   // each with a quarter of the register file, so the bound counts whole
   // groups of four warps
   static constexpr int kBoundThreads = (kThreads + 127) / 128 * 128;
+  static constexpr int kLaunchRegs = (65536 / kBoundThreads) / 8 * 8 < 248 ? (65536 / kBoundThreads) / 8 * 8 : 248;
+  static constexpr int kLowRegs = 32;   // warpgroup 0 after the split
+  static constexpr int kHighRegsRaw =
+      (kLaunchRegs * kBoundThreads - 128 * kLowRegs) / (kBoundThreads > 128 ? kBoundThreads - 128 : 1) / 8 * 8;
+  static constexpr int kHighRegs = kHighRegsRaw < 248 ? kHighRegsRaw : 248;  // epilogue warpgroups
   static constexpr int kEpiThreads = 32 * EPI_WARPS;
-  static constexpr int kEpiBase = 1 + kIssuers + kSfWarps;  // first epilogue warp
   static constexpr int kColGroups = EPI_WARPS / 4;
   static constexpr int kCPT = BN / kColGroups;   // columns per epilogue thread
   // tcgen05.ld chunk width: 16 columns where a large FP32 accumulator lives in
-  // registers (block tiles with more than 64 columns per thread), otherwise 32
-  static constexpr int kCW =
-      (MODE == kModeBlock && !SWAP && kCPT > 64) ? 16 : (kCPT % 32 == 0) ? 32 : 16;
+  // registers without the register split, otherwise 32
+  static constexpr int kCW = kRegSplit ? 32
+                             : (MODE == kModeBlock && !SWAP && kCPT > 64) ? 16
+                             : (kCPT % 32 == 0) ? 32 : 16;
+  // columns loaded per tcgen05.wait::ld in the block-tile promotion
+  static constexpr int kLD = kRegSplit ? (kCPT < 64 ? kCPT : 64) : kCW;
+  // block pair tiles write Y with TMA stores from a per-warp staging area
+  // (32 rows x 64 BF16 columns per box, 128-byte swizzled)
+  static constexpr bool kTmaStoreY = (MODE == kModeBlock) && PAIR;
+  static constexpr int kYBoxCols = 64;
+  static constexpr int kYBoxBytes = 32 * kYBoxCols * 2;
+  static constexpr int kYStageBytes = kTmaStoreY ? kBM * BN * 2 : 0;
   static constexpr int kBbytes = kBrows * 128;
   static constexpr int kStageBytes = kAbytes + kBbytes;
+  // block pair tiles: promotion factors come through a shared-memory ring
+  // filled by the TMA producer, kScQuad K blocks per slot: s_x of this CTA's
+  // 128 rows and s_w of the tile's (at most two) 128-row weight blocks
+  static constexpr bool kScRing = (MODE == kModeBlock) && PAIR;
+  static constexpr int kScQuad = 4;
+  static constexpr int kScSlots = kScRing ? 4 : 0;
+  static constexpr int kScXBytes = kBM * kScQuad * 4;           // 2 KB
+  static constexpr int kScWBytes = 2 * kScQuad * 4;             // 32 B
+  static constexpr int kScSlotBytes = kScXBytes + 128;          // s_w at +kScXBytes
+  static constexpr int kScBytes = kScSlots * kScSlotBytes;
   static constexpr int kAccCols = ACCB * BN;     // accumulators / partials
   static constexpr int kSfBase = kAccCols;
   static constexpr uint32_t kTmemCols =
       pow2_at_least(kAccCols + (MODE == kModeMx ? kSfSlots * kSfSlotCols : 0));
   static constexpr int kBarBytes = 512;
   // dynamic shared memory: [align slack][A stages][B stages][barriers][sx stage]
-  static constexpr size_t kFixedSmem = 1024 + size_t(STAGES) * kStageBytes + kBarBytes;
+  static constexpr size_t kFixedSmem =
+      1024 + size_t(STAGES) * kStageBytes + kYStageBytes + kScBytes + kBarBytes;
 
   static_assert(EPI_WARPS % 4 == 0, "epilogue warps must cover the 4 TMEM lane quarters");
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M = 128");
@@ -107,12 +137,20 @@ struct Cfg {
                 "block tiles: each thread's columns lie in one 128-row weight block");
   static_assert(!SWAP || (kCPT <= 64 && EPI_WARPS == 4),
                 "swapped tiles keep all token columns of a weight row in one thread");
+  static_assert(!kRegSplit || (kThreads % 128 == 0 && kHighRegs >= kLowRegs &&
+                               128 * kLowRegs + (kThreads - 128) * kHighRegs <=
+                                   kLaunchRegs * kThreads),
+                "register split fits in the registers the block is launched with");
+  static_assert(kCPT % kLD == 0 && kLD % kCW == 0, "promotion load groups");
+  static_assert(!kTmaStoreY || (kCPT % kYBoxCols == 0 && kStageBytes % 1024 == 0),
+                "TMA-stored Y boxes");
 };
 
 struct SmemBarriers {
   uint64_t full[8], empty[8];
   uint64_t tfull[8], tempty[8];
   uint64_t sf_full[4], sf_empty[4];
+  uint64_t sc_full[4], sc_empty[4];
   uint64_t drain;
   uint32_t tmem_base;
   uint32_t abort;
@@ -260,6 +298,9 @@ template <int MODE, bool SWAP, int BN, int STAGES, int EPI_WARPS, int ACCB, bool
 __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, PAIR>::kBoundThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmY,
+                    const __grid_constant__ CUtensorMap tmSx,
+                    const __grid_constant__ CUtensorMap tmSw,
                     const __grid_constant__ GemmArgs args, const LaunchShape shape) {
   using C = Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, PAIR>;
   extern __shared__ uint8_t smem_raw[];
@@ -267,8 +308,10 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
   uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
   uint8_t *sA = smem;
   uint8_t *sB = smem + STAGES * kAbytes;
-  SmemBarriers *bars = reinterpret_cast<SmemBarriers *>(smem + STAGES * C::kStageBytes);
-  float *sx_stage = reinterpret_cast<float *>(smem + STAGES * C::kStageBytes + C::kBarBytes);
+  uint8_t *y_stage = smem + STAGES * C::kStageBytes;  // 1024-byte aligned
+  uint8_t *sc_ring = y_stage + C::kYStageBytes;       // 1024-byte aligned
+  SmemBarriers *bars = reinterpret_cast<SmemBarriers *>(sc_ring + C::kScBytes);
+  float *sx_stage = reinterpret_cast<float *>(sc_ring + C::kScBytes + C::kBarBytes);
   volatile uint32_t *abort_flag = &bars->abort;
 
   const int warp = threadIdx.x >> 5;
@@ -293,6 +336,10 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
       mbar_init(&bars->sf_full[s], C::kSfWarps > 0 ? C::kSfWarps : 1);
       mbar_init(&bars->sf_empty[s], 1);
     }
+    for (int s = 0; s < C::kScSlots; ++s) {
+      mbar_init(&bars->sc_full[s], 1);
+      mbar_init(&bars->sc_empty[s], EPI_WARPS);
+    }
     mbar_init(&bars->drain, C::kIssuers);
     bars->abort = 0;
     bars->is_last = 0;
@@ -301,6 +348,10 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (C::kScRing && args.sc_tma) {
+      tma_prefetch_desc(&tmSx);
+      tma_prefetch_desc(&tmSw);
+    }
   }
   if (warp == 1) {
     if (PAIR) {
@@ -316,6 +367,10 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
   if (PAIR) cluster_sync();  // the peer's barriers are initialised before any use
   tc_fence_after();
   const uint32_t tmem_base = bars->tmem_base;
+  if (C::kRegSplit) {
+    if (warp < 4) setmaxnreg_dec<C::kLowRegs>();
+    else setmaxnreg_inc<C::kHighRegs>();
+  }
 
   const int KB = shape.KB;
 
@@ -325,11 +380,30 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
       // ------------------------------------------------------------ TMA producer
       if (lane == 0) {
         uint32_t issued = 0, phase_bits = 0;  // per stage: ever issued, last phase
-        uint32_t it = 0;
+        uint32_t sc_issued = 0, sc_phase_bits = 0;
+        uint32_t it = 0, sq = 0;
         bool ok = true;
+        const bool sc_tma = C::kScRing && args.sc_tma;
         for (int u = cl_id; ok && u < shape.units; u += cl_num) {
           const Unit w = decode_unit<SWAP, PAIR>(u, shape.num_a_tiles, shape.splits, shape.kps, KB, BN, rank);
           for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
+            if (sc_tma && (kb - w.kb0) % C::kScQuad == 0) {
+              // promotion factors of K blocks kb .. kb+3: this CTA's s_x rows and
+              // the tile's weight-block scales, on this CTA's own barrier
+              const uint32_t q = sq % C::kScSlots, qph = (sq / C::kScSlots) & 1u;
+              if (!mbar_wait(&bars->sc_empty[q], qph ^ 1u, abort_flag, limit)) {
+                ok = false;
+                break;
+              }
+              uint8_t *slot = sc_ring + q * C::kScSlotBytes;
+              mbar_arrive_expect_tx(&bars->sc_full[q], C::kScXBytes + C::kScWBytes);
+              if (args.sx_layout == 0) tma_load_2d(slot, &tmSx, &bars->sc_full[q], kb, w.a_row0);
+              else tma_load_2d(slot, &tmSx, &bars->sc_full[q], w.a_row0, kb);
+              tma_load_2d(slot + C::kScXBytes, &tmSw, &bars->sc_full[q], kb, w.b_row0 / kBlockN);
+              sc_issued |= 1u << q;
+              sc_phase_bits = (sc_phase_bits & ~(1u << q)) | (qph << q);
+              ++sq;
+            }
             const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
             if (!mbar_wait(&bars->empty[s], ph ^ 1u, abort_flag, limit)) {
               ok = false;
@@ -360,6 +434,11 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
             if ((issued >> s) & 1u) {
               uint32_t dummy = 0;
               mbar_wait(&bars->full[s], (phase_bits >> s) & 1u, &dummy, limit);
+            }
+          for (int q = 0; q < C::kScSlots; ++q)
+            if ((sc_issued >> q) & 1u) {
+              uint32_t dummy = 0;
+              mbar_wait(&bars->sc_full[q], (sc_phase_bits >> q) & 1u, &dummy, limit);
             }
         }
       }
@@ -523,7 +602,7 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
     const int NBLK = (args.N + kBlockN - 1) / kBlockN;
     uint16_t *y = static_cast<uint16_t *>(args.y);
     const uint16_t *bias = static_cast<const uint16_t *>(args.bias);
-    uint32_t kit = 0, uit = 0;
+    uint32_t kit = 0, uit = 0, sq = 0;
     bool ok = true;
     for (int u = cl_id; u < shape.units; u += cl_num, ++uit) {
       const Unit w = decode_unit<SWAP, PAIR>(u, shape.num_a_tiles, shape.splits, shape.kps, KB, BN, rank);
@@ -539,49 +618,92 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
 #pragma unroll
           for (int j = 0; j < C::kCPT; ++j) acc[j] = 0.0f;
           const bool row_ok = m < args.M;
-          // every column of this thread lies in one 128-row weight block (kCPT
-          // divides 128 and tiles start on multiples of kCPT), so the promotion
-          // factor of a K block is s_x[m][kb] * s_w[nb][kb]; both are fetched two
-          // K blocks ahead so no global load sits on the per-block critical path
-          // (an arrive with release semantics also waits for loads still in flight)
-          const int nb = min(nbase / kBlockN, NBLK - 1);
-          const float *swrow = args.sw + static_cast<int64_t>(nb) * KB;
-          auto sx_at = [&](int kb) -> float {
-            if (!row_ok || kb >= w.kb1) return 0.0f;
-            return __ldg(args.sx + (args.sx_layout == 0
-                                        ? static_cast<int64_t>(m) * args.ldsx + kb
-                                        : static_cast<int64_t>(kb) * args.ldsx + m));
-          };
-          auto sw_at = [&](int kb) -> float { return kb < w.kb1 ? __ldg(swrow + kb) : 0.0f; };
-          float sx_cur = sx_at(w.kb0), sw_cur = sw_at(w.kb0);
-          float sx_nxt = sx_at(w.kb0 + 1), sw_nxt = sw_at(w.kb0 + 1);
-          for (int kb = w.kb0; kb < w.kb1 && ok; ++kb, ++kit) {
+          // one K block: wait for its partial, read it from TMEM, hand the
+          // buffer back to the MMA issuer, promote it with factor f
+          auto promote = [&](float f) -> bool {
             const uint32_t b = kit % ACCB, ph = (kit / ACCB) & 1u;
-            const float f = sx_cur * sw_cur;
-            sx_cur = sx_nxt;
-            sw_cur = sw_nxt;
-            if (!warp_wait(&bars->tfull[b], ph, abort_flag, limit)) {
-              ok = false;
-              break;
-            }
+            if (!warp_wait(&bars->tfull[b], ph, abort_flag, limit)) return false;
             tc_fence_after();
             const uint32_t tbase = tmem_base + lane_base + b * BN + col0;
+            // kLD columns per wait: with the register split, a thread's whole
+            // share of the partial is in flight in one or two rounds
 #pragma unroll
-            for (int c = 0; c < C::kCPT / C::kCW; ++c) {
-              uint32_t r[C::kCW];
-              tmem_ld_chunk<C::kCW>(tbase + c * C::kCW, r);
+            for (int g = 0; g < C::kCPT / C::kLD; ++g) {
+              uint32_t r[C::kLD];
+#pragma unroll
+              for (int c = 0; c < C::kLD / C::kCW; ++c)
+                tmem_ld_chunk<C::kCW>(tbase + g * C::kLD + c * C::kCW, r + c * C::kCW);
               tmem_ld_wait();
-              if (c == C::kCPT / C::kCW - 1) {
+              if (g == C::kCPT / C::kLD - 1) {
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) release_acc(b);
-                sx_nxt = sx_at(kb + 2);
-                sw_nxt = sw_at(kb + 2);
               }
 #pragma unroll
-              for (int j = 0; j < C::kCW; j += 2)
-                ffma2(acc[c * C::kCW + j], acc[c * C::kCW + j + 1], __uint_as_float(r[j]),
+              for (int j = 0; j < C::kLD; j += 2)
+                ffma2(acc[g * C::kLD + j], acc[g * C::kLD + j + 1], __uint_as_float(r[j]),
                       __uint_as_float(r[j + 1]), f, f);
+            }
+            ++kit;
+            return true;
+          };
+          // every column of this thread lies in one 128-row weight block (kCPT
+          // divides 128 and tiles start on multiples of kCPT), so the promotion
+          // factor of a K block is s_x[m][kb] * s_w[nb][kb]
+          if (C::kScRing && args.sc_tma) {
+            // factors from the shared-memory ring, four K blocks per slot:
+            // s_x row-major box [128 rows][4] or column-major box [4][128 rows],
+            // s_w box [2 weight blocks][4]
+            const int row = 32 * quarter + lane;
+            const int nbi = nbase / kBlockN - w.b_row0 / kBlockN;  // 0 or 1
+            for (int kq = w.kb0; kq < w.kb1 && ok; kq += C::kScQuad) {
+              const uint32_t q = sq % C::kScSlots, qph = (sq / C::kScSlots) & 1u;
+              if (!warp_wait(&bars->sc_full[q], qph, abort_flag, limit)) {
+                ok = false;
+                break;
+              }
+              const uint8_t *slot = sc_ring + q * C::kScSlotBytes;
+              float4 xv;
+              if (args.sx_layout == 0) {
+                xv = *reinterpret_cast<const float4 *>(slot + row * 16);
+              } else {
+                const float *xs = reinterpret_cast<const float *>(slot);
+                xv = make_float4(xs[row], xs[kBM + row], xs[2 * kBM + row], xs[3 * kBM + row]);
+              }
+              const float4 wv = *reinterpret_cast<const float4 *>(slot + C::kScXBytes + nbi * 16);
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&bars->sc_empty[q]);
+              ++sq;
+              const float fq[4] = {xv.x * wv.x, xv.y * wv.y, xv.z * wv.z, xv.w * wv.w};
+#pragma unroll
+              for (int u = 0; u < C::kScQuad; ++u) {
+                if (kq + u >= w.kb1) break;
+                if (!promote(fq[u])) {
+                  ok = false;
+                  break;
+                }
+              }
+            }
+          } else {
+            // factors loaded by each thread two K blocks ahead
+            const int nb = min(nbase / kBlockN, NBLK - 1);
+            const float *swrow = args.sw + static_cast<int64_t>(nb) * KB;
+            auto sx_at = [&](int kb) -> float {
+              if (!row_ok || kb >= w.kb1) return 0.0f;
+              return __ldg(args.sx + (args.sx_layout == 0
+                                          ? static_cast<int64_t>(m) * args.ldsx + kb
+                                          : static_cast<int64_t>(kb) * args.ldsx + m));
+            };
+            auto sw_at = [&](int kb) -> float { return kb < w.kb1 ? __ldg(swrow + kb) : 0.0f; };
+            float sx_cur = sx_at(w.kb0), sw_cur = sw_at(w.kb0);
+            float sx_nxt = sx_at(w.kb0 + 1), sw_nxt = sw_at(w.kb0 + 1);
+            for (int kb = w.kb0; kb < w.kb1 && ok; ++kb) {
+              const float f = sx_cur * sw_cur;
+              sx_cur = sx_nxt;
+              sw_cur = sw_nxt;
+              sx_nxt = sx_at(kb + 2);
+              sw_nxt = sw_at(kb + 2);
+              if (!promote(f)) ok = false;
             }
           }
           // all epilogue warps agree on the outcome before anything is stored
@@ -589,12 +711,44 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
             ok = false;
             break;
           }
-          if (m < args.M) {
-            if (bias) {
+          if (bias) {
 #pragma unroll
-              for (int j = 0; j < C::kCPT; ++j)
-                if (nbase + j < args.N) acc[j] += bf16_bits_to_float(bias[nbase + j]);
+            for (int j = 0; j < C::kCPT; ++j)
+              if (nbase + j < args.N) acc[j] += bf16_bits_to_float(bias[nbase + j]);
+          }
+          if (C::kTmaStoreY && args.y_tma) {
+            // BF16 rows into this warp's staging boxes (16-byte chunk c of row r
+            // at chunk position c ^ (r % 8): the 128-byte swizzle the tensor map
+            // names, and conflict-free), then one TMA store per box.  The
+            // previous tile's stores must have finished reading the boxes.
+            uint8_t *stg = y_stage + ew * (32 * C::kCPT * 2);
+            if (lane == 0) bulk_wait_group_read0();
+            __syncwarp();
+#pragma unroll
+            for (int bx = 0; bx < C::kCPT / C::kYBoxCols; ++bx) {
+              uint8_t *rowp = stg + bx * C::kYBoxBytes + lane * 128;
+#pragma unroll
+              for (int c = 0; c < 8; ++c) {
+                const float *v = acc + bx * C::kYBoxCols + c * 8;
+                uint4 q;
+                q.x = pack_bf16x2(v[0], v[1]);
+                q.y = pack_bf16x2(v[2], v[3]);
+                q.z = pack_bf16x2(v[4], v[5]);
+                q.w = pack_bf16x2(v[6], v[7]);
+                *reinterpret_cast<uint4 *>(rowp + ((c ^ (lane & 7)) << 4)) = q;
+              }
             }
+            fence_proxy_async_smem();
+            __syncwarp();
+            const int row0 = w.a_row0 + 32 * quarter;
+            if (lane == 0 && row0 < args.M) {
+#pragma unroll
+              for (int bx = 0; bx < C::kCPT / C::kYBoxCols; ++bx)
+                if (nbase + bx * C::kYBoxCols < args.N)
+                  tma_store_2d(&tmY, stg + bx * C::kYBoxBytes, nbase + bx * C::kYBoxCols, row0);
+              bulk_commit_group();
+            }
+          } else if (m < args.M) {
             store_row<C::kCPT>(y, acc, m, nbase, args);
           }
         } else {
@@ -787,6 +941,8 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
         }
       }
     }
+    // the staging boxes stay in use until this warp's TMA stores complete
+    if (C::kTmaStoreY && lane == 0) bulk_wait_group0();
     if (!ok && et == 0) record_timeout(args);
   }
 
@@ -808,7 +964,28 @@ template <int MODE, bool SWAP, int BN, int STAGES, int EPI_WARPS, int ACCB, bool
 cudaError_t run(const GemmArgs &a, const void *q_act, const void *w, const LaunchShape &sh,
                 int grid, cudaStream_t st, int *status) {
   using C = Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, PAIR>;
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, ty, tsx, tsw;
+  std::memset(&ty, 0, sizeof ty);
+  std::memset(&tsx, 0, sizeof tsx);
+  std::memset(&tsw, 0, sizeof tsw);
+  GemmArgs args = a;
+  args.y_tma = 0;
+  args.sc_tma = 0;
+  auto al16 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  if (C::kTmaStoreY && a.N % 8 == 0 && al16(a.y))
+    args.y_tma = cached_bf16_rows_map(&ty, a.y, a.M, a.N, C::kYBoxCols, 32) ? 1 : 0;
+  if (C::kScRing) {
+    // s_x: row-major [M][KB] in [128 rows x 4 K blocks] boxes, or column-major
+    // [KB][ldsx] in [4 K blocks x 128 rows] boxes; s_w [NB][KB] in [2 x 4] boxes
+    const int KB = (a.K + 127) / 128, NB = (a.N + kBlockN - 1) / kBlockN;
+    const bool sx_ok = al16(a.sx) && a.ldsx % 4 == 0 &&
+                       (a.sx_layout == 0
+                            ? cached_f32_map(&tsx, a.sx, a.M, KB, a.ldsx, C::kScQuad, kBM)
+                            : cached_f32_map(&tsx, a.sx, KB, a.ldsx, a.ldsx, kBM, C::kScQuad));
+    const bool sw_ok = al16(a.sw) && KB % 4 == 0 &&
+                       cached_f32_map(&tsw, a.sw, NB, KB, KB, C::kScQuad, 2);
+    args.sc_tma = (sx_ok && sw_ok) ? 1 : 0;
+  }
   const void *a_ptr = SWAP ? w : q_act;
   const void *b_ptr = SWAP ? q_act : w;
   const int64_t a_rows = SWAP ? a.N : a.M;
@@ -831,8 +1008,23 @@ cudaError_t run(const GemmArgs &a, const void *q_act, const void *w, const Launc
   });
   cudaError_t e = attr_err;
   if (e != cudaSuccess) return e;
+  if (C::kRegSplit) {
+    // setmaxnreg.inc waits for registers the block was launched with: refuse
+    // to launch unless the compiled register count covers the split
+    static std::once_flag regs_once;
+    static int regs = 0;
+    std::call_once(regs_once, [&] {
+      cudaFuncAttributes fa;
+      if (cudaFuncGetAttributes(&fa, kern) == cudaSuccess) regs = fa.numRegs;
+    });
+    if (static_cast<long>(regs) * C::kThreads <
+        128L * C::kLowRegs + static_cast<long>(C::kThreads - 128) * C::kHighRegs) {
+      *status = 4;  // FP8BQ_ERR_UNSUPPORTED: build does not fit the register split
+      return cudaSuccess;
+    }
+  }
   if (!PAIR) {
-    kern<<<grid, C::kThreads, smem, st>>>(ta, tb, a, sh);
+    kern<<<grid, C::kThreads, smem, st>>>(ta, tb, ty, tsx, tsw, args, sh);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg = {};
@@ -856,7 +1048,7 @@ cudaError_t run(const GemmArgs &a, const void *q_act, const void *w, const Launc
   }
   const int clusters = grid < max_clusters ? grid : max_clusters;
   cfg.gridDim = dim3(2 * clusters, 1, 1);
-  e = cudaLaunchKernelEx(&cfg, kern, ta, tb, a, sh);
+  e = cudaLaunchKernelEx(&cfg, kern, ta, tb, ty, tsx, tsw, args, sh);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -76,6 +76,95 @@ bool cached_kmajor_map(CUtensorMap *m, const void *base, int64_t rows, int64_t K
   return true;
 }
 
+bool cached_f32_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols,
+                    int64_t pitch, int box_cols, int box_rows) {
+  struct Entry {
+    const void *base;
+    int64_t rows, cols, pitch;
+    int bc, br;
+    CUtensorMap map;
+  };
+  constexpr int kEntries = 16;
+  static Entry cache[kEntries];
+  static int used = 0, next = 0;
+  static std::mutex mu;
+  {
+    std::lock_guard<std::mutex> g(mu);
+    for (int i = 0; i < used; ++i)
+      if (cache[i].base == base && cache[i].rows == rows && cache[i].cols == cols &&
+          cache[i].pitch == pitch && cache[i].bc == box_cols && cache[i].br == box_rows) {
+        *m = cache[i].map;
+        return true;
+      }
+  }
+  auto enc = get_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(pitch) * 4};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void *>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return false;
+  std::lock_guard<std::mutex> g(mu);
+  Entry &e = cache[next];
+  e.base = base;
+  e.rows = rows;
+  e.cols = cols;
+  e.pitch = pitch;
+  e.bc = box_cols;
+  e.br = box_rows;
+  e.map = *m;
+  next = (next + 1) % kEntries;
+  if (used < kEntries) ++used;
+  return true;
+}
+
+bool cached_bf16_rows_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols,
+                          int box_cols, int box_rows) {
+  struct Entry {
+    const void *base;
+    int64_t rows, cols;
+    int bc, br;
+    CUtensorMap map;
+  };
+  constexpr int kEntries = 16;
+  static Entry cache[kEntries];
+  static int used = 0, next = 0;
+  static std::mutex mu;
+  {
+    std::lock_guard<std::mutex> g(mu);
+    for (int i = 0; i < used; ++i)
+      if (cache[i].base == base && cache[i].rows == rows && cache[i].cols == cols &&
+          cache[i].bc == box_cols && cache[i].br == box_rows) {
+        *m = cache[i].map;
+        return true;
+      }
+  }
+  auto enc = get_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return false;
+  std::lock_guard<std::mutex> g(mu);
+  Entry &e = cache[next];
+  e.base = base;
+  e.rows = rows;
+  e.cols = cols;
+  e.bc = box_cols;
+  e.br = box_rows;
+  e.map = *m;
+  next = (next + 1) % kEntries;
+  if (used < kEntries) ++used;
+  return true;
+}
+
 // [status word | split-K tile counters | split-K FP32 partials | fused: Q | fused: scales]
 WorkspaceLayout workspace_layout(int op, int64_t M, int64_t N, int64_t K) {
   auto up = [](size_t v) { return (v + 255) / 256 * 256; };
@@ -153,7 +242,7 @@ int launch_gemm(const GemmArgs &a, const void *q_act, const void *w, const Devic
   long best_cost = -1;
   for (int bn : {256, 192}) {
     const long units = static_cast<long>(sh.num_a_tiles) * ((a.N + bn - 1) / bn);
-    const long per_col = (a.mode == kModeBlock && bn == 256) ? 95 : 100;
+    const long per_col = (a.mode == kModeBlock && bn == 256) ? 80 : 100;
     const long cost = (units + pairs - 1) / pairs * bn * per_col;
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;

@@ -42,7 +42,9 @@ def _gemm(qa, sa, qw, sw, bias=None, layout=fb.SCALE_ROW_MAJOR, ws=None):
 
 @pytest.mark.parametrize("M,N,K", [(16, 384, 256), (5, 200, 208), (1, 128, 128),
                                    (64, 384, 1024), (128, 256, 128), (200, 520, 384),
-                                   (256, 512, 2048), (131, 257 * 8, 144), (65, 136, 16)])
+                                   (256, 512, 2048), (131, 257 * 8, 144), (65, 136, 16),
+                                   (130, 203, 256), (257, 300, 512), (300, 640, 1024),
+                                   (520, 392, 512)])
 @pytest.mark.parametrize("layout", [fb.SCALE_ROW_MAJOR, fb.SCALE_COL_MAJOR])
 def test_gemm_small_shapes(M, N, K, layout):
     qa, sa = oracle.quant_group(si.activations(M, K))
