@@ -7,7 +7,7 @@ namespace fp8bq {
 cudaError_t run_block_pair(int bn, const GemmArgs &a, const void *q, const void *w,
                            const LaunchShape &sh, int grid, cudaStream_t st, int *status) {
   if (bn == 192) return run<kModeBlock, false, 192, 6, 12, 2, true>(a, q, w, sh, grid, st, status);
-  return run<kModeBlock, false, 256, 4, 8, 2, true>(a, q, w, sh, grid, st, status);
+  return run<kModeBlock, false, 256, 5, 8, 2, true>(a, q, w, sh, grid, st, status);
 }
 
 cudaError_t run_block_swap(int bn, const GemmArgs &a, const void *q, const void *w,

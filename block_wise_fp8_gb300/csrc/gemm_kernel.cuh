@@ -104,7 +104,9 @@ struct Cfg {
   static constexpr bool kTmaStoreY = (MODE == kModeBlock) && PAIR;
   static constexpr int kYBoxCols = 64;
   static constexpr int kYBoxBytes = 32 * kYBoxCols * 2;
-  static constexpr int kYStageBytes = kTmaStoreY ? kBM * BN * 2 : 0;
+  // one box per epilogue warp; a thread's columns beyond one box go out in
+  // further rounds through the same box
+  static constexpr int kYStageBytes = kTmaStoreY ? EPI_WARPS * kYBoxBytes : 0;
   static constexpr int kBbytes = kBrows * 128;
   static constexpr int kStageBytes = kAbytes + kBbytes;
   // block pair tiles: promotion factors come through a shared-memory ring
@@ -717,16 +719,17 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
               if (nbase + j < args.N) acc[j] += bf16_bits_to_float(bias[nbase + j]);
           }
           if (C::kTmaStoreY && args.y_tma) {
-            // BF16 rows into this warp's staging boxes (16-byte chunk c of row r
+            // BF16 rows into this warp's staging box (16-byte chunk c of row r
             // at chunk position c ^ (r % 8): the 128-byte swizzle the tensor map
-            // names, and conflict-free), then one TMA store per box.  The
-            // previous tile's stores must have finished reading the boxes.
-            uint8_t *stg = y_stage + ew * (32 * C::kCPT * 2);
-            if (lane == 0) bulk_wait_group_read0();
-            __syncwarp();
+            // names, and conflict-free), then one TMA store per 64 columns.
+            // Before each refill the previous store must have finished reading.
+            uint8_t *stg = y_stage + ew * C::kYBoxBytes;
+            const int row0 = w.a_row0 + 32 * quarter;
 #pragma unroll
             for (int bx = 0; bx < C::kCPT / C::kYBoxCols; ++bx) {
-              uint8_t *rowp = stg + bx * C::kYBoxBytes + lane * 128;
+              if (lane == 0) bulk_wait_group_read0();
+              __syncwarp();
+              uint8_t *rowp = stg + lane * 128;
 #pragma unroll
               for (int c = 0; c < 8; ++c) {
                 const float *v = acc + bx * C::kYBoxCols + c * 8;
@@ -737,16 +740,12 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
                 q.w = pack_bf16x2(v[6], v[7]);
                 *reinterpret_cast<uint4 *>(rowp + ((c ^ (lane & 7)) << 4)) = q;
               }
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            const int row0 = w.a_row0 + 32 * quarter;
-            if (lane == 0 && row0 < args.M) {
-#pragma unroll
-              for (int bx = 0; bx < C::kCPT / C::kYBoxCols; ++bx)
-                if (nbase + bx * C::kYBoxCols < args.N)
-                  tma_store_2d(&tmY, stg + bx * C::kYBoxBytes, nbase + bx * C::kYBoxCols, row0);
-              bulk_commit_group();
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0 && row0 < args.M && nbase + bx * C::kYBoxCols < args.N) {
+                tma_store_2d(&tmY, stg, nbase + bx * C::kYBoxCols, row0);
+                bulk_commit_group();
+              }
             }
           } else if (m < args.M) {
             store_row<C::kCPT>(y, acc, m, nbase, args);
