@@ -5,6 +5,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 
 namespace fp8bq {
 
@@ -16,14 +17,35 @@ constexpr int kMaxParts = 64; // static path: maximum number of output partition
 // Status values stored in the workspace status word (same numbers as fp8bq_status).
 constexpr uint32_t kStatusTimeout = 8;
 
+// Every kernel of the library is launched with programmatic stream
+// serialization: it may start while the preceding kernel of the stream is
+// finishing, and it executes griddepcontrol.wait before it reads or writes any
+// global memory that another kernel may produce or consume (the GEMMs only
+// prefetch weight tiles into L2 before that point).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
 // ---------------------------------------------------------------- quant kernels
 
 void launch_quant_group(const void *x, int64_t M, int64_t K, int64_t ldx, void *q, float *s,
-                        int s_layout, cudaStream_t st);
+                        int s_layout, int num_sms, cudaStream_t st);
 void launch_quant_mx(const void *x, int64_t M, int64_t K, int64_t ldx, void *q, uint8_t *s,
-                     cudaStream_t st);
+                     int num_sms, cudaStream_t st);
 void launch_quant_static(const void *x, int64_t M, int64_t K, int64_t ldx, const float *s,
-                         void *q, cudaStream_t st);
+                         void *q, int num_sms, cudaStream_t st);
 void launch_quant_weight_block(const void *w, int64_t N, int64_t K, int64_t ldw, void *q,
                                float *s, cudaStream_t st);
 void launch_absmax_scale(const void *x, int64_t rows, int64_t K, int64_t ldx, float *s,

@@ -302,7 +302,7 @@ int fp8bq_quant_act(const void *x, int64_t M, int64_t K, int64_t ldx, void *q, f
   if (M == 0) return FP8BQ_OK;
   DeviceInfo dev;
   RETURN_IF(device_info(&dev));
-  launch_quant_group(x, M, K, ldx, q, s, s_layout, static_cast<cudaStream_t>(stream));
+  launch_quant_group(x, M, K, ldx, q, s, s_layout, dev.num_sms, static_cast<cudaStream_t>(stream));
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? FP8BQ_OK : cuda_fail(e);
 }
@@ -345,7 +345,7 @@ int fp8bq_linear(const void *x, int64_t ldx, const void *w, const float *s_w, co
   float *s = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + L.s);
   // row-major scales: each epilogue thread walks its own row's scales, which
   // stay in L1 across consecutive K blocks
-  launch_quant_group(x, M, K, ldx, q, s, FP8BQ_SCALE_ROW_MAJOR, st);
+  launch_quant_group(x, M, K, ldx, q, s, FP8BQ_SCALE_ROW_MAJOR, dev.num_sms, st);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);
   return gemm_block_impl(q, s, FP8BQ_SCALE_ROW_MAJOR, w, s_w, bias, y, M, N, K, ws,
@@ -363,7 +363,7 @@ int fp8bq_mx_quant_act(const void *x, int64_t M, int64_t K, int64_t ldx, void *q
   if (M == 0) return FP8BQ_OK;
   DeviceInfo dev;
   RETURN_IF(device_info(&dev));
-  launch_quant_mx(x, M, K, ldx, q, s, static_cast<cudaStream_t>(stream));
+  launch_quant_mx(x, M, K, ldx, q, s, dev.num_sms, static_cast<cudaStream_t>(stream));
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? FP8BQ_OK : cuda_fail(e);
 }
@@ -400,7 +400,7 @@ int fp8bq_mx_linear(const void *x, int64_t ldx, const void *w, const uint8_t *s_
   const WorkspaceLayout L = workspace_layout(FP8BQ_OP_MX_LINEAR, M, N, K);
   uint8_t *q = static_cast<uint8_t *>(ws) + L.q;
   uint8_t *s = static_cast<uint8_t *>(ws) + L.s;
-  launch_quant_mx(x, M, K, ldx, q, s, st);
+  launch_quant_mx(x, M, K, ldx, q, s, dev.num_sms, st);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);
   return gemm_mx_impl(q, s, w, s_w, bias, y, M, N, K, ws, FP8BQ_OP_MX_LINEAR, st, dev);
@@ -417,7 +417,7 @@ int fp8bq_static_quant_act(const void *x, int64_t M, int64_t K, int64_t ldx, con
   if (M == 0) return FP8BQ_OK;
   DeviceInfo dev;
   RETURN_IF(device_info(&dev));
-  launch_quant_static(x, M, K, ldx, s_x, q, static_cast<cudaStream_t>(stream));
+  launch_quant_static(x, M, K, ldx, s_x, q, dev.num_sms, static_cast<cudaStream_t>(stream));
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? FP8BQ_OK : cuda_fail(e);
 }
@@ -459,7 +459,7 @@ int fp8bq_static_linear(const void *x, int64_t ldx, const float *s_x, const void
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const WorkspaceLayout L = workspace_layout(FP8BQ_OP_STATIC_LINEAR, M, N, K);
   uint8_t *q = static_cast<uint8_t *>(ws) + L.q;
-  launch_quant_static(x, M, K, ldx, s_x, q, st);
+  launch_quant_static(x, M, K, ldx, s_x, q, dev.num_sms, st);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);
   return gemm_static_impl(q, s_x, w, s_w_part, part_sizes_host, n_parts, bias, y, M, N, K, ws,

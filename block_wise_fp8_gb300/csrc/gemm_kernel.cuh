@@ -369,6 +369,24 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
   if (PAIR) cluster_sync();  // the peer's barriers are initialised before any use
   tc_fence_after();
   const uint32_t tmem_base = bars->tmem_base;
+
+  // Programmatic dependent launch: the next kernel of the stream may be
+  // scheduled now.  Until the preceding kernel has completed (griddepcontrol.wait)
+  // this CTA touches no global memory except L2 prefetches of its first weight
+  // tiles; L2 is the point of coherence, so a prefetch cannot make a later load
+  // see stale data even if the preceding kernel writes those weights.
+  griddep_launch_dependents();
+  if (warp == 0 && lane == 0 && cl_id < shape.units) {
+    const Unit w0 = decode_unit<SWAP, PAIR>(cl_id, shape.num_a_tiles, shape.splits, shape.kps,
+                                            shape.KB, BN, rank);
+    const int npf = min(w0.kb1 - w0.kb0, SWAP ? 64 : 8);
+    for (int i = 0; i < npf; ++i) {
+      if (SWAP) tma_prefetch_l2_2d(&tmA, (w0.kb0 + i) * 128, w0.a_row0);
+      else tma_prefetch_l2_2d(&tmB, (w0.kb0 + i) * 128, w0.b_load_row0);
+    }
+  }
+  griddep_wait();
+
   if (C::kRegSplit) {
     if (warp < 4) setmaxnreg_dec<C::kLowRegs>();
     else setmaxnreg_inc<C::kHighRegs>();
@@ -1023,20 +1041,23 @@ cudaError_t run(const GemmArgs &a, const void *q_act, const void *w, const Launc
     }
   }
   if (!PAIR) {
-    kern<<<grid, C::kThreads, smem, st>>>(ta, tb, ty, tsx, tsw, args, sh);
+    e = launch_pdl(kern, grid, C::kThreads, smem, st, ta, tb, ty, tsx, tsw, args, sh);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.blockDim = dim3(C::kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   static int max_clusters = 0;  // per variant; the library targets one device type
   if (max_clusters == 0) {
     cfg.gridDim = dim3(2 * grid, 1, 1);

@@ -9,6 +9,7 @@
 #include <cuda_fp8.h>
 
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace fp8bq {
 namespace {
@@ -76,104 +77,186 @@ __device__ __forceinline__ uint4 to_e4m3x16(const float (&t)[16]) {
 
 // ---------------------------------------------------------------- group-128 activation quant
 // 8 threads per 128-channel group, 16 channels (32 bytes) per thread; a
-// partial last group masks whole 16-channel chunks (K % 16 == 0).
+// partial last group masks whole 16-channel chunks (K % 16 == 0).  The grid is
+// persistent: each warp takes 4 consecutive groups per step and walks the
+// groups with the grid's stride, loading its next chunk before converting the
+// current one, so two chunks per thread are in flight.
 __global__ void __launch_bounds__(kThreads) quant_group128_kernel(
     const uint8_t *__restrict__ x, int64_t M, int K, int64_t ldx_bytes, int G,
     uint8_t *__restrict__ q, float *__restrict__ s, int s_layout, int64_t lds) {
-  const int64_t gid = static_cast<int64_t>(blockIdx.x) * (kThreads / 8) + (threadIdx.x >> 3);
-  const int sub = threadIdx.x & 7;
-  const bool in_range = gid < M * G;
-  const int64_t row = in_range ? gid / G : 0;
-  const int g = in_range ? static_cast<int>(gid - row * G) : 0;
-  const int k = g * 128 + sub * 16;
-  const bool valid = in_range && k < K;
-
-  uint4 v[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
-  if (valid) {
-    const uint8_t *p = x + row * ldx_bytes + static_cast<int64_t>(k) * 2;
-    v[0] = ld_stream(p);
-    v[1] = ld_stream(p + 16);
-  }
-  float f[16];
-  unpack16(v, f);
-  float amax = amax16(f);
-  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
-  const float sg = __fdiv_rn(fmaxf(amax, kFloor), 448.0f);
-  const float rg = __frcp_rn(sg);
-  float t[16];
+  griddep_launch_dependents();
+  griddep_wait();
+  const int lane = threadIdx.x & 31, sub = lane & 7;
+  const int64_t total = M * G;
+  const int64_t step = static_cast<int64_t>(gridDim.x) * (kThreads / 8);  // groups per step
+  const int64_t warp_g0 = (static_cast<int64_t>(blockIdx.x) * (kThreads / 32) + (threadIdx.x >> 5)) * 4;
+  const int64_t gid = warp_g0 + (lane >> 3);
+  // (row, group) of this thread's group, advanced by (drow, dg) per step
+  int64_t row = gid / G;
+  int g = static_cast<int>(gid - row * G);
+  const int64_t drow = step / G;
+  const int dg = static_cast<int>(step - drow * G);
+  auto load = [&](int64_t r, int gg, uint4 (&v)[2]) {
+    const int k = gg * 128 + sub * 16;
+    if (r < M && k < K) {
+      const uint8_t *p = x + r * ldx_bytes + static_cast<int64_t>(k) * 2;
+      v[0] = ld_stream(p);
+      v[1] = ld_stream(p + 16);
+    } else {
+      v[0] = v[1] = make_uint4(0, 0, 0, 0);
+    }
+  };
+  uint4 cur[2];
+  load(row, g, cur);
+  for (int64_t base = warp_g0; base < total; base += step) {
+    int64_t row_n = row + drow;
+    int g_n = g + dg;
+    if (g_n >= G) {
+      g_n -= G;
+      ++row_n;
+    }
+    uint4 nxt[2];
+    load(row_n, g_n, nxt);
+    float f[16];
+    unpack16(cur, f);
+    float amax = amax16(f);
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+    const float sg = __fdiv_rn(fmaxf(amax, kFloor), 448.0f);
+    const float rg = __frcp_rn(sg);
+    float t[16];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) t[i] = div_by_scale(f[i], sg, rg);
-  const uint4 out = to_e4m3x16(t);
-  if (valid) *reinterpret_cast<uint4 *>(q + row * K + k) = out;
-  if (in_range && sub == 0) {
-    if (s_layout == 0) s[row * lds + g] = sg;
-    else s[static_cast<int64_t>(g) * lds + row] = sg;
+    for (int i = 0; i < 16; ++i) t[i] = div_by_scale(f[i], sg, rg);
+    const uint4 out = to_e4m3x16(t);
+    const int k = g * 128 + sub * 16;
+    if (row < M) {
+      if (k < K) *reinterpret_cast<uint4 *>(q + row * K + k) = out;
+      if (sub == 0) {
+        if (s_layout == 0) s[row * lds + g] = sg;
+        else s[static_cast<int64_t>(g) * lds + row] = sg;
+      }
+    }
+    cur[0] = nxt[0];
+    cur[1] = nxt[1];
+    row = row_n;
+    g = g_n;
   }
 }
 
 // ---------------------------------------------------------------- MXFP8 [1,32] quant
-// 2 threads per 32-channel group.  e = ceil(log2(r)), r = max(amax,1e-10)/448
-// read from r's bits (r is a positive normal float): biased exponent plus one
-// unless the mantissa is zero.  The UE8M0 code is e + 127.
+// 2 threads per 32-channel group (16 per warp step), persistent like the
+// group-128 kernel.  e = ceil(log2(r)), r = max(amax,1e-10)/448 read from r's
+// bits (r is a positive normal float): biased exponent plus one unless the
+// mantissa is zero.  The UE8M0 code is e + 127.
 __global__ void __launch_bounds__(kThreads) quant_mx_kernel(const uint8_t *__restrict__ x,
                                                             int64_t M, int K,
                                                             int64_t ldx_bytes,
                                                             uint8_t *__restrict__ q,
                                                             uint8_t *__restrict__ s) {
+  griddep_launch_dependents();
+  griddep_wait();
   const int G = K / 32;
-  const int64_t gid = static_cast<int64_t>(blockIdx.x) * (kThreads / 2) + (threadIdx.x >> 1);
-  const int sub = threadIdx.x & 1;
-  const bool valid = gid < M * G;
-  const int64_t row = valid ? gid / G : 0;
-  const int g = valid ? static_cast<int>(gid - row * G) : 0;
-  const int k = g * 32 + sub * 16;
-  uint4 v[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
-  if (valid) {
-    const uint8_t *p = x + row * ldx_bytes + static_cast<int64_t>(k) * 2;
-    v[0] = ld_stream(p);
-    v[1] = ld_stream(p + 16);
-  }
-  float f[16];
-  unpack16(v, f);
-  float amax = amax16(f);
-  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-  const float r = __fdiv_rn(fmaxf(amax, kFloor), 448.0f);
-  const uint32_t rb = __float_as_uint(r);
-  const uint32_t u = (rb >> 23) + ((rb & 0x7FFFFFu) != 0u ? 1u : 0u);  // e + 127
-  const float inv = __uint_as_float((254u - u) << 23);                 // 2^-e, exact
-  float t[16];
+  const int lane = threadIdx.x & 31, sub = lane & 1;
+  const int64_t total = M * G;
+  const int64_t step = static_cast<int64_t>(gridDim.x) * (kThreads / 2);
+  const int64_t warp_g0 = (static_cast<int64_t>(blockIdx.x) * (kThreads / 32) + (threadIdx.x >> 5)) * 16;
+  const int64_t gid = warp_g0 + (lane >> 1);
+  int64_t row = gid / G;
+  int g = static_cast<int>(gid - row * G);
+  const int64_t drow = step / G;
+  const int dg = static_cast<int>(step - drow * G);
+  auto load = [&](int64_t r, int gg, uint4 (&v)[2]) {
+    if (r < M) {
+      const uint8_t *p = x + r * ldx_bytes + static_cast<int64_t>(gg * 32 + sub * 16) * 2;
+      v[0] = ld_stream(p);
+      v[1] = ld_stream(p + 16);
+    } else {
+      v[0] = v[1] = make_uint4(0, 0, 0, 0);
+    }
+  };
+  uint4 cur[2];
+  load(row, g, cur);
+  for (int64_t base = warp_g0; base < total; base += step) {
+    int64_t row_n = row + drow;
+    int g_n = g + dg;
+    if (g_n >= G) {
+      g_n -= G;
+      ++row_n;
+    }
+    uint4 nxt[2];
+    load(row_n, g_n, nxt);
+    float f[16];
+    unpack16(cur, f);
+    float amax = amax16(f);
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    const float r = __fdiv_rn(fmaxf(amax, kFloor), 448.0f);
+    const uint32_t rb = __float_as_uint(r);
+    const uint32_t u = (rb >> 23) + ((rb & 0x7FFFFFu) != 0u ? 1u : 0u);  // e + 127
+    const float inv = __uint_as_float((254u - u) << 23);                 // 2^-e, exact
+    float t[16];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) t[i] = __fmul_rn(f[i], inv);
-  const uint4 out = to_e4m3x16(t);
-  if (valid) {
-    *reinterpret_cast<uint4 *>(q + row * K + k) = out;
-    if (sub == 0) s[row * G + g] = static_cast<uint8_t>(u);
+    for (int i = 0; i < 16; ++i) t[i] = __fmul_rn(f[i], inv);
+    const uint4 out = to_e4m3x16(t);
+    if (row < M) {
+      *reinterpret_cast<uint4 *>(q + row * K + g * 32 + sub * 16) = out;
+      if (sub == 0) s[row * G + g] = static_cast<uint8_t>(u);
+    }
+    cur[0] = nxt[0];
+    cur[1] = nxt[1];
+    row = row_n;
+    g = g_n;
   }
 }
 
 // ---------------------------------------------------------------- static per-tensor quant
+// One thread per 16-channel chunk, persistent grid, next chunk loaded first.
 __global__ void __launch_bounds__(kThreads) quant_static_kernel(const uint8_t *__restrict__ x,
                                                                 int64_t M, int K,
                                                                 int64_t ldx_bytes,
                                                                 const float *__restrict__ s_ptr,
                                                                 uint8_t *__restrict__ q) {
+  griddep_launch_dependents();
+  griddep_wait();
   const int C = K / 16;
-  const int64_t cid = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
-  if (cid >= M * C) return;
-  const int64_t row = cid / C;
-  const int k = static_cast<int>(cid - row * C) * 16;
+  const int64_t total = M * C;
+  const int64_t step = static_cast<int64_t>(gridDim.x) * kThreads;
+  const int64_t cid0 = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+  int64_t row = cid0 / C;
+  int c = static_cast<int>(cid0 - row * C);
+  const int64_t drow = step / C;
+  const int dc = static_cast<int>(step - drow * C);
   const float sv = __ldg(s_ptr);
   const float rv = __frcp_rn(sv);
-  const uint8_t *p = x + row * ldx_bytes + static_cast<int64_t>(k) * 2;
-  uint4 v[2] = {ld_stream(p), ld_stream(p + 16)};
-  float f[16];
-  unpack16(v, f);
-  float t[16];
+  auto load = [&](int64_t r, int cc, uint4 (&v)[2]) {
+    if (r < M) {
+      const uint8_t *p = x + r * ldx_bytes + static_cast<int64_t>(cc) * 32;
+      v[0] = ld_stream(p);
+      v[1] = ld_stream(p + 16);
+    }
+  };
+  uint4 cur[2];
+  load(row, c, cur);
+  for (int64_t cid = cid0; cid < total; cid += step) {
+    int64_t row_n = row + drow;
+    int c_n = c + dc;
+    if (c_n >= C) {
+      c_n -= C;
+      ++row_n;
+    }
+    uint4 nxt[2];
+    load(row_n, c_n, nxt);
+    float f[16];
+    unpack16(cur, f);
+    float t[16];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) t[i] = div_by_scale(f[i], sv, rv);
-  *reinterpret_cast<uint4 *>(q + row * K + k) = to_e4m3x16(t);
+    for (int i = 0; i < 16; ++i) t[i] = div_by_scale(f[i], sv, rv);
+    *reinterpret_cast<uint4 *>(q + row * K + static_cast<int64_t>(c) * 16) = to_e4m3x16(t);
+    cur[0] = nxt[0];
+    cur[1] = nxt[1];
+    row = row_n;
+    c = c_n;
+  }
 }
 
 // ---------------------------------------------------------------- 128x128 weight blocks
@@ -182,6 +265,8 @@ __global__ void __launch_bounds__(kThreads) quant_weight_block_kernel(
     const uint8_t *__restrict__ w, int N, int K, int64_t ldw_bytes, uint8_t *__restrict__ q,
     float *__restrict__ s, int KB) {
   __shared__ float red[kThreads / 32];
+  griddep_launch_dependents();
+  griddep_wait();
   const int nb = blockIdx.y, kb = blockIdx.x;
   const int r = nb * 128 + (threadIdx.x >> 1);
   const int kbase = kb * 128 + (threadIdx.x & 1) * 64;
@@ -228,6 +313,8 @@ __global__ void __launch_bounds__(kThreads) absmax_kernel(const uint8_t *__restr
                                                           int64_t rows, int K,
                                                           int64_t ldx_bytes,
                                                           uint32_t *__restrict__ acc) {
+  griddep_launch_dependents();
+  griddep_wait();
   const int C = K / 16;
   const int64_t total = rows * C;
   float m = 0.0f;
@@ -247,6 +334,8 @@ __global__ void __launch_bounds__(kThreads) absmax_kernel(const uint8_t *__restr
 }
 
 __global__ void absmax_finalize_kernel(float *s) {
+  griddep_launch_dependents();
+  griddep_wait();
   const float amax = __uint_as_float(*reinterpret_cast<uint32_t *>(s));
   *s = __fdiv_rn(fmaxf(amax, kFloor), 448.0f);
 }
@@ -257,36 +346,52 @@ inline unsigned blocks_for(int64_t work, int per_block) {
 
 }  // namespace
 
+// Persistent grids: enough CTAs for the work, at most as many as fit on the
+// device at once (the kernel's occupancy, queried once per kernel).
+template <typename Kern>
+unsigned persistent_grid(Kern kern, int64_t work, int per_block, int num_sms) {
+  static int per_sm = [&] {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, 0) != cudaSuccess ||
+        n < 1)
+      n = 1;
+    return n;
+  }();
+  const int64_t need = (work + per_block - 1) / per_block;
+  const int64_t cap = static_cast<int64_t>(num_sms) * per_sm;
+  return static_cast<unsigned>(need < 1 ? 1 : need < cap ? need : cap);
+}
+
 void launch_quant_group(const void *x, int64_t M, int64_t K, int64_t ldx, void *q, float *s,
-                        int s_layout, cudaStream_t st) {
+                        int s_layout, int num_sms, cudaStream_t st) {
   const int G = static_cast<int>((K + 127) / 128);
   const int64_t lds = s_layout == 0 ? G : ((M + 3) / 4) * 4;
-  quant_group128_kernel<<<blocks_for(M * G, kThreads / 8), kThreads, 0, st>>>(
-      static_cast<const uint8_t *>(x), M, static_cast<int>(K), ldx * 2, G,
-      static_cast<uint8_t *>(q), s, s_layout, lds);
+  launch_pdl(quant_group128_kernel, persistent_grid(quant_group128_kernel, M * G, kThreads / 8, num_sms), kThreads, 0,
+             st, static_cast<const uint8_t *>(x), M, static_cast<int>(K), ldx * 2, G,
+             static_cast<uint8_t *>(q), s, s_layout, lds);
 }
 
 void launch_quant_mx(const void *x, int64_t M, int64_t K, int64_t ldx, void *q, uint8_t *s,
-                     cudaStream_t st) {
-  quant_mx_kernel<<<blocks_for(M * (K / 32), kThreads / 2), kThreads, 0, st>>>(
-      static_cast<const uint8_t *>(x), M, static_cast<int>(K), ldx * 2,
-      static_cast<uint8_t *>(q), s);
+                     int num_sms, cudaStream_t st) {
+  launch_pdl(quant_mx_kernel, persistent_grid(quant_mx_kernel, M * (K / 32), kThreads / 2, num_sms), kThreads,
+             0, st, static_cast<const uint8_t *>(x), M, static_cast<int>(K), ldx * 2,
+             static_cast<uint8_t *>(q), s);
 }
 
 void launch_quant_static(const void *x, int64_t M, int64_t K, int64_t ldx, const float *s,
-                         void *q, cudaStream_t st) {
-  quant_static_kernel<<<blocks_for(M * (K / 16), kThreads), kThreads, 0, st>>>(
-      static_cast<const uint8_t *>(x), M, static_cast<int>(K), ldx * 2, s,
-      static_cast<uint8_t *>(q));
+                         void *q, int num_sms, cudaStream_t st) {
+  launch_pdl(quant_static_kernel, persistent_grid(quant_static_kernel, M * (K / 16), kThreads, num_sms), kThreads, 0,
+             st, static_cast<const uint8_t *>(x), M, static_cast<int>(K), ldx * 2, s,
+             static_cast<uint8_t *>(q));
 }
 
 void launch_quant_weight_block(const void *w, int64_t N, int64_t K, int64_t ldw, void *q,
                                float *s, cudaStream_t st) {
   const int KB = static_cast<int>((K + 127) / 128);
   const int NB = static_cast<int>((N + 127) / 128);
-  quant_weight_block_kernel<<<dim3(KB, NB), kThreads, 0, st>>>(
-      static_cast<const uint8_t *>(w), static_cast<int>(N), static_cast<int>(K), ldw * 2,
-      static_cast<uint8_t *>(q), s, KB);
+  launch_pdl(quant_weight_block_kernel, dim3(KB, NB), kThreads, 0, st,
+             static_cast<const uint8_t *>(w), static_cast<int>(N), static_cast<int>(K), ldw * 2,
+             static_cast<uint8_t *>(q), s, KB);
 }
 
 void launch_absmax_scale(const void *x, int64_t rows, int64_t K, int64_t ldx, float *s,
@@ -297,10 +402,9 @@ void launch_absmax_scale(const void *x, int64_t rows, int64_t K, int64_t ldx, fl
   const unsigned cap = static_cast<unsigned>(num_sms) * 8u;
   if (grid > cap) grid = cap;
   if (grid == 0) grid = 1;
-  absmax_kernel<<<grid, kThreads, 0, st>>>(static_cast<const uint8_t *>(x), rows,
-                                           static_cast<int>(K), ldx * 2,
-                                           reinterpret_cast<uint32_t *>(s));
-  absmax_finalize_kernel<<<1, 1, 0, st>>>(s);
+  launch_pdl(absmax_kernel, grid, kThreads, 0, st, static_cast<const uint8_t *>(x), rows,
+             static_cast<int>(K), ldx * 2, reinterpret_cast<uint32_t *>(s));
+  launch_pdl(absmax_finalize_kernel, 1, 1, 0, st, s);
 }
 
 }  // namespace fp8bq
