@@ -44,22 +44,6 @@ __device__ __forceinline__ float amax16(const float (&f)[16]) {
   return m;
 }
 
-// x / s rounded to binary32, bit-identical to __fdiv_rn(x, s), at the cost of one
-// multiply in almost every case.  r = RN(1/s), so t = RN(x * r) is within 2.5 ulp
-// of RN(x / s).  E4M3 rounding only changes at the midpoints between adjacent
-// E4M3 values, which in the E4M3 normal range (|t| >= 2^-6) are exactly the
-// binary32 values whose low 20 mantissa bits are 0x80000; binade edges are not
-// rounding boundaries.  So t and RN(x / s) encode to the same E4M3 code unless t
-// lies within 4 ulp of such a midpoint or in the E4M3 subnormal range, and only
-// then is the division performed.
-__device__ __forceinline__ float div_by_scale(float x, float s, float r) {
-  float t = __fmul_rn(x, r);
-  const uint32_t b = __float_as_uint(t) & 0x7FFFFFFFu;
-  const bool near_tie = ((b & 0xFFFFFu) - 0x7FFFCu) <= 8u;
-  const bool sub_e4m3 = b < 0x3C800000u && b != 0u;  // 0 < |t| < 2^-6
-  if (near_tie || sub_e4m3) t = __fdiv_rn(x, s);
-  return t;
-}
 
 // 16 binary32 values -> 16 E4M3 codes (RNE, saturating), packed little-endian.
 __device__ __forceinline__ uint4 to_e4m3x16(const float (&t)[16]) {
@@ -75,6 +59,82 @@ __device__ __forceinline__ uint4 to_e4m3x16(const float (&t)[16]) {
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// Group scales from a table.  The group amax is a BF16 value m * 2^k with an
+// 8-bit significand m in [1, 2) (128 possibilities), and 448 = 7 * 2^6, so
+// RN(amax / 448) = RN(m / 448) * 2^k and RN(1 / s) = RN(1 / RN(m / 448)) * 2^-k
+// exactly whenever every value involved is a binary32 normal number, which
+// holds for amax >= 1e-10.  Each CTA fills the table for the 128 significands
+// with IEEE divisions once; a group then costs one shared-memory load and two
+// exponent additions instead of two correctly rounded divisions.  Entry m holds
+// {s, RN(1/s)} for amax = 1 + m/128.
+struct ScaleTable {
+  float2 e[128];
+  float2 floor_entry;  // amax below the 1e-10 floor
+};
+
+__device__ __forceinline__ void fill_scale_table(ScaleTable &t) {
+  for (int m = threadIdx.x; m <= 128; m += blockDim.x) {
+    const float a = m < 128 ? 1.0f + static_cast<float>(m) * 0.0078125f : kFloor;
+    const float sv = __fdiv_rn(a, 448.0f);
+    const float2 v = make_float2(sv, __frcp_rn(sv));
+    if (m < 128) t.e[m] = v;
+    else t.floor_entry = v;
+  }
+}
+
+// {s, RN(1/s)} for a group with maximum magnitude amax (a BF16 value).
+__device__ __forceinline__ float2 scale_of(const ScaleTable &t, float amax) {
+  if (!(amax >= kFloor)) return t.floor_entry;
+  const uint32_t b = __float_as_uint(amax);
+  const float2 v = t.e[(b >> 16) & 0x7Fu];
+  const int k = static_cast<int>((b >> 23) & 0xFFu) - 127;  // amax = (1 + m/128) * 2^k
+  return make_float2(__uint_as_float(__float_as_uint(v.x) + (static_cast<uint32_t>(k) << 23)),
+                     __uint_as_float(__float_as_uint(v.y) - (static_cast<uint32_t>(k) << 23)));
+}
+
+// E4M3 codes of RN(x / s) for 16 BF16 values x (two 16-byte words), without a
+// division: with r = RN(1/s), q0 = RN(x r) and q1 = RN(q0 + RN(x - s q0) r)
+// (FMAs, two values per instruction), and with CORRECTIONS = 2 once more from
+// q1.  By Markstein's theorem the corrected quotient is RN(x / s) once the
+// previous one is within an ulp; checked with exact rational arithmetic for
+// one correction over every pair of BF16 significand and group-scale
+// significand (s = RN(m/448)), and for both forms on random scales.  Where
+// the remainder underflows the quotient lies far below the smallest E4M3
+// value and encodes to zero either way.  The FMA form turns x = -0 into +0,
+// so the codes take the sign bits of x (which every nonzero quotient shares).
+template <int CORRECTIONS>
+__device__ __forceinline__ uint4 quant16(const uint4 (&v)[2], const float (&f)[16], float s,
+                                        float r) {
+  const float2 r2 = make_float2(r, r), ns2 = make_float2(-s, -s);
+  const uint32_t w[8] = {v[0].x, v[0].y, v[0].z, v[0].w, v[1].x, v[1].y, v[1].z, v[1].w};
+  uint32_t out[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t half[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const float2 x = make_float2(f[4 * i + 2 * h], f[4 * i + 2 * h + 1]);
+      float2 q = __fmul2_rn(x, r2);
+#pragma unroll
+      for (int c = 0; c < CORRECTIONS; ++c) q = __ffma2_rn(__ffma2_rn(ns2, q, x), r2, q);
+      half[h] = __nv_cvt_float2_to_fp8x2(q, __NV_SATFINITE, __NV_E4M3);
+    }
+    const uint32_t codes = (half[0] & 0xFFFFu) | (half[1] << 16);
+    out[i] = codes | (__byte_perm(w[2 * i], w[2 * i + 1], 0x7531) & 0x80808080u);
+  }
+  return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
+// Each BF16 pair of the four words clamped to [lo, hi] (BF16 pairs).
+__device__ __forceinline__ void clamp_bf16x2(uint4 &v, uint32_t lo, uint32_t hi) {
+  uint32_t *w = reinterpret_cast<uint32_t *>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    asm("{\n\t.reg .b32 t;\n\tmax.bf16x2 t, %1, %2;\n\tmin.bf16x2 %0, t, %3;\n\t}"
+        : "=r"(w[i])
+        : "r"(w[i]), "r"(lo), "r"(hi));
+}
+
 // ---------------------------------------------------------------- group-128 activation quant
 // 8 threads per 128-channel group, 16 channels (32 bytes) per thread; a
 // partial last group masks whole 16-channel chunks (K % 16 == 0).  The grid is
@@ -84,7 +144,10 @@ __device__ __forceinline__ uint4 to_e4m3x16(const float (&t)[16]) {
 __global__ void __launch_bounds__(kThreads) quant_group128_kernel(
     const uint8_t *__restrict__ x, int64_t M, int K, int64_t ldx_bytes, int G,
     uint8_t *__restrict__ q, float *__restrict__ s, int s_layout, int64_t lds) {
+  __shared__ ScaleTable table;
   griddep_launch_dependents();
+  fill_scale_table(table);
+  __syncthreads();
   griddep_wait();
   const int lane = threadIdx.x & 31, sub = lane & 7;
   const int64_t total = M * G;
@@ -123,12 +186,9 @@ __global__ void __launch_bounds__(kThreads) quant_group128_kernel(
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
-    const float sg = __fdiv_rn(fmaxf(amax, kFloor), 448.0f);
-    const float rg = __frcp_rn(sg);
-    float t[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) t[i] = div_by_scale(f[i], sg, rg);
-    const uint4 out = to_e4m3x16(t);
+    const float2 sc = scale_of(table, amax);
+    const float sg = sc.x;
+    const uint4 out = quant16<1>(cur, f, sg, sc.y);
     const int k = g * 128 + sub * 16;
     if (row < M) {
       if (k < K) *reinterpret_cast<uint4 *>(q + row * K + k) = out;
@@ -154,7 +214,10 @@ __global__ void __launch_bounds__(kThreads) quant_mx_kernel(const uint8_t *__res
                                                             int64_t ldx_bytes,
                                                             uint8_t *__restrict__ q,
                                                             uint8_t *__restrict__ s) {
+  __shared__ ScaleTable table;
   griddep_launch_dependents();
+  fill_scale_table(table);
+  __syncthreads();
   griddep_wait();
   const int G = K / 32;
   const int lane = threadIdx.x & 31, sub = lane & 1;
@@ -190,8 +253,7 @@ __global__ void __launch_bounds__(kThreads) quant_mx_kernel(const uint8_t *__res
     unpack16(cur, f);
     float amax = amax16(f);
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-    const float r = __fdiv_rn(fmaxf(amax, kFloor), 448.0f);
-    const uint32_t rb = __float_as_uint(r);
+    const uint32_t rb = __float_as_uint(scale_of(table, amax).x);  // RN(max(amax,1e-10)/448)
     const uint32_t u = (rb >> 23) + ((rb & 0x7FFFFFu) != 0u ? 1u : 0u);  // e + 127
     const float inv = __uint_as_float((254u - u) << 23);                 // 2^-e, exact
     float t[16];
@@ -228,6 +290,17 @@ __global__ void __launch_bounds__(kThreads) quant_static_kernel(const uint8_t *_
   const int dc = static_cast<int>(step - drow * C);
   const float sv = __ldg(s_ptr);
   const float rv = __frcp_rn(sv);
+  // A scale this small would make the clamp limit below underflow; such
+  // launches divide (the branch is uniform over the grid).
+  const bool divide = !(sv >= 0x1p-100f);
+  // x / s may overflow binary32 here (x is not bounded by the scale), and the
+  // FMA form would turn the infinity into NaN.  Every |x| >= 448 s encodes to
+  // the saturated 448 anyway, so inputs are clamped to +-L with L = 464 s
+  // rounded up to a BF16 value: values within L are unchanged, values beyond
+  // give quotients in [464, 469], which saturate to the same code.
+  uint32_t lim = __float_as_uint(__fmul_ru(sv, 464.0f));
+  lim = (lim & 0xFFFFu) ? (lim + 0x10000u) & 0xFFFF0000u : lim;
+  const uint32_t lim2 = (lim >> 16) | (lim & 0xFFFF0000u), nlim2 = lim2 | 0x80008000u;
   auto load = [&](int64_t r, int cc, uint4 (&v)[2]) {
     if (r < M) {
       const uint8_t *p = x + r * ldx_bytes + static_cast<int64_t>(cc) * 32;
@@ -246,12 +319,23 @@ __global__ void __launch_bounds__(kThreads) quant_static_kernel(const uint8_t *_
     }
     uint4 nxt[2];
     load(row_n, c_n, nxt);
+    uint4 clamped[2] = {cur[0], cur[1]};
+    if (!divide) {
+      clamp_bf16x2(clamped[0], nlim2, lim2);
+      clamp_bf16x2(clamped[1], nlim2, lim2);
+    }
     float f[16];
-    unpack16(cur, f);
-    float t[16];
+    unpack16(clamped, f);
+    uint4 out;
+    if (divide) {
+      float t[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) t[i] = div_by_scale(f[i], sv, rv);
-    *reinterpret_cast<uint4 *>(q + row * K + static_cast<int64_t>(c) * 16) = to_e4m3x16(t);
+      for (int i = 0; i < 16; ++i) t[i] = __fdiv_rn(f[i], sv);
+      out = to_e4m3x16(t);
+    } else {
+      out = quant16<2>(cur, f, sv, rv);
+    }
+    *reinterpret_cast<uint4 *>(q + row * K + static_cast<int64_t>(c) * 16) = out;
     cur[0] = nxt[0];
     cur[1] = nxt[1];
     row = row_n;
