@@ -917,15 +917,17 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
               if (j < args.M)
                 __stcg(part + (static_cast<int64_t>(w.split) * args.M + j) * args.N + n, acc[j]);
           }
-          __threadfence();
+          // the barrier orders every epilogue thread's partial stores before the
+          // counter update, whose release (GPU scope) publishes them; the last
+          // CTA's acquire on the same update makes all splits' partials visible
+          // to its epilogue threads after the next barrier
           named_bar_sync(2, C::kEpiThreads);
           if (et == 0) {
-            const uint32_t prev = atomicAdd(args.counters + w.tile, 1u);
+            const uint32_t prev = atom_add_acq_rel_gpu(args.counters + w.tile, 1u);
             bars->is_last = (prev == static_cast<uint32_t>(shape.splits - 1)) ? 1u : 0u;
           }
           named_bar_sync(2, C::kEpiThreads);
           if (bars->is_last) {
-            __threadfence();
             if (n_ok) {
               // ascending split order; all of one split's loads are in flight at once
               float sum[C::kCPT];
