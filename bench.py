@@ -57,8 +57,8 @@ FP8_PER_BF16 = 2.0   # nominal dense FP8 / BF16 tensor rate
 # digest is recorded; anything else reports null.
 NCU_TRAFFIC = {
     # profiles/block_gemm_prefill_4096x24576x6144.md (N = 24576 launch)
-    "source_sha256": "3945102f9c819f420ea9225efd32bb2a26e0fc6ff5c8cedddbbb260d70bf04e9",
-    "bytes_per_launch": 182380800 + 173614080,
+    "source_sha256": "4ae53f595a1dc7f5cbc29b5803fd598cd952b385c327e60650bf60927e4476e9",
+    "bytes_per_launch": 191881984 + 176778496,
 }
 
 
@@ -357,6 +357,33 @@ def _time_back_to_back(torch, stream, fns, reps):
     return s.elapsed_time(e) / reps
 
 
+def _time_graph(torch, fns, per_graph, reps=20):
+    """Mean ms per launch of `per_graph` launches (cycling through `fns`) captured
+    back to back in one CUDA graph and replayed `reps` times: launches follow
+    each other with no host in between, as in a captured decode step."""
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for f in fns:
+            f()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(per_graph):
+            fns[i % len(fns)]()
+    g.replay()
+    torch.cuda.synchronize()
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(reps):
+        g.replay()
+    e.record()
+    e.synchronize()
+    return s.elapsed_time(e) / (reps * per_graph)
+
+
 def _copies(t, n):
     return [t] + [t.clone() for _ in range(n - 1)]
 
@@ -364,7 +391,10 @@ def _copies(t, n):
 def run_extra(fb, torch, dev, stream, hbm_peak, fp8_peak):
     """Decode and quantiser GB/s, MXFP8 and static TFLOPS (informational).  Each
     figure is the mean over back-to-back launches rotating through enough input
-    copies to exceed 1.5x the L2 size."""
+    copies to exceed 1.5x the L2 size.  Launches shorter than the host's own
+    cost per call (about 11 us through the Python binding) are timed inside a
+    CUDA graph (`*_us`, used for the fractions); the eager figures
+    (`*_eager_us`) are reported beside them."""
     out = {}
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
 
@@ -393,16 +423,20 @@ def run_extra(fb, torch, dev, stream, hbm_peak, fp8_peak):
         ws = fb.new_workspace(fb.OP_LINEAR, M, N, K, device=dev)
         g = [lambda i=i: fb.fp8bq_gemm(q, sx, qws[i], sws[i], y, ws) for i in range(ns)]
         l = [lambda i=i: fb.fp8bq_linear(x, qws[i], sws[i], y, ws) for i in range(ns)]
-        t = _time_back_to_back(torch, stream, g, 60)
-        tl = _time_back_to_back(torch, stream, l, 60)
+        te = _time_back_to_back(torch, stream, g, 60)
+        tle = _time_back_to_back(torch, stream, l, 60)
+        t = _time_graph(torch, g, 2 * ns)
+        tl = _time_graph(torch, l, 2 * ns)
         gemm_bytes = N * K + sw.numel() * 4 + M * (K + K // 128 * 4) + 2 * M * N
         lin_bytes = N * K + sw.numel() * 4 + 2 * M * K + 2 * M * N
         dec[str(M)] = {"gemm_us": round(t * 1e3, 2),
                        "gemm_gbs": round(gemm_bytes / (t * 1e-3) / 1e9, 1),
                        "gemm_frac_hbm": round(gemm_bytes / (t * 1e-3) / 1e9 / hbm_peak, 4),
+                       "gemm_eager_us": round(te * 1e3, 2),
                        "linear_us": round(tl * 1e3, 2),
                        "linear_gbs": round(lin_bytes / (tl * 1e-3) / 1e9, 1),
-                       "linear_frac_hbm": round(lin_bytes / (tl * 1e-3) / 1e9 / hbm_peak, 4)}
+                       "linear_frac_hbm": round(lin_bytes / (tl * 1e-3) / 1e9 / hbm_peak, 4),
+                       "linear_eager_us": round(tle * 1e3, 2)}
     out["decode_N6144_K6144"] = dec
     del qw, sw, qws, sws
 
@@ -414,8 +448,8 @@ def run_extra(fb, torch, dev, stream, hbm_peak, fp8_peak):
     xs = _copies(to_dev(si.activations(M, K)), ns)
     qs = [torch.empty(M, K, dtype=torch.uint8, device=dev) for _ in range(ns)]
     ss = [torch.empty(M, K // 128, dtype=torch.float32, device=dev) for _ in range(ns)]
-    t = _time_back_to_back(torch, stream, [lambda i=i: fb.fp8bq_quant_act(xs[i], qs[i], ss[i])
-                                           for i in range(ns)], 60)
+    t = _time_graph(torch, [lambda i=i: fb.fp8bq_quant_act(xs[i], qs[i], ss[i])
+                            for i in range(ns)], 2 * ns)
     quant["group128_4096x6144"] = {"us": round(t * 1e3, 2), "gbs": round(b / (t * 1e-3) / 1e9, 1),
                                    "frac_hbm": round(b / (t * 1e-3) / 1e9 / hbm_peak, 4)}
     del xs, qs, ss
@@ -426,8 +460,8 @@ def run_extra(fb, torch, dev, stream, hbm_peak, fp8_peak):
     xms = _copies(xm, ns)
     qms = [torch.empty(M, K, dtype=torch.uint8, device=dev) for _ in range(ns)]
     ums = [torch.empty(M, K // 32, dtype=torch.uint8, device=dev) for _ in range(ns)]
-    t = _time_back_to_back(torch, stream, [lambda i=i: fb.fp8bq_mx_quant_act(xms[i], qms[i], ums[i])
-                                           for i in range(ns)], 60)
+    t = _time_graph(torch, [lambda i=i: fb.fp8bq_mx_quant_act(xms[i], qms[i], ums[i])
+                            for i in range(ns)], 2 * ns)
     quant["mx_2048x7168"] = {"us": round(t * 1e3, 2), "gbs": round(b / (t * 1e-3) / 1e9, 1),
                              "frac_hbm": round(b / (t * 1e-3) / 1e9 / hbm_peak, 4)}
     out["quant"] = quant
@@ -471,10 +505,9 @@ def run_extra(fb, torch, dev, stream, hbm_peak, fp8_peak):
         fb.fp8bq_static_quant_act(xs, s_x, qs)
         ys = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
         wss = fb.new_workspace(fb.OP_STATIC_GEMM, M, N, K, device=dev)
-        t = _time_back_to_back(
-            torch, stream,
-            [lambda i=i: fb.fp8bq_static_gemm(qs, s_x, qwss[i], sp, parts, ys, wss)
-             for i in range(ns)], 30)
+        t = _time_graph(
+            torch, [lambda i=i: fb.fp8bq_static_gemm(qs, s_x, qwss[i], sp, parts, ys, wss)
+                    for i in range(ns)], 2 * ns)
         tf = 2.0 * M * N * K / (t * 1e-3) / 1e12
         b = N * K + M * K + 2 * M * N
         st[str(M)] = {"us": round(t * 1e3, 2), "tflops": round(tf, 2),
