@@ -13,6 +13,7 @@ constexpr int kBlockK = 128;  // K width of one scale block / one pipeline stage
 constexpr int kBlockN = 128;  // rows of W sharing one weight scale
 constexpr int kMxGroup = 32;  // K elements per UE8M0 scale
 constexpr int kMaxParts = 64; // static path: maximum number of output partitions
+constexpr int kMxBN = 224;    // weight rows per MXFP8 tile (must match gemm_mx.cu)
 
 // Status values stored in the workspace status word (same numbers as fp8bq_status).
 constexpr uint32_t kStatusTimeout = 8;
@@ -95,8 +96,21 @@ struct DeviceInfo {
 
 // Workspace layout (byte offsets), shared by the host entry points.
 struct WorkspaceLayout {
-  size_t status, counters, partials, q, s, total;
+  size_t status, counters, partials, q, s, sfa, sfb, total;
 };
+
+// MXFP8 scale-factor chunks, the form the MX GEMM loads with each operand stage:
+// per row tile and 128-wide K block, 32 rows of 16 bytes per 32 x 4 block of
+// codes (word c of row i = the four codes of tile row i + 32c).  Activations:
+// 128-row tiles, one 512-byte block; weights: kMxBN-row tiles, kMxSfBBlocks.
+constexpr int kMxSfBBlocks = (kMxBN / 32 + 3) / 4;
+inline int64_t mx_sfa_bytes(int64_t M, int64_t K) { return (M + 127) / 128 * ((K + 127) / 128) * 512; }
+inline int64_t mx_sfb_bytes(int64_t N, int64_t K) {
+  return (N + kMxBN - 1) / kMxBN * ((K + 127) / 128) * 512 * kMxSfBBlocks;
+}
+// Rearranges s_x [M, K/32] and s_w [N, K/32] (row-major UE8M0) into chunks.
+void launch_mx_sf_tiles(const uint8_t *ux, int64_t M, const uint8_t *uw, int64_t N, int64_t K,
+                        uint8_t *sfa, uint8_t *sfb, int num_sms, cudaStream_t st);
 WorkspaceLayout workspace_layout(int op, int64_t M, int64_t N, int64_t K);
 
 // Work decomposition of one GEMM launch.
@@ -139,6 +153,8 @@ cudaError_t run_tensor_swap(int bn, const GemmArgs &a, const void *q, const void
                             const LaunchShape &sh, int grid, cudaStream_t st, int *status);
 cudaError_t run_mx_normal(const GemmArgs &a, const void *q, const void *w,
                           const LaunchShape &sh, int grid, cudaStream_t st, int *status);
+cudaError_t run_mx_pair(const GemmArgs &a, const void *q, const void *w, const LaunchShape &sh,
+                        int grid, cudaStream_t st, int *status);
 
 // Chooses the kernel variant for the shape and launches it.  Returns 0 or an
 // fp8bq status; a CUDA error is returned through `cuda_err`.

@@ -164,9 +164,14 @@ int gemm_mx_impl(const void *q, const uint8_t *s_x, const void *w, const uint8_t
                  const void *bias, void *y, int64_t M, int64_t N, int64_t K, void *ws, int op,
                  cudaStream_t st, const DeviceInfo &dev) {
   GemmArgs a = base_args(kModeMx, M, N, K, bias, y, ws, op);
-  a.ux = s_x;
-  a.uw = s_w;
-  cudaError_t e;
+  const WorkspaceLayout L = workspace_layout(op, M, N, K);
+  uint8_t *sfa = static_cast<uint8_t *>(ws) + L.sfa;
+  uint8_t *sfb = static_cast<uint8_t *>(ws) + L.sfb;
+  launch_mx_sf_tiles(s_x, M, s_w, N, K, sfa, sfb, dev.num_sms, st);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e);
+  a.ux = sfa;  // the GEMM reads the chunks
+  a.uw = sfb;
   int r = launch_gemm(a, q, w, dev, st, &e);
   return finish_launch(r, e);
 }

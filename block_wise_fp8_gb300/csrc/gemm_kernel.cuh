@@ -65,12 +65,17 @@ template <int MODE, bool SWAP, int BN, int STAGES, int EPI_WARPS, int ACCB, bool
 struct Cfg {
   static constexpr int kMmaM = PAIR ? 256 : 128;     // rows of the MMA (both CTAs)
   static constexpr int kBrows = PAIR ? BN / 2 : BN;  // weight rows loaded by this CTA
-  static constexpr int kSfWarps = (MODE == kModeMx) ? 4 : 0;
-  static constexpr int kSfSlots = 4;
-  static constexpr int kSfPrefetch = 4;          // stages of UE8M0 codes loaded ahead
-  static constexpr int kSfColsA = 4;             // 128 rows / 32
+  // MX: the UE8M0 codes arrive pre-arranged (one chunk per row tile and K
+  // block, written by the scale-factor tiling kernel) with each operand stage;
+  // the MMA thread copies them into a TMEM slot (tcgen05.cp) ahead of its MMAs
+  static constexpr int kSfSlots = 4;             // TMEM slots, used round-robin
   static constexpr int kSfColsB = (MODE == kModeMx) ? BN / 32 : 4;
   static constexpr int kSfSlotCols = 16;         // A at +0, B at +8
+  static constexpr int kSfColsBPad = (kSfColsB + 3) / 4 * 4;
+  // per stage: [A: 32 rows x 16 B][B: kSfColsBPad/4 blocks of 32 rows x 16 B];
+  // word c of row i holds the four codes of tile row i + 32c
+  static constexpr int kSfBBytes = 128 * kSfColsBPad;
+  static constexpr int kSfStageBytes = (MODE == kModeMx) ? 512 + kSfBBytes : 0;
   // block tiles: two MMA-issuing warps take alternate K blocks (disjoint TMEM
   // partial buffers), so one issues while the other waits on its barriers
   static constexpr int kIssuers = (MODE == kModeBlock) ? 2 : 1;
@@ -78,7 +83,7 @@ struct Cfg {
   // registers: warpgroup 0 (producer, the two issuers and one idle warp) hands
   // registers to the epilogue warpgroups with setmaxnreg
   static constexpr bool kRegSplit = (MODE == kModeBlock) && PAIR;
-  static constexpr int kEpiBase = kRegSplit ? 4 : 1 + kIssuers + kSfWarps;  // first epilogue warp
+  static constexpr int kEpiBase = kRegSplit ? 4 : 1 + kIssuers;  // first epilogue warp
   static constexpr int kThreads = 32 * (kEpiBase + EPI_WARPS);
   // register budget: warps are dealt round-robin to the SM's four schedulers,
   // each with a quarter of the register file, so the bound counts whole
@@ -115,6 +120,7 @@ struct Cfg {
   static constexpr bool kScRing = (MODE == kModeBlock) && PAIR;
   static constexpr int kScQuad = 4;
   static constexpr int kScSlots = kScRing ? 4 : 0;
+  static constexpr int kScDiv = kScSlots > 0 ? kScSlots : 1;  // ring index divisor
   static constexpr int kScXBytes = kBM * kScQuad * 4;           // 2 KB
   static constexpr int kScWBytes = 2 * kScQuad * 4;             // 32 B
   static constexpr int kScSlotBytes = kScXBytes + 128;          // s_w at +kScXBytes
@@ -125,16 +131,18 @@ struct Cfg {
       pow2_at_least(kAccCols + (MODE == kModeMx ? kSfSlots * kSfSlotCols : 0));
   static constexpr int kBarBytes = 512;
   // dynamic shared memory: [align slack][A stages][B stages][barriers][sx stage]
-  static constexpr size_t kFixedSmem =
-      1024 + size_t(STAGES) * kStageBytes + kYStageBytes + kScBytes + kBarBytes;
+  static constexpr size_t kFixedSmem = 1024 + size_t(STAGES) * (kStageBytes + kSfStageBytes) +
+                                       kYStageBytes + kScBytes + kBarBytes;
 
   static_assert(EPI_WARPS % 4 == 0, "epilogue warps must cover the 4 TMEM lane quarters");
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M = 128");
   static_assert(kCPT % kCW == 0 && kCPT % 2 == 0, "chunking");
   static_assert(kTmemCols <= 512, "TMEM columns");
   static_assert(STAGES <= 8 && ACCB <= 8, "barrier arrays");
-  static_assert(MODE != kModeMx || (!SWAP && BN % 32 == 0 && kSfColsB <= 8), "MX tiles");
-  static_assert(!PAIR || (!SWAP && MODE != kModeMx && kBrows % 8 == 0), "pair tiles");
+  static_assert(MODE != kModeMx || (!SWAP && BN % 32 == 0 && kSfColsB <= 8 && BN == kMxBN &&
+                                    kSfBBytes == 512 * kMxSfBBlocks),
+                "MX tiles match the scale-factor chunks");
+  static_assert(!PAIR || (!SWAP && kBrows % 8 == 0), "pair tiles");
   static_assert(MODE != kModeBlock || SWAP || (128 % kCPT == 0 && BN % kCPT == 0),
                 "block tiles: each thread's columns lie in one 128-row weight block");
   static_assert(!SWAP || (kCPT <= 64 && EPI_WARPS == 4),
@@ -151,7 +159,6 @@ struct Cfg {
 struct SmemBarriers {
   uint64_t full[8], empty[8];
   uint64_t tfull[8], tempty[8];
-  uint64_t sf_full[4], sf_empty[4];
   uint64_t sc_full[4], sc_empty[4];
   uint64_t drain;
   uint32_t tmem_base;
@@ -254,19 +261,6 @@ __device__ __forceinline__ Unit decode_unit(int u, int num_a_tiles, int splits, 
   return r;
 }
 
-// Four UE8M0 codes (K groups 4kb..4kb+3) of one row, packed little-endian.
-__device__ __forceinline__ uint32_t sf_word(const uint8_t *base, int row, int rows, int G,
-                                            int kb) {
-  if (row >= rows) return 0u;
-  const uint8_t *p = base + static_cast<int64_t>(row) * G + 4 * kb;
-  if ((G & 3) == 0) return __ldg(reinterpret_cast<const uint32_t *>(p));
-  uint32_t v = 0;
-#pragma unroll
-  for (int g = 0; g < 4; ++g)
-    if (4 * kb + g < G) v |= static_cast<uint32_t>(__ldg(p + g)) << (8 * g);
-  return v;
-}
-
 // Store `n` (multiple of 8 unless ragged) BF16 values of row m starting at column c0.
 template <int CNT>
 __device__ __forceinline__ void store_row(uint16_t *y, const float *v, int m, int c0,
@@ -312,8 +306,9 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
   uint8_t *sB = smem + STAGES * kAbytes;
   uint8_t *y_stage = smem + STAGES * C::kStageBytes;  // 1024-byte aligned
   uint8_t *sc_ring = y_stage + C::kYStageBytes;       // 1024-byte aligned
-  SmemBarriers *bars = reinterpret_cast<SmemBarriers *>(sc_ring + C::kScBytes);
-  float *sx_stage = reinterpret_cast<float *>(sc_ring + C::kScBytes + C::kBarBytes);
+  uint8_t *sSF = sc_ring + C::kScBytes;               // MX: UE8M0 chunks per stage
+  SmemBarriers *bars = reinterpret_cast<SmemBarriers *>(sSF + STAGES * C::kSfStageBytes);
+  float *sx_stage = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(bars) + C::kBarBytes);
   volatile uint32_t *abort_flag = &bars->abort;
 
   const int warp = threadIdx.x >> 5;
@@ -334,10 +329,6 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
       mbar_init(&bars->tfull[b], 1);
       mbar_init(&bars->tempty[b], PAIR ? 2 * EPI_WARPS : EPI_WARPS);
     }
-    for (int s = 0; s < C::kSfSlots; ++s) {
-      mbar_init(&bars->sf_full[s], C::kSfWarps > 0 ? C::kSfWarps : 1);
-      mbar_init(&bars->sf_empty[s], 1);
-    }
     for (int s = 0; s < C::kScSlots; ++s) {
       mbar_init(&bars->sc_full[s], 1);
       mbar_init(&bars->sc_empty[s], EPI_WARPS);
@@ -350,7 +341,7 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
-    if (C::kScRing && args.sc_tma) {
+    if ((C::kScRing && args.sc_tma) || MODE == kModeMx) {
       tma_prefetch_desc(&tmSx);
       tma_prefetch_desc(&tmSw);
     }
@@ -410,7 +401,7 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
             if (sc_tma && (kb - w.kb0) % C::kScQuad == 0) {
               // promotion factors of K blocks kb .. kb+3: this CTA's s_x rows and
               // the tile's weight-block scales, on this CTA's own barrier
-              const uint32_t q = sq % C::kScSlots, qph = (sq / C::kScSlots) & 1u;
+              const uint32_t q = sq % C::kScDiv, qph = (sq / C::kScDiv) & 1u;
               if (!mbar_wait(&bars->sc_empty[q], qph ^ 1u, abort_flag, limit)) {
                 ok = false;
                 break;
@@ -430,16 +421,30 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
               break;
             }
             if (args.fault_skip_first_load && blockIdx.x == 0 && it == 0) continue;
+            // MX: this CTA's A-row chunk and the weight tile's chunk of UE8M0
+            // codes (256-byte rows: 2 for A, kSfBBytes / 256 for B)
+            const int sfa_row = ((w.a_row0 / kBM) * KB + kb) * 2;
+            const int sfb_row = ((w.b_row0 / BN) * KB + kb) * (C::kSfBBytes / 256);
+            uint8_t *sf = sSF + s * C::kSfStageBytes;
             if (PAIR) {
               // both CTAs' bytes complete on the even CTA's barrier
-              if (leader) mbar_arrive_expect_tx(&bars->full[s], 2 * C::kStageBytes);
+              if (leader)
+                mbar_arrive_expect_tx(&bars->full[s], 2 * (C::kStageBytes + C::kSfStageBytes));
               const uint32_t bar0 = mapa_shared(smem_u32(&bars->full[s]), 0);
               tma_load_2d_pair(sA + s * kAbytes, &tmA, bar0, kb * 128, w.a_row0);
               tma_load_2d_pair(sB + s * C::kBbytes, &tmB, bar0, kb * 128, w.b_load_row0);
+              if (MODE == kModeMx) {
+                tma_load_2d_pair(sf, &tmSx, bar0, 0, sfa_row);
+                tma_load_2d_pair(sf + 512, &tmSw, bar0, 0, sfb_row);
+              }
             } else {
-              mbar_arrive_expect_tx(&bars->full[s], C::kStageBytes);
+              mbar_arrive_expect_tx(&bars->full[s], C::kStageBytes + C::kSfStageBytes);
               tma_load_2d(sA + s * kAbytes, &tmA, &bars->full[s], kb * 128, w.a_row0);
               tma_load_2d(sB + s * C::kBbytes, &tmB, &bars->full[s], kb * 128, w.b_load_row0);
+              if (MODE == kModeMx) {
+                tma_load_2d(sf, &tmSx, &bars->full[s], 0, sfa_row);
+                tma_load_2d(sf + 512, &tmSw, &bars->full[s], 0, sfb_row);
+              }
             }
             issued |= 1u << s;
             phase_bits = (phase_bits & ~(1u << s)) | (ph << s);
@@ -499,15 +504,22 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
               ok = false;
               break;
             }
-            uint32_t sfslot = 0;
+            const uint32_t sfslot = it % C::kSfSlots;
+            tc_fence_after();
             if (MODE == kModeMx) {
-              sfslot = it % C::kSfSlots;
-              if (!mbar_wait(&bars->sf_full[sfslot], (it / C::kSfSlots) & 1u, abort_flag, limit)) {
-                ok = false;
-                break;
+              // UE8M0 codes of this K block: shared memory -> TMEM slot, ahead of the
+              // MMAs that read them (same issuing thread, executed in order)
+              const uint32_t sfcol = tmem_base + C::kSfBase + sfslot * C::kSfSlotCols;
+              const uint32_t src = smem_u32(sSF + s * C::kSfStageBytes);
+  #pragma unroll
+              for (int j = 0; j <= C::kSfColsBPad / 4; ++j) {
+                // j = 0: A codes to columns +0..3; j >= 1: B codes to +8.., +12..
+                const uint32_t col = sfcol + (j == 0 ? 0 : 4 + 4 * j);
+                const uint64_t d = sdesc_kmajor_noswizzle(src + 512 * j, 128, 128);
+                if (PAIR) tmem_cp_32x128b_warpx4_pair(col, d);
+                else tmem_cp_32x128b_warpx4(col, d);
               }
             }
-            tc_fence_after();
             const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(sA + s * kAbytes));
             const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(sB + s * C::kBbytes));
   #pragma unroll
@@ -516,8 +528,12 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
               const uint32_t acc = (MODE == kModeBlock) ? (k > 0) : (kb > w.kb0 || k > 0);
               if (MODE == kModeMx) {
                 const uint32_t sfcol = tmem_base + C::kSfBase + sfslot * C::kSfSlotCols;
-                umma_mxf8f6f4(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc_mxf8_e4m3(kBM, BN, k, k),
-                              sfcol, sfcol + 8, acc);
+                if (PAIR)
+                  umma_mxf8f6f4_pair(d_tmem, adesc + 2 * k, bdesc + 2 * k,
+                                     idesc_mxf8_e4m3(C::kMmaM, BN, k, k), sfcol, sfcol + 8, acc);
+                else
+                  umma_mxf8f6f4(d_tmem, adesc + 2 * k, bdesc + 2 * k,
+                                idesc_mxf8_e4m3(kBM, BN, k, k), sfcol, sfcol + 8, acc);
               } else if (PAIR) {
                 umma_f8f6f4_pair(d_tmem, adesc + 2 * k, bdesc + 2 * k,
                                  idesc_f8f6f4_e4m3(C::kMmaM, BN), acc);
@@ -527,7 +543,6 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
             }
             if (PAIR) umma_commit_pair(&bars->empty[s], 0x3);
             else umma_commit(&bars->empty[s]);
-            if (MODE == kModeMx) umma_commit(&bars->sf_empty[sfslot]);
             if (MODE == kModeBlock) {
               if (PAIR) umma_commit_pair(&bars->tfull[it % ACCB], 0x3);
               else umma_commit(&bars->tfull[it % ACCB]);
@@ -545,65 +560,6 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
         else umma_commit(&bars->drain);
         uint32_t dummy = 0;
         mbar_wait(&bars->drain, 0, &dummy, limit);
-      }
-      __syncwarp();
-    } else if (warp < C::kEpiBase) {
-      // ------------------------------------------------------------ MX scale-factor writers
-      // (warps 1 + kIssuers .. kEpiBase - 1)
-      // Warp with lane quarter q writes TMEM lanes 32q..32q+31.  Layout (replicated in
-      // every quarter): lane i, column c of a slot holds the four UE8M0 codes of stage
-      // kb (K groups 4kb..4kb+3, one byte per MMA, selected by the sf id) of tile row
-      // i + 32c.  The codes are loaded kSfPrefetch stages before they are written.
-      if (MODE == kModeMx) {
-        constexpr int PD = C::kSfPrefetch;
-        constexpr int NA = C::kSfColsA, NB = C::kSfColsB;
-        const int q = warp & 3;
-        const int G = args.K / 32;
-        uint32_t sfit = 0;
-        bool ok = true;
-        uint32_t ring[PD][NA + NB];
-        for (int u = cl_id; ok && u < shape.units; u += cl_num) {
-          const Unit w = decode_unit<SWAP, PAIR>(u, shape.num_a_tiles, shape.splits, shape.kps, KB, BN, rank);
-          auto load = [&](int kb, uint32_t *dst) {
-  #pragma unroll
-            for (int c = 0; c < NA; ++c) dst[c] = sf_word(args.ux, w.a_row0 + lane + 32 * c, args.M, G, kb);
-  #pragma unroll
-            for (int c = 0; c < NB; ++c)
-              dst[NA + c] = sf_word(args.uw, w.b_row0 + lane + 32 * c, args.N, G, kb);
-          };
-  #pragma unroll
-          for (int i = 0; i < PD; ++i)
-            if (w.kb0 + i < w.kb1) load(w.kb0 + i, ring[i]);
-          for (int kb = w.kb0; ok && kb < w.kb1; kb += PD) {
-  #pragma unroll
-            for (int i = 0; i < PD; ++i) {
-              const int k = kb + i;
-              if (k < w.kb1 && ok) {
-                const uint32_t slot = sfit % C::kSfSlots;
-                if (!warp_wait(&bars->sf_empty[slot], ((sfit / C::kSfSlots) & 1u) ^ 1u,
-                               abort_flag, limit)) {
-                  ok = false;
-                } else {
-                  tc_fence_after();
-                  const uint32_t col = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
-                                       C::kSfBase + slot * C::kSfSlotCols;
-                  tmem_st4(col, ring[i][0], ring[i][1], ring[i][2], ring[i][3]);
-  #pragma unroll
-                  for (int c = 0; c < NB; c += 4)
-                    tmem_st4(col + 8 + c, ring[i][NA + c], ring[i][NA + c + 1],
-                             ring[i][NA + c + 2], ring[i][NA + c + 3]);
-                  tmem_st_wait();
-                  tc_fence_before();
-                  __syncwarp();
-                  if (lane == 0) mbar_arrive(&bars->sf_full[slot]);
-                  ++sfit;
-                  if (k + PD < w.kb1) load(k + PD, ring[i]);
-                }
-              }
-            }
-          }
-        }
-        if (!ok && lane == 0) record_timeout(args);
       }
       __syncwarp();
     }
@@ -677,7 +633,7 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
             const int row = 32 * quarter + lane;
             const int nbi = nbase / kBlockN - w.b_row0 / kBlockN;  // 0 or 1
             for (int kq = w.kb0; kq < w.kb1 && ok; kq += C::kScQuad) {
-              const uint32_t q = sq % C::kScSlots, qph = (sq / C::kScSlots) & 1u;
+              const uint32_t q = sq % C::kScDiv, qph = (sq / C::kScDiv) & 1u;
               if (!warp_wait(&bars->sc_full[q], qph, abort_flag, limit)) {
                 ok = false;
                 break;
@@ -1004,6 +960,18 @@ cudaError_t run(const GemmArgs &a, const void *q_act, const void *w, const Launc
     const bool sw_ok = al16(a.sw) && KB % 4 == 0 &&
                        cached_f32_map(&tsw, a.sw, NB, KB, KB, C::kScQuad, 2);
     args.sc_tma = (sx_ok && sw_ok) ? 1 : 0;
+  }
+  if (MODE == kModeMx) {
+    // scale-factor chunks as rows of 256 bytes (typed FP32 only to describe the
+    // copy): 2 rows per activation chunk, kSfBBytes / 256 per weight chunk
+    const int64_t KB = (a.K + 127) / 128;
+    const int64_t rows_a = (a.M + kBM - 1) / kBM * KB * 2;
+    const int64_t rows_b = (a.N + BN - 1) / BN * KB * (C::kSfBBytes / 256);
+    if (!al16(a.ux) || !al16(a.uw) || !cached_f32_map(&tsx, a.ux, rows_a, 64, 64, 64, 2) ||
+        !cached_f32_map(&tsw, a.uw, rows_b, 64, 64, 64, C::kSfBBytes / 256)) {
+      *status = 4;  // FP8BQ_ERR_UNSUPPORTED: tensor map rejected
+      return cudaSuccess;
+    }
   }
   const void *a_ptr = SWAP ? w : q_act;
   const void *b_ptr = SWAP ? q_act : w;

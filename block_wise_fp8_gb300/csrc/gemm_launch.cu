@@ -165,7 +165,8 @@ bool cached_bf16_rows_map(CUtensorMap *m, const void *base, int64_t rows, int64_
   return true;
 }
 
-// [status word | split-K tile counters | split-K FP32 partials | fused: Q | fused: scales]
+// [status word | split-K tile counters | split-K FP32 partials | fused: Q | fused: scales |
+//  MX: activation and weight scale-factor chunks]
 WorkspaceLayout workspace_layout(int op, int64_t M, int64_t N, int64_t K) {
   auto up = [](size_t v) { return (v + 255) / 256 * 256; };
   WorkspaceLayout L{};
@@ -183,6 +184,10 @@ WorkspaceLayout workspace_layout(int op, int64_t M, int64_t N, int64_t K) {
   L.s = off;
   if (op == 1) off += up(static_cast<size_t>(M) * KB * 4);
   if (op == 3) off += up(static_cast<size_t>(M) * (K / 32));
+  L.sfa = off;
+  if (mx) off += up(static_cast<size_t>(mx_sfa_bytes(M, K)));
+  L.sfb = off;
+  if (mx) off += up(static_cast<size_t>(mx_sfb_bytes(N, K)));
   L.total = off;
   return L;
 }
@@ -221,14 +226,23 @@ int launch_gemm(const GemmArgs &a, const void *q_act, const void *w, const Devic
     return status;
   }
   if (a.mode == kModeMx) {
-    // MXFP8: single-CTA 128 x 128 tiles, persistent CTAs, M fastest
-    sh.num_a_tiles = (a.M + 127) / 128;
+    // MXFP8: 224-wide weight tiles, persistent CTAs, M fastest.  224 is the
+    // widest UMMA N for which two accumulators and the scale-factor slots fit
+    // in the 512 TMEM columns (2 x 224 + 64), so the epilogue of one tile
+    // overlaps the MMAs of the next.  Above 128 tokens, CTA pairs take 256 x 224
+    // tiles (each CTA loads half the weight tile); otherwise single CTAs take
+    // 128 x 224 tiles.
+    const bool pair = a.M > 128;
+    const int rows = pair ? 256 : 128;
+    sh.num_a_tiles = (a.M + rows - 1) / rows;
     sh.splits = 1;
     sh.kps = sh.KB;
-    sh.units = sh.num_a_tiles * ((a.N + 127) / 128);
+    sh.units = sh.num_a_tiles * ((a.N + kMxBN - 1) / kMxBN);
     sh.sx_stage = 0;
-    const int grid = sh.units < dev.num_sms ? sh.units : dev.num_sms;
-    *cuda_err = run_mx_normal(a, q_act, w, sh, grid, st, &status);
+    const int slots = pair ? dev.num_sms / 2 : dev.num_sms;
+    const int grid = sh.units < slots ? sh.units : slots;
+    *cuda_err = pair ? run_mx_pair(a, q_act, w, sh, grid, st, &status)
+                     : run_mx_normal(a, q_act, w, sh, grid, st, &status);
     return status;
   }
   // prefill: CTA pairs over 256 x bn tiles, persistent clusters, M fastest.  The

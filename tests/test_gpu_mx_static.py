@@ -49,7 +49,7 @@ def test_mx_gemm_scale_layout():
 
 
 @pytest.mark.parametrize("M,N,K", [(16, 384, 256), (5, 200, 96), (130, 136, 224),
-                                   (512, 1024, 7168)])
+                                   (257, 232, 128), (300, 520, 416), (512, 1024, 7168)])
 def test_mx_gemm_shapes(M, N, K):
     qa, ua = oracle.quant_mx(si.activations(M, K))
     qw, uw = oracle.quant_mx(si.weights(N, K))
