@@ -72,6 +72,9 @@ _SIGS = {
     "orc_gemm_static_sampled": (None, [_P, ctypes.c_float, _P, _P, _P, ctypes.c_int, _P,
                                        _I64, _I64, _I64, _P, _P, _I64, _P,
                                        ctypes.c_int]),
+    "orc_bf16_from_f64": (ctypes.c_uint16, [ctypes.c_double]),
+    "orc_sumsq_f32": (ctypes.c_float, [_P, _I64]),
+    "orc_add_rmsnorm": (None, [_P, _I64, _P, _I64, _P, ctypes.c_float, _I64, _I64, _P, _P]),
     "orc_e4m3_dot_int": (ctypes.c_int64, [_P, _P, _I64]),
     "orc_e4m3_dot_f64": (ctypes.c_double, [_P, _P, _I64]),
 }
@@ -198,6 +201,52 @@ def quant_weight_static(w, part_sizes):
     s = np.empty(parts.size, np.float32)
     lib().orc_quant_weight_static(_p(w), N, K, K, _p(parts), parts.size, _p(q), _p(s))
     return q, s
+
+
+# --------------------------------------------------------------------------
+# residual add + RMSNorm
+# --------------------------------------------------------------------------
+
+def bf16_from_f64(v: float) -> int:
+    """binary64 -> BF16 bits (RNE, overflow to infinity)."""
+    return int(lib().orc_bf16_from_f64(float(v)))
+
+
+def sumsq_f32(r) -> np.float32:
+    """Sum of squares of a BF16 row (uint16 bits), exact, rounded once to binary32."""
+    r = _c(r, np.uint16).ravel()
+    return np.float32(lib().orc_sumsq_f32(_p(r), r.size))
+
+
+def add_rmsnorm(x, gamma, eps: float, residual=None):
+    """r = BF16(x + residual), y = BF16(RMSNorm(r) * gamma) -> (r, y), uint16 [M,d]."""
+    x = _c(x, np.uint16)
+    M, d = x.shape
+    g = _c(gamma, np.uint16).ravel()
+    if g.size != d:
+        raise ValueError("gamma must have d elements")
+    res = None if residual is None else _c(residual, np.uint16)
+    if res is not None and res.shape != x.shape:
+        raise ValueError("residual must match x")
+    r = np.empty((M, d), np.uint16)
+    y = np.empty((M, d), np.uint16)
+    lib().orc_add_rmsnorm(_p(x), d, _p(res), d, _p(g), float(np.float32(eps)), M, d,
+                          _p(r), _p(y))
+    return r, y
+
+
+def add_rmsnorm_quant_group(x, gamma, eps: float, residual=None):
+    """Residual add + RMSNorm, then group-128 quantisation of the BF16 output:
+    -> (r, q, s)."""
+    r, y = add_rmsnorm(x, gamma, eps, residual)
+    q, s = quant_group(y)
+    return r, q, s
+
+
+def add_rmsnorm_quant_static(x, gamma, eps: float, s_x: float, residual=None):
+    """Residual add + RMSNorm, then static per-tensor quantisation: -> (r, q)."""
+    r, y = add_rmsnorm(x, gamma, eps, residual)
+    return r, quant_static(y, s_x)
 
 
 # --------------------------------------------------------------------------

@@ -443,3 +443,118 @@ void orc_gemm_static_sampled(const uint8_t *qa, float s_x, const uint8_t *qw,
   g.rows = rows; g.cols = cols; g.n = n;
   run_gemm(g, nthreads);
 }
+
+/* ======================================================================= */
+/* Residual add + RMSNorm                                                   */
+/* ======================================================================= */
+
+/* binary64 -> BF16 bits, round to nearest even; beyond the largest finite
+ * BF16 (plus half an ulp) -> infinity; NaN -> quiet NaN with the sign kept. */
+uint16_t orc_bf16_from_f64(double v) {
+  uint16_t sign = signbit(v) ? 0x8000u : 0u;
+  if (v != v) return sign | 0x7FC0u;
+  double a = fabs(v);
+  if (a == 0.0) return sign;
+  if (isinf(a)) return sign | 0x7F80u;
+  int ex;
+  frexp(a, &ex);             /* a in [2^(ex-1), 2^ex) */
+  int e = ex - 1;
+  if (e < -126) e = -126;    /* subnormal BF16: quantum 2^-133 */
+  double quantum = ldexp(1.0, e - 7);
+  uint32_t n = rne_uint(a / quantum); /* exact scaling by a power of two */
+  double r = (double)n * quantum;     /* n may be 256: the next binade */
+  if (r >= 0x1p128) return sign | 0x7F80u;
+  union {
+    float f;
+    uint32_t u;
+  } c;
+  c.f = (float)r; /* exact: r has at most 8 significant bits */
+  return sign | (uint16_t)(c.u >> 16);
+}
+
+/* Sum of r_i^2 over a row of BF16 values, computed exactly and rounded once to
+ * binary32 (nearest, ties to even).  The page fixes only that the sum is taken
+ * in FP32 ([GLM-17] §第1站 "求和与开方在 FP32 上完成"); its order is open, and
+ * the correctly rounded value is the one every order approximates.  Each
+ * nonzero finite r = m * 2^(E-134) with an integer m <= 255 and a biased
+ * exponent E in 1..254, so r^2 = m^2 * 2^(2E-268): the row sum is the integer
+ * A = sum m^2 * 2^(2E-2) times 2^-266, accumulated in 32-bit limbs.  NaN in the
+ * row gives NaN, otherwise an infinity gives +infinity. */
+#define SUMSQ_LIMBS 20
+float orc_sumsq_f32(const uint16_t *r, int64_t d) {
+  uint32_t A[SUMSQ_LIMBS];
+  memset(A, 0, sizeof A);
+  int any_nan = 0, any_inf = 0;
+  for (int64_t i = 0; i < d; ++i) {
+    uint32_t b = r[i] & 0x7FFFu;
+    uint32_t E = b >> 7, frac = b & 0x7Fu;
+    if (E == 0xFF) {
+      if (frac) any_nan = 1;
+      else any_inf = 1;
+      continue;
+    }
+    uint32_t m = E ? (frac | 0x80u) : frac;
+    if (E == 0) E = 1;
+    if (m == 0) continue;
+    uint32_t k = 2 * E - 2; /* bit position of m^2 in A */
+    uint64_t add = (uint64_t)(m * m) << (k % 32);
+    for (uint32_t l = k / 32; add != 0 && l < SUMSQ_LIMBS; ++l) {
+      uint64_t t = (uint64_t)A[l] + (add & 0xFFFFFFFFu);
+      A[l] = (uint32_t)t;
+      add = (add >> 32) + (t >> 32);
+    }
+  }
+  if (any_nan) return NAN;
+  if (any_inf) return INFINITY;
+  int p = -1; /* highest set bit of A */
+  for (int l = SUMSQ_LIMBS - 1; l >= 0 && p < 0; --l)
+    if (A[l]) {
+      int h = 31;
+      while (!((A[l] >> h) & 1u)) --h;
+      p = 32 * l + h;
+    }
+  if (p < 0) return 0.0f;
+  /* keep 24 significant bits, or fewer where the result is subnormal
+   * (binary32 quantum 2^-149 = bit 117 of A) */
+  int lsb = p - 23 > 117 ? p - 23 : 117;
+  uint64_t mant = 0;
+  for (int bit = p; bit >= lsb; --bit)
+    mant = (mant << 1) | ((A[bit / 32] >> (bit % 32)) & 1u);
+  int half = lsb > 0 ? (int)((A[(lsb - 1) / 32] >> ((lsb - 1) % 32)) & 1u) : 0;
+  int sticky = 0;
+  for (int bit = lsb - 2; bit >= 0 && !sticky; --bit)
+    if ((A[bit / 32] >> (bit % 32)) & 1u) sticky = 1;
+  if (half && (sticky || (mant & 1u))) ++mant;
+  double v = ldexp((double)mant, lsb - 266); /* exact; >= 2^128 overflows below */
+  return (float)v;
+}
+
+/* Residual add and RMSNorm of one decoder-layer input ([GLM-17] §第1站):
+ *   r = x + residual, the BF16 residual stream (the add rounded to BF16 once);
+ *   y = r / sqrt(mean(r^2) + eps) * g, sums and root in FP32, output BF16.
+ * Readings: the mean is RN32(S / d) with S = orc_sumsq_f32(r); then
+ * RN32(mean + eps), the correctly rounded FP32 square root, the FP32 quotient
+ * r / rms and the FP32 product with g, rounded to BF16 once at the end.
+ * residual may be NULL (plain RMSNorm: r = x).  r_out and y are [M][d]. */
+void orc_add_rmsnorm(const uint16_t *x, int64_t ldx, const uint16_t *res,
+                     int64_t ldr, const uint16_t *g, float eps, int64_t M,
+                     int64_t d, uint16_t *r_out, uint16_t *y) {
+  for (int64_t i = 0; i < M; ++i) {
+    uint16_t *ri = r_out + i * d;
+    for (int64_t k = 0; k < d; ++k) {
+      double a = (double)orc_bf16_to_f32(x[i * ldx + k]);
+      if (res) a += (double)orc_bf16_to_f32(res[i * ldr + k]);
+      ri[k] = orc_bf16_from_f64(a); /* the sum of two BF16 values is exact in
+                                       binary64 unless one is negligible */
+    }
+    volatile float S = orc_sumsq_f32(ri, d);
+    volatile float ms = S / (float)d;
+    volatile float t = ms + eps;
+    volatile float rms = sqrtf(t);
+    for (int64_t k = 0; k < d; ++k) {
+      volatile float a = orc_bf16_to_f32(ri[k]) / rms;
+      volatile float b = a * orc_bf16_to_f32(g[k]);
+      y[i * d + k] = orc_bf16_from_f64((double)b);
+    }
+  }
+}

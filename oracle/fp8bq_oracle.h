@@ -51,6 +51,16 @@ void orc_quant_static(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
 float orc_absmax_scale(const uint16_t *x, int64_t r0, int64_t r1, int64_t K,
                        int64_t ldx);
 
+/* ---- residual add + RMSNorm (the step before the activation quantiser) -- */
+/* binary64 -> BF16 (RNE, overflow to infinity).                             */
+uint16_t orc_bf16_from_f64(double v);
+/* sum of squares of a BF16 row, exact, rounded once to binary32 (RNE).      */
+float   orc_sumsq_f32(const uint16_t *r, int64_t d);
+/* r = BF16(x + residual) (residual may be NULL), y = BF16 RMSNorm(r) * g.   */
+void    orc_add_rmsnorm(const uint16_t *x, int64_t ldx, const uint16_t *res,
+                        int64_t ldr, const uint16_t *g, float eps, int64_t M,
+                        int64_t d, uint16_t *r_out, uint16_t *y);
+
 /* ---- quantisers (weight side, used to build test weights) -------------- */
 /* 128x128 (bn x bk) block quantisation: s[ceil(N/bn)][ceil(K/bk)].          */
 void orc_quant_weight_block(const uint16_t *w, int64_t N, int64_t K,
