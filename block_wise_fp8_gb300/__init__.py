@@ -29,6 +29,7 @@ __all__ = [
     "fp8bq_quant_act", "fp8bq_gemm", "fp8bq_linear", "fp8bq_gemm_noalloc",
     "NOALLOC_SCRATCH_BYTES", "fp8bq_mx_quant_act",
     "fp8bq_mx_gemm", "fp8bq_mx_linear", "fp8bq_static_quant_act", "fp8bq_static_gemm",
+    "fp8bq_add_rmsnorm_quant_act", "fp8bq_add_rmsnorm_static_quant_act",
     "fp8bq_static_linear", "fp8bq_quant_weight_block", "fp8bq_absmax_scale",
     "new_workspace",
 ]
@@ -64,6 +65,7 @@ def _load():
             "(there is no CPU fallback)")
     lib = ctypes.CDLL(_build.LIB)
     P, I64, I32, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+    F32 = ctypes.c_float
     sigs = {
         "fp8bq_version": (I32, []),
         "fp8bq_status_string": (ctypes.c_char_p, [I32]),
@@ -79,6 +81,10 @@ def _load():
         "fp8bq_mx_gemm": (I32, [P, P, P, P, P, P, I64, I64, I64, P, SZ, P]),
         "fp8bq_mx_linear": (I32, [P, I64, P, P, P, P, I64, I64, I64, P, SZ, P]),
         "fp8bq_static_quant_act": (I32, [P, I64, I64, I64, P, P, P]),
+        "fp8bq_add_rmsnorm_quant_act": (I32, [P, I64, P, I64, P, P, F32, I64, I64, P, P, P,
+                                              I32, P]),
+        "fp8bq_add_rmsnorm_static_quant_act": (I32, [P, I64, P, I64, P, P, F32, P, I64, I64,
+                                                     P, P, P]),
         "fp8bq_static_gemm": (I32, [P, P, P, P, P, I32, P, P, I64, I64, I64, P, SZ, P]),
         "fp8bq_static_linear": (I32, [P, I64, P, P, P, P, I32, P, P, I64, I64, I64, P, SZ,
                                       P]),
@@ -234,6 +240,27 @@ def fp8bq_static_quant_act(x, s_x, q, stream=None):
     M, K = x.shape
     _check(_lib.fp8bq_static_quant_act(_ptr(x), M, K, _ld(x), _ptr(s_x), _ptr(q),
                                        _stream(stream)), "fp8bq_static_quant_act")
+
+
+def fp8bq_add_rmsnorm_quant_act(x, gamma, eps: float, residual=None, residual_out=None,
+                                y=None, q=None, s=None, s_layout: int = SCALE_ROW_MAJOR,
+                                stream=None):
+    """Residual add + RMSNorm (+ group-128 quantisation when q is given)."""
+    M, K = x.shape
+    _check(_lib.fp8bq_add_rmsnorm_quant_act(
+        _ptr(x), _ld(x), _ptr(residual), 0 if residual is None else _ld(residual),
+        _ptr(residual_out), _ptr(gamma), float(eps), M, K, _ptr(y), _ptr(q), _ptr(s),
+        s_layout, _stream(stream)), "fp8bq_add_rmsnorm_quant_act")
+
+
+def fp8bq_add_rmsnorm_static_quant_act(x, gamma, eps: float, s_x, q, residual=None,
+                                       residual_out=None, y=None, stream=None):
+    """Residual add + RMSNorm, then static per-tensor quantisation with s_x[0]."""
+    M, K = x.shape
+    _check(_lib.fp8bq_add_rmsnorm_static_quant_act(
+        _ptr(x), _ld(x), _ptr(residual), 0 if residual is None else _ld(residual),
+        _ptr(residual_out), _ptr(gamma), float(eps), _ptr(s_x), M, K, _ptr(y), _ptr(q),
+        _stream(stream)), "fp8bq_add_rmsnorm_static_quant_act")
 
 
 def fp8bq_static_gemm(q, s_x, w, s_w_part, part_sizes, y, ws, bias=None, stream=None):

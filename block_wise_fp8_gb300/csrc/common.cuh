@@ -47,6 +47,12 @@ void launch_quant_mx(const void *x, int64_t M, int64_t K, int64_t ldx, void *q, 
                      int num_sms, cudaStream_t st);
 void launch_quant_static(const void *x, int64_t M, int64_t K, int64_t ldx, const float *s,
                          void *q, int num_sms, cudaStream_t st);
+// Residual add + RMSNorm, then (q != null) group-128 quantisation (s_x == null)
+// or static quantisation with the scale s_x[0].  res, r_out, y may be null.
+cudaError_t launch_add_rmsnorm(const void *x, int64_t ldx, const void *res, int64_t ldr,
+                               void *r_out, const void *g, float eps, int64_t M, int64_t K,
+                               void *y, void *q, float *s, int s_layout, const float *s_x,
+                               int num_sms, cudaStream_t st);
 void launch_quant_weight_block(const void *w, int64_t N, int64_t K, int64_t ldw, void *q,
                                float *s, cudaStream_t st);
 void launch_absmax_scale(const void *x, int64_t rows, int64_t K, int64_t ldx, float *s,

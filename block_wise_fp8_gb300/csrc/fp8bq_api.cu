@@ -413,6 +413,66 @@ int fp8bq_mx_linear(const void *x, int64_t ldx, const void *w, const uint8_t *s_
 
 // ------------------------------------------------------------------ static path
 
+// ------------------------------------------------------------------ residual add + RMSNorm
+
+namespace {
+
+constexpr int64_t kNormMaxK = 16384;
+
+int norm_common(const void *x, int64_t ldx, const void *residual, int64_t ld_res,
+                const void *residual_out, const void *gamma, float eps, int64_t M, int64_t K,
+                const void *y, const void *q) {
+  RETURN_IF(check_act(x, M, K, ldx, 16));
+  if (!gamma) return FP8BQ_ERR_NULL;
+  if (K > kNormMaxK || !(eps >= 0.0f) || !(eps <= 3.4e38f)) return FP8BQ_ERR_UNSUPPORTED;
+  if (residual && (ld_res < K || !aligned(residual, 16) || ld_res % 8 != 0))
+    return ld_res < K ? FP8BQ_ERR_SHAPE : FP8BQ_ERR_ALIGN;
+  if (residual_out && residual_out == residual && ld_res != K) return FP8BQ_ERR_SHAPE;
+  if (!aligned(gamma, 16) || !aligned(residual_out, 16) || !aligned(y, 16) || !aligned(q, 16))
+    return FP8BQ_ERR_ALIGN;
+  return FP8BQ_OK;
+}
+
+}  // namespace
+
+int fp8bq_add_rmsnorm_quant_act(const void *x, int64_t ldx, const void *residual,
+                                int64_t ld_res, void *residual_out, const void *gamma, float eps,
+                                int64_t M, int64_t K, void *y, void *q, float *s, int s_layout,
+                                void *stream) {
+  if (M == 0) return empty_batch(K, 1);
+  RETURN_IF(norm_common(x, ldx, residual, ld_res, residual_out, gamma, eps, M, K, y, q));
+  if (q) {
+    if (!s) return FP8BQ_ERR_NULL;
+    if (s_layout != FP8BQ_SCALE_ROW_MAJOR && s_layout != FP8BQ_SCALE_COL_MAJOR)
+      return FP8BQ_ERR_UNSUPPORTED;
+    if (!aligned(s, 4)) return FP8BQ_ERR_ALIGN;
+  }
+  DeviceInfo dev;
+  RETURN_IF(device_info(&dev));
+  cudaError_t e = launch_add_rmsnorm(x, ldx, residual, ld_res, residual_out, gamma, eps, M, K,
+                                     y, q, s, s_layout, nullptr, dev.num_sms,
+                                     static_cast<cudaStream_t>(stream));
+  if (e == cudaSuccess) e = cudaGetLastError();
+  return e == cudaSuccess ? FP8BQ_OK : cuda_fail(e);
+}
+
+int fp8bq_add_rmsnorm_static_quant_act(const void *x, int64_t ldx, const void *residual,
+                                       int64_t ld_res, void *residual_out, const void *gamma,
+                                       float eps, const float *s_x, int64_t M, int64_t K,
+                                       void *y, void *q, void *stream) {
+  if (M == 0) return empty_batch(K, 1);
+  if (!q || !s_x) return FP8BQ_ERR_NULL;
+  RETURN_IF(norm_common(x, ldx, residual, ld_res, residual_out, gamma, eps, M, K, y, q));
+  if (!aligned(s_x, 4)) return FP8BQ_ERR_ALIGN;
+  DeviceInfo dev;
+  RETURN_IF(device_info(&dev));
+  cudaError_t e = launch_add_rmsnorm(x, ldx, residual, ld_res, residual_out, gamma, eps, M, K,
+                                     y, q, nullptr, FP8BQ_SCALE_ROW_MAJOR, s_x, dev.num_sms,
+                                     static_cast<cudaStream_t>(stream));
+  if (e == cudaSuccess) e = cudaGetLastError();
+  return e == cudaSuccess ? FP8BQ_OK : cuda_fail(e);
+}
+
 int fp8bq_static_quant_act(const void *x, int64_t M, int64_t K, int64_t ldx, const float *s_x,
                            void *q, void *stream) {
   if (M == 0) return empty_batch(K, 1);

@@ -1,0 +1,593 @@
+// norm_quant.cu -- residual add + RMSNorm, fused with the activation
+// quantiser that follows it ("GLM-5.3 推理全链路(十七)", §第1站 RMSNorm 的两个出口):
+//
+//   r = BF16(x + residual)                       the updated residual stream
+//   y = BF16(r / sqrt(RN32(S / d) + eps) * g)    S = sum of r^2 over the row
+//   then the group-128 quantiser (q, s) or the static per-tensor one (q) on y
+//
+// S is the correctly rounded binary32 value of the exact sum (the page fixes
+// only that the sum is taken in FP32; its order is open), computed with
+// integers (see "exact sum of squares" below).  The quotient, root and
+// products are IEEE binary32 operations, so every output is bit-identical to
+// the definition; the quantisers are the exact ones of quant.cu applied to the
+// BF16 y, so the fused result equals norm-then-quantise.
+//
+// One CTA per row (persistent over rows), 256 threads (512 above 8192
+// channels); thread t holds the 8-channel chunks (c * THREADS + t) * 8, so a
+// 128-channel group is 16 consecutive threads of one chunk.
+#include <cuda_bf16.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "ptx.cuh"
+#include "quant_math.cuh"
+
+namespace fp8bq {
+namespace {
+
+struct NormArgs {
+  const uint8_t *x;
+  int64_t ldx_bytes;
+  const uint8_t *res;  // may be null: no residual add
+  int64_t ldr_bytes;
+  uint8_t *r_out;      // may be null; [M][K] BF16
+  const uint8_t *g;    // [K] BF16
+  float eps;
+  int64_t M;
+  int K;
+  uint8_t *y;          // may be null; [M][K] BF16
+  uint8_t *q;          // may be null (norm only); [M][K] E4M3
+  float *s;            // group scales
+  int s_layout;
+  int64_t lds;
+  const float *s_x;    // static scale (device)
+};
+
+__device__ __forceinline__ uint32_t bf16x2_add(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// ---------------------------------------------------------------- exact sum of squares
+//
+// A nonzero finite BF16 value is m * 2^(E-134) with an integer significand m
+// (< 256) and biased exponent E (1 for subnormals), so its square is
+// m^2 * 4^(E-134).  Each thread sums its own squares as a 64-bit integer in
+// units of 2^-40 * 4^(Et-134), Et its largest exponent (at most 32 terms below
+// 2^56 each): a value of exponent e adds (m^2 << 40) >> 2 (Et - e), exact for
+// e >= Et - 20; a thread holding a nonzero value further down (which loses
+// bits there) reports a bound on the loss, at most one unit per term.  The
+// block then takes the row's largest exponent Eb, moves every thread sum to
+// units of 2^-64 * 4^(Eb-134) as four 23-bit limbs, adds the limbs and the
+// loss bounds with warp-wide integer reductions (no carries: the limb sums
+// stay below 2^32) and rounds the 128-bit total A to binary32.  The exact sum
+// lies in [A, A + U]; when A and A + U round alike that is the answer,
+// otherwise (a midpoint within U, possible only for rows built to sit within
+// 2^-26 of one through a value far below the largest) thread 0 recomputes the
+// row's sum exactly, as the definition states.
+
+// (hi:lo) * 2^base rounded to binary32 (nearest even), with a correctly rounded
+// uint64 -> binary32 conversion: when the value needs more than 64 bits, its
+// top 64 bits with every lower bit folded into bit 0 (far below the rounding
+// position) round alike.  Returns false for a result below the normal range
+// (the scaling would round a second time).
+__device__ __forceinline__ bool to_binary32(uint64_t lo, uint64_t hi, int base, float &out) {
+  uint64_t top;
+  int sh = 0;
+  if (hi == 0ull) {
+    top = lo;
+  } else {
+    const int p = 127 - __clzll(static_cast<long long>(hi));  // highest set bit, >= 64
+    sh = p - 63;
+    top = (hi << (64 - sh)) | (lo >> sh);
+    if (lo & ((1ull << sh) - 1ull)) top |= 1ull;
+  }
+  if (top == 0ull) {
+    out = 0.0f;
+    return true;
+  }
+  const float f = __ull2float_rn(top);  // exact power-of-two scaling follows
+  const int e = static_cast<int>((__float_as_uint(f) >> 23) & 0xFFu) + base + sh;
+  if (e <= 0) return false;
+  out = e >= 255 ? __uint_as_float(0x7F800000u)
+                 : __uint_as_float((__float_as_uint(f) & 0x807FFFFFu) | (static_cast<uint32_t>(e) << 23));
+  return true;
+}
+
+// The row's sum of squares by one thread, exactly (32-bit limbs of m^2 * 4^(E-1)
+// scaled by 2^-266), rounded to binary32: the slow path of an undecided row.
+// Reads the row back from global memory (values already written by the block).
+__device__ __noinline__ float exact_row_sum(const uint8_t *r_row, const uint8_t *x_row, const uint8_t *res_row,
+                               int K) {
+  uint32_t A[20];
+#pragma unroll
+  for (int l = 0; l < 20; ++l) A[l] = 0u;
+  for (int k = 0; k < K; ++k) {
+    uint32_t h;
+    if (r_row) {
+      h = reinterpret_cast<const uint16_t *>(r_row)[k];
+    } else {
+      const uint32_t xv = reinterpret_cast<const uint16_t *>(x_row)[k];
+      const uint32_t rv = res_row ? reinterpret_cast<const uint16_t *>(res_row)[k] : 0u;
+      h = res_row ? bf16x2_add(xv, rv) & 0xFFFFu : xv;
+    }
+    const uint32_t e = (h >> 7) & 0xFFu;
+    const uint32_t m = (h & 0x7Fu) | (e ? 0x80u : 0u);
+    if (m == 0u) continue;
+    const uint32_t bitpos = 2u * (e ? e : 1u) - 2u;
+    uint64_t add = static_cast<uint64_t>(m * m) << (bitpos % 32u);
+    for (uint32_t l = bitpos / 32u; add != 0ull && l < 20u; ++l) {
+      const uint64_t t = static_cast<uint64_t>(A[l]) + (add & 0xFFFFFFFFull);
+      A[l] = static_cast<uint32_t>(t);
+      add = (add >> 32) + (t >> 32);
+    }
+  }
+  int p = -1;
+  for (int l = 19; l >= 0 && p < 0; --l)
+    if (A[l]) p = 32 * l + 31 - __clz(static_cast<int>(A[l]));
+  if (p < 0) return 0.0f;
+  const int lsb = p - 23 > 117 ? p - 23 : 117;  // 2^-149 is bit 117
+  uint32_t mant = 0u;
+  for (int b = p; b >= lsb; --b) mant = (mant << 1) | ((A[b / 32] >> (b % 32)) & 1u);
+  const uint32_t half = (A[(lsb - 1) / 32] >> ((lsb - 1) % 32)) & 1u;
+  uint32_t rest = 0u;
+  for (int b = lsb - 2; b >= 0 && !rest; --b) rest = (A[b / 32] >> (b % 32)) & 1u;
+  if (half && (rest || (mant & 1u))) ++mant;
+  int e2 = lsb - 266;
+  if (mant == (1u << 24)) {
+    mant >>= 1;
+    ++e2;
+  }
+  if (mant < (1u << 23)) return __uint_as_float(mant);
+  const int biased = e2 + 23 + 127;
+  if (biased >= 255) return __uint_as_float(0x7F800000u);
+  return __uint_as_float((static_cast<uint32_t>(biased) << 23) | (mant & 0x7FFFFFu));
+}
+
+// acc += square of BF16 h in units 2^-40 * 4^(Et-134): the general form (any
+// exponent gap, subnormals), truncated bits counted in `lost`.
+__device__ __forceinline__ void add_square_general(uint64_t &acc, uint32_t &lost, uint32_t h,
+                                                   int Et) {
+  const uint32_t e = (h >> 7) & 0xFFu;
+  const uint32_t m = (h & 0x7Fu) | (e ? 0x80u : 0u);
+  const uint32_t m2 = m * m;
+  if (m2 == 0u) return;
+  const int sl = 40 - 2 * (Et - static_cast<int>(e ? e : 1u));
+  if (sl >= 0) {
+    acc += static_cast<uint64_t>(m2) << sl;
+  } else {
+    const int sr = -sl;
+    if (sr >= 32) {
+      lost += 1u;
+    } else {
+      acc += m2 >> sr;
+      lost += (m2 & ((1u << sr) - 1u)) ? 1u : 0u;
+    }
+  }
+}
+
+// The thread's sum in the general form, over its n 16-byte chunks.
+__device__ __noinline__ void thread_sum_general(const uint4 *r, int n, int Et, uint64_t &acc,
+                                                uint32_t &lost) {
+  acc = 0ull;
+  lost = 0u;
+  for (int c = 0; c < n; ++c) {
+    const uint32_t w[4] = {r[c].x, r[c].y, r[c].z, r[c].w};
+    for (int i = 0; i < 8; ++i)
+      add_square_general(acc, lost, (i & 1) ? (w[i >> 1] >> 16) : (w[i >> 1] & 0xFFFFu), Et);
+  }
+}
+
+constexpr uint64_t kNormWaitNs = 2000000000ull;  // bound on a row copy's wait
+
+template <int THREADS, int CH, int QMODE>  // QMODE: 0 norm only, 1 group-128, 2 static
+__global__ void __launch_bounds__(THREADS, THREADS == 256 ? 3 : 1) add_rmsnorm_kernel(NormArgs a) {
+  constexpr int NW = THREADS / 32;
+  __shared__ ScaleTable table;
+  // per-warp partial results, double-buffered by row parity: a row's barriers
+  // separate its writes from its reads, the parity the next row's writes
+  __shared__ int red_e[2][NW];
+  __shared__ uint32_t red_l[2][NW][4], red_u[2][NW];
+  __shared__ float s_slow;
+  // rows arrive by TMA bulk copies into two stages of [x row][residual row]
+  extern __shared__ __align__(128) uint8_t stage_mem[];
+  __shared__ uint64_t full[2];
+  __shared__ uint32_t no_abort;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const uint32_t row_bytes = static_cast<uint32_t>(a.K) * 2u;
+  const uint32_t row_pitch = (row_bytes + 127u) & ~127u;
+  const uint32_t stage_bytes = row_pitch * (a.res ? 2u : 1u);
+  griddep_launch_dependents();
+  if (t == 0) {
+    mbar_init(&full[0], 1);
+    mbar_init(&full[1], 1);
+    no_abort = 0u;
+    fence_mbar_init();
+  }
+  if (QMODE == 1) fill_scale_table(table);
+  __syncthreads();
+  griddep_wait();
+  auto issue = [&](int64_t rw, int st) {  // thread 0: start loading row rw into stage st
+    if (rw >= a.M) return;
+    uint8_t *dst = stage_mem + st * stage_bytes;
+    mbar_arrive_expect_tx(&full[st], a.res ? 2u * row_bytes : row_bytes);
+    bulk_load_1d(dst, a.x + rw * a.ldx_bytes, row_bytes, &full[st]);
+    if (a.res) bulk_load_1d(dst + row_pitch, a.res + rw * a.ldr_bytes, row_bytes, &full[st]);
+  };
+  if (t == 0) {
+    issue(blockIdx.x, 0);
+    issue(static_cast<int64_t>(blockIdx.x) + gridDim.x, 1);
+  }
+  StaticScale sc{};
+  if (QMODE == 2) sc = static_scale(__ldg(a.s_x));
+  const float eps = a.eps;
+  const float d_f = static_cast<float>(a.K);  // exact: K < 2^24
+  // the norm gains are the same for every row: loaded once
+  uint4 gch[CH];
+#pragma unroll
+  for (int c = 0; c < CH; ++c) {
+    const int k = (c * THREADS + t) * 8;
+    gch[c] = k < a.K ? __ldg(reinterpret_cast<const uint4 *>(a.g + static_cast<int64_t>(k) * 2))
+                     : make_uint4(0, 0, 0, 0);
+  }
+
+  int par = 0;
+  uint32_t it = 0;
+  for (int64_t row = blockIdx.x; row < a.M; row += gridDim.x, par ^= 1, ++it) {
+    // ---- r = x + residual (BF16), kept in registers
+    const int st = static_cast<int>(it & 1u);
+    const bool timed = !mbar_wait(&full[st], (it >> 1) & 1u, &no_abort, kNormWaitNs);
+    const uint8_t *xs = stage_mem + st * stage_bytes;
+    uint4 r[CH];
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+      const int k = (c * THREADS + t) * 8;
+      r[c] = k < a.K ? *reinterpret_cast<const uint4 *>(xs + k * 2) : make_uint4(0, 0, 0, 0);
+    }
+    if (a.res) {
+#pragma unroll
+      for (int c = 0; c < CH; ++c) {
+        const int k = (c * THREADS + t) * 8;
+        if (k < a.K) {
+          const uint4 v = *reinterpret_cast<const uint4 *>(xs + row_pitch + k * 2);
+          r[c].x = bf16x2_add(r[c].x, v.x);
+          r[c].y = bf16x2_add(r[c].y, v.y);
+          r[c].z = bf16x2_add(r[c].z, v.z);
+          r[c].w = bf16x2_add(r[c].w, v.w);
+        }
+      }
+    }
+    if (a.r_out) {
+#pragma unroll
+      for (int c = 0; c < CH; ++c) {
+        const int k = (c * THREADS + t) * 8;
+        if (k < a.K) *reinterpret_cast<uint4 *>(a.r_out + (row * a.K + k) * 2) = r[c];
+      }
+    }
+    // ---- this thread's largest |r| (NaN-propagating BF16 max; the patterns of
+    // non-negative values order like the values, NaN and infinity on top)
+    __nv_bfloat162 mxv = __floats2bfloat162_rn(0.0f, 0.0f);
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+      const uint32_t w[4] = {r[c].x, r[c].y, r[c].z, r[c].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t ab = w[i] & 0x7FFF7FFFu;
+        mxv = __hmax2_nan(mxv, *reinterpret_cast<const __nv_bfloat162 *>(&ab));
+      }
+    }
+    const uint32_t mx2 = *reinterpret_cast<const uint32_t *>(&mxv) & 0x7FFF7FFFu;
+    const uint32_t mx = max(mx2 & 0xFFFFu, mx2 >> 16);
+    const uint32_t nonfinite = mx >= 0x7F80u ? (mx > 0x7F80u ? 2u : 1u) : 0u;
+    const int Et = max(static_cast<int>(mx >> 7), 1);
+    // ---- this thread's squares, units 2^-40 * 4^(Et-134)
+    uint64_t acc = 0ull;
+    uint32_t lost = 0u;
+    bool within20 = mx == 0u;  // every nonzero value within 20 binades of Et
+    if (!nonfinite && mx != 0u) {
+      if (Et >= 28) {
+        // fast form: value h (exponent field e) adds (m^2 << 40) >> 2 (Et - e),
+        // exact for e >= Et - 20; zeros and subnormals (e = 0) shift by
+        // 2 Et >= 56 and add nothing.  A nonzero value with e <= Et - 21
+        // (0 < |h| < (Et - 20) << 7 as patterns) loses bits: `far`.
+        const uint32_t far_lim = static_cast<uint32_t>(Et - 20) << 7;
+        bool far = false;
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+          const uint32_t w[4] = {r[c].x, r[c].y, r[c].z, r[c].w};
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const uint32_t h = ((i & 1) ? (w[i >> 1] >> 16) : w[i >> 1]) & 0x7FFFu;
+            const uint32_t e = h >> 7;
+            const uint32_t m = (h | 0x80u) & 0xFFu;
+            const int sr = min(2 * (Et - static_cast<int>(e)), 63);
+            acc += (static_cast<uint64_t>(m * m) << 40) >> sr;
+            far |= (h - 1u) < far_lim - 1u;  // h = 0 wraps above the limit
+          }
+        }
+        lost = far ? static_cast<uint32_t>(CH * 8) : 0u;  // < 1 unit per term
+        within20 = !far;
+      } else {  // a thread whose values all lie below 2^-99: the general form
+        thread_sum_general(r, CH, Et, acc, lost);
+      }
+    }
+    // ---- block sum.  1: the row's largest exponent Eb (non-finite rows 256 / 257)
+    const int Ethr = nonfinite ? 255 + static_cast<int>(nonfinite) : (mx ? Et : 0);
+    const unsigned Ew = __reduce_max_sync(0xffffffffu, static_cast<unsigned>(Ethr));
+    if (lane == 0) red_e[par][warp] = static_cast<int>(Ew);
+    // every thread has its row in registers past this barrier: the stage is
+    // refilled with the row two steps ahead (a copy that never lands makes every
+    // thread leave together; the outputs are then undefined)
+    if (__syncthreads_or(timed)) return;
+    if (t == 0) {
+      fence_proxy_async_smem();
+      issue(row + 2 * static_cast<int64_t>(gridDim.x), st);
+    }
+    const int Eb = static_cast<int>(
+        __reduce_max_sync(0xffffffffu, lane < NW ? static_cast<unsigned>(red_e[par][lane]) : 0u));
+    float S;
+    if (Eb >= 255) {
+      S = __uint_as_float(Eb == 257 ? 0x7FC00000u : 0x7F800000u);
+    } else if (Eb == 0) {
+      S = 0.0f;
+    } else {
+      // 2: this thread's sum in units 2^-64 * 4^(Eb-134) (at most 2^85) as four
+      // 23-bit limbs, and its truncation bound in units of 2^8 of those
+      const int gap2 = Ethr ? 2 * (Eb - Et) : 200;
+      uint32_t L[4], u8 = 0u;
+      {
+        const uint64_t a0 = gap2 <= 24 ? acc << (24 - gap2)
+                                       : (gap2 - 24 < 64 ? acc >> (gap2 - 24) : 0ull);
+        L[0] = static_cast<uint32_t>(a0) & 0x7FFFFFu;
+        const int s1 = gap2 - 1, s2 = gap2 + 22, s3 = gap2 + 45;
+        L[1] = static_cast<uint32_t>(s1 < 64 ? acc >> s1 : 0ull) & 0x7FFFFFu;
+        L[2] = static_cast<uint32_t>(s2 < 64 ? acc >> s2 : 0ull) & 0x7FFFFFu;
+        L[3] = static_cast<uint32_t>(s3 < 64 ? acc >> s3 : 0ull);
+        const bool cut = gap2 > 24 && (gap2 - 24 >= 64 ? acc != 0ull
+                                                       : (acc & ((1ull << (gap2 - 24)) - 1ull)) != 0ull);
+        if (lost || cut) {
+          const uint64_t ub = (gap2 <= 24 ? static_cast<uint64_t>(lost) << (24 - gap2) : lost) +
+                              (cut ? 1ull : 0ull);
+          u8 = static_cast<uint32_t>((ub + 255ull) >> 8);
+        }
+      }
+      // 3: warp sums (each below 2^28), then the block's (below 2^32)
+      uint32_t T[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) T[k] = __reduce_add_sync(0xffffffffu, L[k]);
+      const uint32_t Uw = __reduce_add_sync(0xffffffffu, u8);
+      if (lane == 0) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) red_l[par][warp][k] = T[k];
+        red_u[par][warp] = Uw;
+      }
+      __syncthreads();
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        T[k] = __reduce_add_sync(0xffffffffu, lane < NW ? red_l[par][lane][k] : 0u);
+      const uint32_t U8 = __reduce_add_sync(0xffffffffu, lane < NW ? red_u[par][lane] : 0u);
+      // 4: A = sum T_k 2^(23k) as 128 bits, rounded to binary32 by the hardware's
+      // correctly rounded uint64 conversion (bits below the top 64 folded into a
+      // sticky bit 0); the exact sum lies in [A, A + 256 U8]
+      uint64_t lo = static_cast<uint64_t>(T[0]) + (static_cast<uint64_t>(T[1]) << 23);
+      uint64_t hi = 0ull;
+      {
+        const uint64_t t2 = static_cast<uint64_t>(T[2]) << 46;
+        lo += t2;
+        hi += (static_cast<uint64_t>(T[2]) >> 18) + (lo < t2 ? 1ull : 0ull);
+        hi += static_cast<uint64_t>(T[3]) << 5;
+      }
+      const int base = 2 * (Eb - 134) - 64;
+      float Sa;
+      bool ok = to_binary32(lo, hi, base, Sa);
+      if (ok && U8 != 0u) {
+        const uint64_t add = static_cast<uint64_t>(U8) << 8;
+        const uint64_t lo2 = lo + add;
+        float Sb;
+        ok = to_binary32(lo2, hi + (lo2 < lo ? 1ull : 0ull), base, Sb) &&
+             __float_as_uint(Sb) == __float_as_uint(Sa);
+      }
+      if (ok) {
+        S = Sa;
+      } else {
+        // undecided (a midpoint within the bound) or a subnormal sum: the row's
+        // exact sum by thread 0 (block-uniform branch)
+        if (t == 0)
+          s_slow = exact_row_sum(a.r_out ? a.r_out + row * a.K * 2 : nullptr,
+                                 a.x + row * a.ldx_bytes, a.res ? a.res + row * a.ldr_bytes : nullptr,
+                                 a.K);
+        __syncthreads();
+        S = s_slow;
+      }
+    }
+    const float rms = __fsqrt_rn(__fadd_rn(__fdiv_rn(S, d_f), eps));
+    // r / rms as q0 = RN(r * RN(1/rms)) corrected once, q = RN(q0 - RN(rms q0 - r)
+    // * RN(1/rms)) with exact FMA remainders: equal to the IEEE quotient whenever
+    // rms, r and the quotient are binary32 normal numbers (checked exhaustively
+    // over BF16 significands against every binary32 significand), and to +-0
+    // with the right sign for r = +-0.  The thread divides when its smallest
+    // nonzero |r| could fall below 2^-100 or give a quotient below 2^-125 (its
+    // values lie above 2^(Et-147) when none is 20 binades below Et); |r / rms|
+    // never exceeds sqrt(K).
+    const int rms_e = static_cast<int>((__float_as_uint(rms) >> 23) & 0xFFu);
+    const bool fastdiv = rms_e >= 2 && rms_e <= 252 &&
+                         (mx == 0u || (within20 && Et >= 47 && Et >= rms_e - 104));
+    const float inv = __frcp_rn(rms);
+    const float2 inv2 = make_float2(inv, inv), rms2 = make_float2(rms, rms);
+
+    // ---- y = BF16(r / rms * g), then the quantiser
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+      const int k = (c * THREADS + t) * 8;
+      const bool valid = k < a.K;
+      const uint32_t rw[4] = {r[c].x, r[c].y, r[c].z, r[c].w};
+      const uint32_t gw[4] = {gch[c].x, gch[c].y, gch[c].z, gch[c].w};
+      uint32_t yw[4];
+      float fy[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 x2 = make_float2(bf16_lo(rw[i]), bf16_hi(rw[i]));
+        float2 q;
+        if (fastdiv) {
+          q = __fmul2_rn(x2, inv2);
+          const float2 rem = __ffma2_rn(rms2, q, make_float2(-x2.x, -x2.y));
+          q = __ffma2_rn(make_float2(-rem.x, -rem.y), inv2, q);
+        } else {
+          q = make_float2(__fdiv_rn(x2.x, rms), __fdiv_rn(x2.y, rms));
+        }
+        const float2 v = __fmul2_rn(q, make_float2(bf16_lo(gw[i]), bf16_hi(gw[i])));
+        const __nv_bfloat162 b = __floats2bfloat162_rn(v.x, v.y);
+        yw[i] = *reinterpret_cast<const uint32_t *>(&b);
+        fy[2 * i] = bf16_lo(yw[i]);
+        fy[2 * i + 1] = bf16_hi(yw[i]);
+      }
+      if (!valid) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) fy[i] = 0.0f;
+      }
+      if (a.y && valid)
+        *reinterpret_cast<uint4 *>(a.y + (row * a.K + k) * 2) = make_uint4(yw[0], yw[1], yw[2], yw[3]);
+      if (QMODE == 1) {
+        // group of 128 channels = 16 consecutive threads of this chunk
+        // max |y| over the chunk (BF16 max; patterns order like the values)
+        uint32_t ya[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) ya[i] = yw[i] & 0x7FFF7FFFu;
+        const __nv_bfloat162 m01 = __hmax2(*reinterpret_cast<const __nv_bfloat162 *>(&ya[0]),
+                                           *reinterpret_cast<const __nv_bfloat162 *>(&ya[1]));
+        const __nv_bfloat162 m23 = __hmax2(*reinterpret_cast<const __nv_bfloat162 *>(&ya[2]),
+                                           *reinterpret_cast<const __nv_bfloat162 *>(&ya[3]));
+        const __nv_bfloat162 m03 = __hmax2(m01, m23);
+        uint32_t am2 = valid ? *reinterpret_cast<const uint32_t *>(&m03) : 0u;
+        uint32_t am = max(am2 & 0xFFFFu, am2 >> 16);
+        am = max(am, __shfl_xor_sync(0xffffffffu, am, 1));
+        am = max(am, __shfl_xor_sync(0xffffffffu, am, 2));
+        am = max(am, __shfl_xor_sync(0xffffffffu, am, 4));
+        am = max(am, __shfl_xor_sync(0xffffffffu, am, 8));
+        const float amax = __uint_as_float(am << 16);
+        const float2 sg = scale_of(table, amax);
+        uint32_t out[2];
+        quant_words<1, 4>(yw, fy, sg.x, sg.y, out);
+        if (a.q && valid) {
+          *reinterpret_cast<uint2 *>(a.q + row * a.K + k) = make_uint2(out[0], out[1]);
+          if ((t & 15) == 0) {
+            const int gi = k / 128;
+            if (a.s_layout == 0) a.s[row * a.lds + gi] = sg.x;
+            else a.s[static_cast<int64_t>(gi) * a.lds + row] = sg.x;
+          }
+        }
+      } else if (QMODE == 2) {
+        uint32_t out[2];
+        if (sc.divide) {
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            uint32_t codes = 0;
+#pragma unroll
+            for (int j = 0; j < 4; j += 2) {
+              const uint32_t pr = __nv_cvt_float2_to_fp8x2(
+                  make_float2(__fdiv_rn(fy[4 * i + j], sc.s), __fdiv_rn(fy[4 * i + j + 1], sc.s)),
+                  __NV_SATFINITE, __NV_E4M3);
+              codes |= (pr & 0xFFFFu) << (8 * j);
+            }
+            out[i] = codes;
+          }
+        } else {
+          uint4 cl = make_uint4(yw[0], yw[1], yw[2], yw[3]);
+          clamp_bf16x2(cl, sc.nlim2, sc.lim2);
+          const uint32_t cw[4] = {cl.x, cl.y, cl.z, cl.w};
+          float fc[8];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            fc[2 * i] = bf16_lo(cw[i]);
+            fc[2 * i + 1] = bf16_hi(cw[i]);
+          }
+          quant_words<2, 4>(yw, fc, sc.s, sc.r, out);
+        }
+        if (a.q && valid) *reinterpret_cast<uint2 *>(a.q + row * a.K + k) = make_uint2(out[0], out[1]);
+      }
+    }
+  }
+}
+
+// One kernel instance: its opt-in shared-memory limit (for its largest rows,
+// set once) and its CTAs per SM at the last size asked for, both per instance.
+template <auto KERN, int THREADS, int MAX_K>
+cudaError_t launch_norm_instance(const NormArgs &a, size_t smem, int num_sms, cudaStream_t st) {
+  static const cudaError_t attr = cudaFuncSetAttribute(
+      KERN, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * 2 * ((MAX_K * 2 + 127) / 128 * 128));
+  static std::mutex mu;
+  static size_t last_smem = ~size_t(0);
+  static int last_n = 1;
+  if (attr != cudaSuccess) return attr;
+  int n;
+  {
+    std::lock_guard<std::mutex> g(mu);
+    if (smem != last_smem) {
+      int q = 0;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&q, KERN, THREADS, smem) != cudaSuccess ||
+          q < 1) {
+        cudaGetLastError();  // not the launch's error
+        q = 1;
+      }
+      last_smem = smem;
+      last_n = q;
+    }
+    n = last_n;
+  }
+  const int64_t cap = static_cast<int64_t>(num_sms) * n;
+  const int64_t grid = a.M < cap ? a.M : cap;
+  return launch_pdl(KERN, dim3(static_cast<unsigned>(grid < 1 ? 1 : grid)), dim3(THREADS), smem, st,
+                    a);
+}
+
+template <int QMODE>
+cudaError_t launch_norm_mode(const NormArgs &a, int num_sms, cudaStream_t st) {
+  // two stages of [x row][residual row], rows padded to 128 bytes
+  const size_t pitch = (static_cast<size_t>(a.K) * 2 + 127) / 128 * 128;
+  const size_t smem = 2 * pitch * (a.res ? 2 : 1);
+  // 256 threads per row up to 8192 channels, 512 beyond; CH 8-channel chunks each
+  const int chunks = (a.K + 7) / 8;
+  if (chunks <= 256)
+    return launch_norm_instance<add_rmsnorm_kernel<256, 1, QMODE>, 256, 2048>(a, smem, num_sms, st);
+  if (chunks <= 512)
+    return launch_norm_instance<add_rmsnorm_kernel<256, 2, QMODE>, 256, 4096>(a, smem, num_sms, st);
+  if (chunks <= 768)
+    return launch_norm_instance<add_rmsnorm_kernel<256, 3, QMODE>, 256, 6144>(a, smem, num_sms, st);
+  if (chunks <= 1024)
+    return launch_norm_instance<add_rmsnorm_kernel<256, 4, QMODE>, 256, 8192>(a, smem, num_sms, st);
+  if (chunks <= 1536)
+    return launch_norm_instance<add_rmsnorm_kernel<512, 3, QMODE>, 512, 12288>(a, smem, num_sms, st);
+  return launch_norm_instance<add_rmsnorm_kernel<512, 4, QMODE>, 512, 16384>(a, smem, num_sms, st);
+}
+
+}  // namespace
+
+cudaError_t launch_add_rmsnorm(const void *x, int64_t ldx, const void *res, int64_t ldr,
+                               void *r_out, const void *g, float eps, int64_t M, int64_t K,
+                               void *y, void *q, float *s, int s_layout, const float *s_x,
+                               int num_sms, cudaStream_t st) {
+  NormArgs a{};
+  a.x = static_cast<const uint8_t *>(x);
+  a.ldx_bytes = ldx * 2;
+  a.res = static_cast<const uint8_t *>(res);
+  a.ldr_bytes = ldr * 2;
+  a.r_out = static_cast<uint8_t *>(r_out);
+  a.g = static_cast<const uint8_t *>(g);
+  a.eps = eps;
+  a.M = M;
+  a.K = static_cast<int>(K);
+  a.y = static_cast<uint8_t *>(y);
+  a.q = static_cast<uint8_t *>(q);
+  a.s = s;
+  a.s_layout = s_layout;
+  const int64_t G = (K + 127) / 128;
+  a.lds = s_layout == 0 ? G : ((M + 3) / 4) * 4;
+  a.s_x = s_x;
+  if (q == nullptr) return launch_norm_mode<0>(a, num_sms, st);
+  if (s_x == nullptr) return launch_norm_mode<1>(a, num_sms, st);
+  return launch_norm_mode<2>(a, num_sms, st);
+}
+
+}  // namespace fp8bq

@@ -193,6 +193,40 @@ FP8BQ_API int fp8bq_mx_linear(const void *x, int64_t ldx, const void *w,
                               int64_t M, int64_t N, int64_t K, void *ws,
                               size_t ws_bytes, void *stream);
 
+/* ------------------------------------------------ residual add + RMSNorm + quant */
+
+/* The step before the linear's activation quantiser, fused with it
+ * ("GLM-5.3 推理全链路(十七)", §第1站 RMSNorm 的两个出口: residual add, RMSNorm
+ * y = x / sqrt(mean(x^2) + eps) * g with the sum and the root in FP32, BF16 out;
+ * the static per-tensor path fuses the quantisation into the same launch):
+ *   r = BF16(x + residual)          (residual == NULL: r = x)
+ *   S = sum_k r_k^2, the exact sum rounded once to binary32
+ *   rms = sqrt(RN32(RN32(S / K) + eps))          (IEEE binary32 operations)
+ *   y_k = BF16(RN32(RN32(r_k / rms) * gamma_k))
+ * then q, s = the group-128 quantisation of y (fp8bq_quant_act's rule), bit for
+ * bit the same as quantising a separately written y.
+ * x: BF16 [M, K] pitch ldx; residual: BF16 [M, K] pitch ld_res or NULL;
+ * residual_out: BF16 [M, K] (contiguous) or NULL -- it may be the residual
+ * buffer itself (in place) when ld_res == K, no other outputs may overlap an
+ * input; gamma: BF16 [K]; eps: finite, >= 0; y: BF16 [M, K] or NULL.  q: E4M3
+ * [M, K] and s: FP32 scales in `s_layout`, or q == NULL for the norm alone.
+ * K % 16 == 0, K <= 16384; every pointer 16-byte aligned (s: 4). */
+FP8BQ_API int fp8bq_add_rmsnorm_quant_act(const void *x, int64_t ldx,
+                                          const void *residual, int64_t ld_res,
+                                          void *residual_out, const void *gamma,
+                                          float eps, int64_t M, int64_t K, void *y,
+                                          void *q, float *s, int s_layout,
+                                          void *stream);
+
+/* As fp8bq_add_rmsnorm_quant_act, then static per-tensor quantisation of y with
+ * the device-resident scale s_x[0] (fp8bq_static_quant_act's rule) into q. */
+FP8BQ_API int fp8bq_add_rmsnorm_static_quant_act(const void *x, int64_t ldx,
+                                                 const void *residual, int64_t ld_res,
+                                                 void *residual_out, const void *gamma,
+                                                 float eps, const float *s_x, int64_t M,
+                                                 int64_t K, void *y, void *q,
+                                                 void *stream);
+
 /* ------------------------------------------------ static per-tensor path */
 
 /* Static quantisation with one device-resident FP32 scale s_x[0]:

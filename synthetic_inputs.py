@@ -8,13 +8,16 @@ Recipe (identical on every machine that runs the same numpy):
   * splitmix64 as a counter-based generator: output i of stream s is
     mix64(seed_s + (i + 1) * 0x9E3779B97F4A7C15), seed_s = base_seed + s.
     Streams: 0 = activations X, 1 = weights W, 2 = calibration batch,
-    3 = outlier-channel pick.
+    3 = outlier-channel pick, 4 = residual stream, 5 = norm gains.
   * uniform u = (z >> 11) * 2^-53; normal by Box-Muller (cosine branch), element
     e using outputs 2e and 2e+1: sqrt(-2 ln(1 - u0)) * cos(2 pi u1).
   * value = sigma * normal, times `outlier_scale` on the outlier channels, then
     rounded binary64 -> binary32 -> BF16 (nearest-even at each step).
   * outlier channels: round(frac * K) channels from a partial Fisher-Yates
     shuffle of 0..K-1 driven by stream 3.
+  * residual stream: sigma 4, the outlier channels x20 (the large channels of
+    a transformer's residual stream); norm gains: exp(0.5 * normal), a
+    positive log-normal spread around 1.
 
 BF16 tensors are returned as numpy.uint16 bit patterns, row-major.
 """
@@ -30,6 +33,7 @@ _M1 = np.uint64(0xBF58476D1CE4E5B9)
 _M2 = np.uint64(0x94D049BB133111EB)
 
 STREAM_X, STREAM_W, STREAM_CALIB, STREAM_OUTLIER = 0, 1, 2, 3
+STREAM_RES, STREAM_GAIN = 4, 5
 
 
 def _mix64(z: np.ndarray) -> np.ndarray:
@@ -152,10 +156,24 @@ def calibration(rows: int, K: int, base_seed: int = 0) -> np.ndarray:
     return normal_bf16(rows, K, 1.0, STREAM_CALIB, base_seed)
 
 
+def residual_stream(M: int, K: int, base_seed: int = 0) -> np.ndarray:
+    """Residual stream R ~ N(0, 4^2) [M, K], outlier channels x20."""
+    return normal_bf16(M, K, 4.0, STREAM_RES, base_seed, outlier_channels(K, 0.01, base_seed), 20.0)
+
+
+def norm_gain(K: int, base_seed: int = 0) -> np.ndarray:
+    """Per-channel norm gains g = exp(0.5 * N(0,1)) [K] as BF16 bits."""
+    z = _normals(base_seed + STREAM_GAIN, 0, K)
+    return f32_to_bf16_bits(np.exp(0.5 * z).astype(np.float32))
+
+
 # Shapes of the five workloads.
 TINY = dict(M=16, K=256, N=384)
 DECODE = dict(K=6144, N=6144, M_list=(1, 8, 32, 64))
 PREFILL = dict(M=4096, K=6144, N_list=(6144, 24576))
 MXFP8 = dict(M=2048, K=7168, N=4096)
+# residual add + RMSNorm + quantisation before the linear: the hidden size
+# 6144 (dynamic group-128) and the static workload's 4096 channels
+NORM = dict(M_list=(1, 512, 4096), K_list=(6144, 4096), eps=1e-5)
 STATIC = dict(M_list=(1, 512, 4096), K=4096, N=14336, parts=(4096, 4096, 6144),
               calib_rows=256)
