@@ -14,8 +14,9 @@ Also reported, measured in the same run:
   e2e          the same metric through fp8bq_linear with host buffers, the
                pinned-host -> device copy of X and the device -> host copy of Y
                inside the timed region;
-  extra        decode (M in {1,8,32,64}) and quantiser GB/s against HBM, MXFP8
-               and static per-tensor TFLOPS;
+  extra        decode (M in {1,8,32,64}), quantiser and fused residual-add +
+               RMSNorm + quantisation GB/s against HBM, MXFP8 and static
+               per-tensor TFLOPS;
   cpu_baseline the CPU oracle on a bounded sample of the same workload.
 
 L2 is flushed (256 MiB write) between timed steps; every step is timed with
@@ -389,7 +390,8 @@ def _copies(t, n):
 
 
 def run_extra(fb, torch, dev, stream, hbm_peak, fp8_peak):
-    """Decode and quantiser GB/s, MXFP8 and static TFLOPS (informational).  Each
+    """Decode, quantiser and fused residual-add + RMSNorm + quantisation GB/s,
+    MXFP8 and static TFLOPS (informational).  Each
     figure is the mean over back-to-back launches rotating through enough input
     copies to exceed 1.5x the L2 size.  Launches shorter than the host's own
     cost per call (about 11 us through the Python binding) are timed inside a
@@ -515,6 +517,43 @@ def run_extra(fb, torch, dev, stream, hbm_peak, fp8_peak):
                       "gbs": round(b / (t * 1e-3) / 1e9, 1),
                       "frac_hbm": round(b / (t * 1e-3) / 1e9 / hbm_peak, 4)}
     out["static_N14336_K4096"] = st
+    del qwss, qws
+
+    # residual add + RMSNorm + quantisation (the step before the linear):
+    # x, residual in; updated residual, E4M3 codes (and group scales) out
+    norm = {}
+    eps = si.NORM["eps"]
+    cases = [("group", 4096, 6144), ("group", 64, 6144), ("group", 1, 6144),
+             ("static", 4096, 4096), ("static", 512, 4096), ("static", 1, 4096)]
+    for mode, M, K in cases:
+        b = M * K * 2 * 3 + M * K + 2 * K + (M * (K // 128) * 4 if mode == "group" else 0)
+        ns = n_sets(b)
+        xs = _copies(to_dev(si.activations(M, K)), ns)
+        rs = _copies(to_dev(si.residual_stream(M, K)), ns)
+        gn = to_dev(si.norm_gain(K))
+        if mode == "static":  # the scale of the normalised rows, from one run
+            y0 = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
+            fb.fp8bq_add_rmsnorm_quant_act(xs[0], gn, eps, residual=rs[0], y=y0)
+            s_n = torch.empty(1, dtype=torch.float32, device=dev)
+            fb.fp8bq_absmax_scale(y0, s_n)
+            del y0
+        ros = [torch.empty(M, K, dtype=torch.bfloat16, device=dev) for _ in range(ns)]
+        qs = [torch.empty(M, K, dtype=torch.uint8, device=dev) for _ in range(ns)]
+        if mode == "group":
+            ss = [torch.empty(M, K // 128, dtype=torch.float32, device=dev) for _ in range(ns)]
+            fns = [lambda i=i: fb.fp8bq_add_rmsnorm_quant_act(
+                xs[i], gn, eps, residual=rs[i], residual_out=ros[i], q=qs[i], s=ss[i])
+                for i in range(ns)]
+        else:
+            fns = [lambda i=i: fb.fp8bq_add_rmsnorm_static_quant_act(
+                xs[i], gn, eps, s_n, qs[i], residual=rs[i], residual_out=ros[i])
+                for i in range(ns)]
+        t = _time_graph(torch, fns, 2 * ns)
+        norm[f"{mode}_{M}x{K}"] = {"us": round(t * 1e3, 2),
+                                   "gbs": round(b / (t * 1e-3) / 1e9, 1),
+                                   "frac_hbm": round(b / (t * 1e-3) / 1e9 / hbm_peak, 4)}
+        del xs, rs, ros, qs
+    out["add_rmsnorm_quant"] = norm
     return out
 
 
