@@ -75,6 +75,9 @@ _SIGS = {
     "orc_bf16_from_f64": (ctypes.c_uint16, [ctypes.c_double]),
     "orc_sumsq_f32": (ctypes.c_float, [_P, _I64]),
     "orc_add_rmsnorm": (None, [_P, _I64, _P, _I64, _P, ctypes.c_float, _I64, _I64, _P, _P]),
+    "orc_gemm_channel": (None, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P, ctypes.c_int]),
+    "orc_gemm_channel_sampled": (None, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _I64,
+                                        _P, ctypes.c_int]),
     "orc_e4m3_dot_int": (ctypes.c_int64, [_P, _P, _I64]),
     "orc_e4m3_dot_f64": (ctypes.c_double, [_P, _P, _I64]),
 }
@@ -164,6 +167,14 @@ def quant_mx(x):
     u = np.empty((M, K // 32), np.uint8)
     lib().orc_quant_mx(_p(x), M, K, K, _p(q), _p(u))
     return q, u
+
+
+def quant_channel(x):
+    """Per-token (or, for weights, per-channel) quantisation: one scale per row,
+    the group rule with the group spanning the whole row -> (q [M,K], s [M])."""
+    x = _c(x, np.uint16)
+    q, s = quant_group(x, group=x.shape[1])
+    return q, s.reshape(-1)
 
 
 def quant_static(x, s: float):
@@ -352,3 +363,32 @@ def e4m3_dot_int(a, b) -> int:
 def e4m3_dot_f64(a, b) -> float:
     a, b = _c(a, np.uint8), _c(b, np.uint8)
     return float(lib().orc_e4m3_dot_f64(_p(a), _p(b), a.size))
+
+
+def gemm_channel(qa, sa, qw, sw, bias=None, threads: int | None = None) -> np.ndarray:
+    """Channelwise GEMM: y[i,j] = (sum_k qa*qw) * sa[i] * sw[j] (+bias), binary64."""
+    qa, qw = _c(qa, np.uint8), _c(qw, np.uint8)
+    sa, sw = _c(sa, np.float32).ravel(), _c(sw, np.float32).ravel()
+    M, K = qa.shape
+    N = qw.shape[0]
+    if sa.size != M or sw.size != N:
+        raise ValueError("one activation scale per row, one weight scale per output channel")
+    b = _bias(bias)
+    y = np.empty((M, N), np.float64)
+    lib().orc_gemm_channel(_p(qa), _p(sa), _p(qw), _p(sw), _p(b), M, N, K, _p(y),
+                           threads or default_threads())
+    return y
+
+
+def gemm_channel_sampled(qa, sa, qw, sw, rows, cols, bias=None,
+                         threads: int | None = None) -> np.ndarray:
+    qa, qw = _c(qa, np.uint8), _c(qw, np.uint8)
+    sa, sw = _c(sa, np.float32).ravel(), _c(sw, np.float32).ravel()
+    rows, cols = _c(rows, np.int64), _c(cols, np.int64)
+    M, K = qa.shape
+    N = qw.shape[0]
+    b = _bias(bias)
+    y = np.empty(rows.size, np.float64)
+    lib().orc_gemm_channel_sampled(_p(qa), _p(sa), _p(qw), _p(sw), _p(b), M, N, K, _p(rows),
+                                   _p(cols), rows.size, _p(y), threads or default_threads())
+    return y

@@ -258,12 +258,13 @@ double orc_e4m3_dot_f64(const uint8_t *a, const uint8_t *b, int64_t n) {
   return acc;
 }
 
-enum { KIND_BLOCK = 0, KIND_MX = 1, KIND_STATIC = 2 };
+enum { KIND_BLOCK = 0, KIND_MX = 1, KIND_STATIC = 2, KIND_CHANNEL = 3 };
 
 typedef struct {
   int kind;
   const uint8_t *qa, *qw;
-  const float *sa, *sw;    /* block: row-major grids; static: sa[0] = s_x, sw = s_part */
+  const float *sa, *sw;    /* block: row-major grids; static: sa[0] = s_x, sw = s_part;
+                              channel: sa[M] per token, sw[N] per output channel */
   const uint8_t *ua, *uw;  /* MX scale codes */
   const int64_t *part_sizes;
   int n_parts;
@@ -318,6 +319,15 @@ static double elem_static(const gemm_job *g, int64_t i, int64_t j) {
   return acc * (double)g->sa[0] * (double)g->sw[p];
 }
 
+/* Channelwise element: one dynamic scale per token (activation row) and one
+ * per output channel (weight row) come out of the full-K sum ([SGL-19]
+ * §一条 GEMM 的三种缩放组合, the per-token x per-channel case:
+ * Y_ij = (sum_k Qx[i,k] Qw[j,k]) * s_x[i] * s_w[j]). */
+static double elem_channel(const gemm_job *g, int64_t i, int64_t j) {
+  double acc = orc_e4m3_dot_f64(g->qa + i * g->K, g->qw + j * g->K, g->K);
+  return acc * (double)g->sa[i] * (double)g->sw[j];
+}
+
 static void *gemm_worker(void *arg) {
   const gemm_job *g = (const gemm_job *)arg;
   for (int64_t t = g->t0; t < g->t1; ++t) {
@@ -332,6 +342,7 @@ static void *gemm_worker(void *arg) {
     double y;
     if (g->kind == KIND_BLOCK) y = elem_block(g, i, j);
     else if (g->kind == KIND_MX) y = elem_mx(g, i, j);
+    else if (g->kind == KIND_CHANNEL) y = elem_channel(g, i, j);
     else y = elem_static(g, i, j);
     if (g->bias) y += (double)orc_bf16_to_f32(g->bias[j]); /* epilogue bias */
     g->y[t] = y;
@@ -557,4 +568,24 @@ void orc_add_rmsnorm(const uint16_t *x, int64_t ldx, const uint16_t *res,
       y[i * d + k] = orc_bf16_from_f64((double)b);
     }
   }
+}
+
+void orc_gemm_channel(const uint8_t *qa, const float *sa, const uint8_t *qw,
+                      const float *sw, const uint16_t *bias, int64_t M, int64_t N,
+                      int64_t K, double *y, int nthreads) {
+  gemm_job g = job0(KIND_CHANNEL, M, N, K, y, bias);
+  g.qa = qa; g.qw = qw; g.sa = sa; g.sw = sw;
+  run_gemm(g, nthreads);
+}
+
+void orc_gemm_channel_sampled(const uint8_t *qa, const float *sa,
+                              const uint8_t *qw, const float *sw,
+                              const uint16_t *bias, int64_t M, int64_t N,
+                              int64_t K, const int64_t *rows,
+                              const int64_t *cols, int64_t n, double *y,
+                              int nthreads) {
+  gemm_job g = job0(KIND_CHANNEL, M, N, K, y, bias);
+  g.qa = qa; g.qw = qw; g.sa = sa; g.sw = sw;
+  g.rows = rows; g.cols = cols; g.n = n;
+  run_gemm(g, nthreads);
 }

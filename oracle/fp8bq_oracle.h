@@ -51,6 +51,17 @@ void orc_quant_static(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
 float orc_absmax_scale(const uint16_t *x, int64_t r0, int64_t r1, int64_t K,
                        int64_t ldx);
 
+/* Channelwise (per-token x per-channel): y = (sum_k qa*qw) * sa[i] * sw[j]. */
+void orc_gemm_channel(const uint8_t *qa, const float *sa, const uint8_t *qw,
+                      const float *sw, const uint16_t *bias, int64_t M, int64_t N,
+                      int64_t K, double *y, int nthreads);
+void orc_gemm_channel_sampled(const uint8_t *qa, const float *sa,
+                              const uint8_t *qw, const float *sw,
+                              const uint16_t *bias, int64_t M, int64_t N,
+                              int64_t K, const int64_t *rows,
+                              const int64_t *cols, int64_t n, double *y,
+                              int nthreads);
+
 /* ---- residual add + RMSNorm (the step before the activation quantiser) -- */
 /* binary64 -> BF16 (RNE, overflow to infinity).                             */
 uint16_t orc_bf16_from_f64(double v);
