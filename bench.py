@@ -15,8 +15,8 @@ Also reported, measured in the same run:
                pinned-host -> device copy of X and the device -> host copy of Y
                inside the timed region;
   extra        decode (M in {1,8,32,64}), quantiser and fused residual-add +
-               RMSNorm + quantisation GB/s against HBM, MXFP8 and static
-               per-tensor TFLOPS;
+               RMSNorm + quantisation GB/s against HBM, MXFP8, static
+               per-tensor and channelwise TFLOPS;
   cpu_baseline the CPU oracle on a bounded sample of the same workload.
 
 L2 is flushed (256 MiB write) between timed steps; every step is timed with
@@ -518,6 +518,56 @@ def run_extra(fb, torch, dev, stream, hbm_peak, fp8_peak):
                       "frac_hbm": round(b / (t * 1e-3) / 1e9 / hbm_peak, 4)}
     out["static_N14336_K4096"] = st
     del qwss, qws
+
+    # channelwise W8A8: per-token quantiser, GEMM at the prefill and decode shapes
+    ch = {}
+    M, K = si.PREFILL["M"], si.PREFILL["K"]
+    b = M * K * 3 + M * 4
+    ns = n_sets(b)
+    xs = _copies(to_dev(si.activations(M, K)), ns)
+    qs = [torch.empty(M, K, dtype=torch.uint8, device=dev) for _ in range(ns)]
+    ss = [torch.empty(M, dtype=torch.float32, device=dev) for _ in range(ns)]
+    t = _time_graph(torch, [lambda i=i: fb.fp8bq_channel_quant_act(xs[i], qs[i], ss[i])
+                            for i in range(ns)], 2 * ns)
+    ch["quant_4096x6144"] = {"us": round(t * 1e3, 2), "gbs": round(b / (t * 1e-3) / 1e9, 1),
+                             "frac_hbm": round(b / (t * 1e-3) / 1e9 / hbm_peak, 4)}
+    qa, sa = qs[0], ss[0]
+    del xs
+    for N in si.PREFILL["N_list"]:
+        wb = to_dev(si.weights(N, K))
+        qw = torch.empty(N, K, dtype=torch.uint8, device=dev)
+        sw = torch.empty(N, dtype=torch.float32, device=dev)
+        fb.fp8bq_channel_quant_act(wb, qw, sw)
+        del wb
+        y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        ws = fb.new_workspace(fb.OP_CHANNEL_GEMM, M, N, K, device=dev)
+        t = _time_back_to_back(torch, stream, [lambda: fb.fp8bq_channel_gemm(qa, sa, qw, sw, y, ws)], 20)
+        tf = 2.0 * M * N * K / (t * 1e-3) / 1e12
+        ch[f"gemm_{M}x{N}x{K}"] = {"us": round(t * 1e3, 2), "tflops": round(tf, 1),
+                                   "frac_fp8": round(tf / fp8_peak, 4)}
+        del qw, sw, y
+    K = N = si.DECODE["K"]
+    wb = to_dev(si.weights(N, K))
+    qw = torch.empty(N, K, dtype=torch.uint8, device=dev)
+    sw = torch.empty(N, dtype=torch.float32, device=dev)
+    fb.fp8bq_channel_quant_act(wb, qw, sw)
+    del wb
+    ns = n_sets(N * K)
+    qws, sws = _copies(qw, ns), _copies(sw, ns)
+    for M in si.DECODE["M_list"]:
+        qd = torch.empty(M, K, dtype=torch.uint8, device=dev)
+        sd = torch.empty(M, dtype=torch.float32, device=dev)
+        fb.fp8bq_channel_quant_act(to_dev(si.activations(M, K)), qd, sd)
+        y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        ws = fb.new_workspace(fb.OP_CHANNEL_GEMM, M, N, K, device=dev)
+        t = _time_graph(torch, [lambda i=i: fb.fp8bq_channel_gemm(qd, sd, qws[i], sws[i], y, ws)
+                                for i in range(ns)], 2 * ns)
+        bb = N * K + N * 4 + M * (K + 4) + 2 * M * N
+        ch[f"gemm_decode_{M}x{N}x{K}"] = {"us": round(t * 1e3, 2),
+                                          "gbs": round(bb / (t * 1e-3) / 1e9, 1),
+                                          "frac_hbm": round(bb / (t * 1e-3) / 1e9 / hbm_peak, 4)}
+    out["channel_w8a8"] = ch
+    del qw, sw, qws, sws
 
     # residual add + RMSNorm + quantisation (the step before the linear):
     # x, residual in; updated residual, E4M3 codes (and group scales) out

@@ -23,7 +23,9 @@ from . import _build
 
 __all__ = [
     "Fp8bqError", "SCALE_ROW_MAJOR", "SCALE_COL_MAJOR", "OP_GEMM", "OP_LINEAR",
-    "OP_MX_GEMM", "OP_MX_LINEAR", "OP_STATIC_GEMM", "OP_STATIC_LINEAR", "library_path",
+    "OP_MX_GEMM", "OP_MX_LINEAR", "OP_STATIC_GEMM", "OP_STATIC_LINEAR", "OP_CHANNEL_GEMM",
+    "OP_CHANNEL_LINEAR", "fp8bq_channel_quant_act", "fp8bq_channel_gemm", "fp8bq_channel_linear",
+    "library_path",
     "fp8bq_version", "fp8bq_status_string", "fp8bq_last_cuda_error",
     "fp8bq_workspace_bytes", "fp8bq_workspace_init", "fp8bq_poll_status",
     "fp8bq_quant_act", "fp8bq_gemm", "fp8bq_linear", "fp8bq_gemm_noalloc",
@@ -36,7 +38,7 @@ __all__ = [
 
 SCALE_ROW_MAJOR, SCALE_COL_MAJOR = 0, 1
 (OP_GEMM, OP_LINEAR, OP_MX_GEMM, OP_MX_LINEAR, OP_STATIC_GEMM,
- OP_STATIC_LINEAR) = range(6)
+ OP_STATIC_LINEAR, OP_CHANNEL_GEMM, OP_CHANNEL_LINEAR) = range(8)
 NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024      # FP8BQ_NOALLOC_SCRATCH_BYTES
 
 STATUS_NAMES = {0: "FP8BQ_OK", 1: "FP8BQ_ERR_NULL", 2: "FP8BQ_ERR_SHAPE",
@@ -81,6 +83,9 @@ def _load():
         "fp8bq_mx_gemm": (I32, [P, P, P, P, P, P, I64, I64, I64, P, SZ, P]),
         "fp8bq_mx_linear": (I32, [P, I64, P, P, P, P, I64, I64, I64, P, SZ, P]),
         "fp8bq_static_quant_act": (I32, [P, I64, I64, I64, P, P, P]),
+        "fp8bq_channel_quant_act": (I32, [P, I64, I64, I64, P, P, P]),
+        "fp8bq_channel_gemm": (I32, [P, P, P, P, P, P, I64, I64, I64, P, SZ, P]),
+        "fp8bq_channel_linear": (I32, [P, I64, P, P, P, P, I64, I64, I64, P, SZ, P]),
         "fp8bq_add_rmsnorm_quant_act": (I32, [P, I64, P, I64, P, P, F32, I64, I64, P, P, P,
                                               I32, P]),
         "fp8bq_add_rmsnorm_static_quant_act": (I32, [P, I64, P, I64, P, P, F32, P, I64, I64,
@@ -240,6 +245,29 @@ def fp8bq_static_quant_act(x, s_x, q, stream=None):
     M, K = x.shape
     _check(_lib.fp8bq_static_quant_act(_ptr(x), M, K, _ld(x), _ptr(s_x), _ptr(q),
                                        _stream(stream)), "fp8bq_static_quant_act")
+
+
+def fp8bq_channel_quant_act(x, q, s, stream=None):
+    """One scale per row (per-token activations, or per-channel weights)."""
+    M, K = x.shape
+    _check(_lib.fp8bq_channel_quant_act(_ptr(x), M, K, _ld(x), _ptr(q), _ptr(s),
+                                        _stream(stream)), "fp8bq_channel_quant_act")
+
+
+def fp8bq_channel_gemm(q, s_x, w, s_w, y, ws, bias=None, stream=None):
+    M, K = q.shape
+    N = w.shape[0]
+    _check(_lib.fp8bq_channel_gemm(_ptr(q), _ptr(s_x), _ptr(w), _ptr(s_w), _ptr(bias), _ptr(y),
+                                   M, N, K, _ptr(ws), _nbytes(ws), _stream(stream)),
+           "fp8bq_channel_gemm")
+
+
+def fp8bq_channel_linear(x, w, s_w, y, ws, bias=None, stream=None):
+    M, K = x.shape
+    N = w.shape[0]
+    _check(_lib.fp8bq_channel_linear(_ptr(x), _ld(x), _ptr(w), _ptr(s_w), _ptr(bias), _ptr(y),
+                                     M, N, K, _ptr(ws), _nbytes(ws), _stream(stream)),
+           "fp8bq_channel_linear")
 
 
 def fp8bq_add_rmsnorm_quant_act(x, gamma, eps: float, residual=None, residual_out=None,

@@ -17,7 +17,8 @@ LIB = os.path.join(OUT, "libfp8bq.so")
 INCLUDE = os.path.join(os.path.dirname(PKG), "include")
 
 SOURCES = ["fp8bq_api.cu", "quant.cu", "gemm_launch.cu", "gemm_block.cu",
-           "gemm_tensor.cu", "gemm_mx.cu", "norm_quant.cu"]
+           "gemm_tensor.cu", "gemm_mx.cu", "gemm_channel.cu",
+           "norm_quant.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC",
                      "-Xcompiler", "-fvisibility=hidden", "-I", INCLUDE]

@@ -47,6 +47,9 @@ void launch_quant_mx(const void *x, int64_t M, int64_t K, int64_t ldx, void *q, 
                      int num_sms, cudaStream_t st);
 void launch_quant_static(const void *x, int64_t M, int64_t K, int64_t ldx, const float *s,
                          void *q, int num_sms, cudaStream_t st);
+// One scale per row: s[i] = max(amax_i, 1e-10) / 448, q = RNE_sat(x / s[i]).
+void launch_quant_token(const void *x, int64_t M, int64_t K, int64_t ldx, void *q, float *s,
+                        int num_sms, cudaStream_t st);
 // Residual add + RMSNorm, then (q != null) group-128 quantisation (s_x == null)
 // or static quantisation with the scale s_x[0].  res, r_out, y may be null.
 cudaError_t launch_add_rmsnorm(const void *x, int64_t ldx, const void *res, int64_t ldr,
@@ -60,13 +63,16 @@ void launch_absmax_scale(const void *x, int64_t rows, int64_t K, int64_t ldx, fl
 
 // ---------------------------------------------------------------- GEMM
 
-enum GemmMode : int { kModeBlock = 0, kModeTensor = 1, kModeMx = 2 };
+// kModeChannel: one FP32 scale per token (activation row) and per output
+// channel (weight row), applied after the full-K sum like kModeTensor's
+enum GemmMode : int { kModeBlock = 0, kModeTensor = 1, kModeMx = 2, kModeChannel = 3 };
 
 // Everything a GEMM launch needs besides the two tensor maps.
 struct GemmArgs {
   int mode;
   int M, N, K;
-  // block path
+  // block path; the channel path uses sx [M] (per token) and sw [N] (per
+  // output channel)
   const float *sx;
   int sx_layout;  // 0 row-major [M][KB], 1 column-major [KB][ldsx]
   int ldsx;       // KB for row-major, round_up(M,4) for column-major
@@ -157,6 +163,10 @@ cudaError_t run_tensor_pair(int bn, const GemmArgs &a, const void *q, const void
                             const LaunchShape &sh, int grid, cudaStream_t st, int *status);
 cudaError_t run_tensor_swap(int bn, const GemmArgs &a, const void *q, const void *w,
                             const LaunchShape &sh, int grid, cudaStream_t st, int *status);
+cudaError_t run_channel_pair(int bn, const GemmArgs &a, const void *q, const void *w,
+                             const LaunchShape &sh, int grid, cudaStream_t st, int *status);
+cudaError_t run_channel_swap(int bn, const GemmArgs &a, const void *q, const void *w,
+                             const LaunchShape &sh, int grid, cudaStream_t st, int *status);
 cudaError_t run_mx_normal(const GemmArgs &a, const void *q, const void *w,
                           const LaunchShape &sh, int grid, cudaStream_t st, int *status);
 cudaError_t run_mx_pair(const GemmArgs &a, const void *q, const void *w, const LaunchShape &sh,

@@ -176,6 +176,17 @@ int gemm_mx_impl(const void *q, const uint8_t *s_x, const void *w, const uint8_t
   return finish_launch(r, e);
 }
 
+int gemm_channel_impl(const void *q, const float *s_x, const void *w, const float *s_w,
+                      const void *bias, void *y, int64_t M, int64_t N, int64_t K, void *ws, int op,
+                      cudaStream_t st, const DeviceInfo &dev) {
+  GemmArgs a = base_args(kModeChannel, M, N, K, bias, y, ws, op);
+  a.sx = s_x;
+  a.sw = s_w;
+  cudaError_t e;
+  int r = launch_gemm(a, q, w, dev, st, &e);
+  return finish_launch(r, e);
+}
+
 int gemm_static_impl(const void *q, const float *s_x, const void *w, const float *s_w_part,
                      const int64_t *parts, int n_parts, const void *bias, void *y, int64_t M,
                      int64_t N, int64_t K, void *ws, int op, cudaStream_t st,
@@ -266,7 +277,7 @@ const char *fp8bq_status_string(int s) {
 int fp8bq_last_cuda_error(void) { return g_last_cuda_error; }
 
 size_t fp8bq_workspace_bytes(int op, int64_t M, int64_t N, int64_t K) {
-  if (op < FP8BQ_OP_GEMM || op > FP8BQ_OP_STATIC_LINEAR || M < 0 || N < 1 || K < 1) return 256;
+  if (op < FP8BQ_OP_GEMM || op > FP8BQ_OP_CHANNEL_LINEAR || M < 0 || N < 1 || K < 1) return 256;
   return workspace_layout(op, M, N, K).total;
 }
 
@@ -593,6 +604,60 @@ int fp8bq_gemm_noalloc(const void *q, const float *s_x, int s_layout, const void
   if (e != cudaSuccess) return cuda_fail(e);
   return gemm_block_impl(q, s_x, s_layout, w, s_w, bias, y, M, N, K, scratch, FP8BQ_OP_GEMM, st,
                          dev);
+}
+
+
+// ------------------------------------------------------------------ channelwise path
+
+int fp8bq_channel_quant_act(const void *x, int64_t M, int64_t K, int64_t ldx, void *q, float *s,
+                            void *stream) {
+  if (M == 0) return empty_batch(K, 1);
+  if (!q || !s) return FP8BQ_ERR_NULL;
+  RETURN_IF(check_act(x, M, K, ldx, 16));
+  if (!aligned(q, 16) || !aligned(s, 4)) return FP8BQ_ERR_ALIGN;
+  DeviceInfo dev;
+  RETURN_IF(device_info(&dev));
+  launch_quant_token(x, M, K, ldx, q, s, dev.num_sms, static_cast<cudaStream_t>(stream));
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? FP8BQ_OK : cuda_fail(e);
+}
+
+int fp8bq_channel_gemm(const void *q, const float *s_x, const void *w, const float *s_w,
+                       const void *bias, void *y, int64_t M, int64_t N, int64_t K, void *ws,
+                       size_t ws_bytes, void *stream) {
+  if (M == 0) return empty_batch(K, N);
+  if (!q || !s_x || !w || !s_w || !y) return FP8BQ_ERR_NULL;
+  RETURN_IF(check_gemm_shape(M, N, K, 16));
+  if (!aligned(q, 16) || !aligned(w, 16) || !aligned(y, 16) || !aligned(s_x, 4) ||
+      !aligned(s_w, 4) || !aligned(bias, 2))
+    return FP8BQ_ERR_ALIGN;
+  RETURN_IF(check_ws(ws, ws_bytes, FP8BQ_OP_CHANNEL_GEMM, M, N, K));
+  DeviceInfo dev;
+  RETURN_IF(device_info(&dev));
+  return gemm_channel_impl(q, s_x, w, s_w, bias, y, M, N, K, ws, FP8BQ_OP_CHANNEL_GEMM,
+                           static_cast<cudaStream_t>(stream), dev);
+}
+
+int fp8bq_channel_linear(const void *x, int64_t ldx, const void *w, const float *s_w,
+                         const void *bias, void *y, int64_t M, int64_t N, int64_t K, void *ws,
+                         size_t ws_bytes, void *stream) {
+  if (M == 0) return empty_batch(K, N);
+  if (!w || !s_w || !y) return FP8BQ_ERR_NULL;
+  RETURN_IF(check_act(x, M, K, ldx, 16));
+  RETURN_IF(check_gemm_shape(M, N, K, 16));
+  if (!aligned(w, 16) || !aligned(y, 16) || !aligned(s_w, 4) || !aligned(bias, 2))
+    return FP8BQ_ERR_ALIGN;
+  RETURN_IF(check_ws(ws, ws_bytes, FP8BQ_OP_CHANNEL_LINEAR, M, N, K));
+  DeviceInfo dev;
+  RETURN_IF(device_info(&dev));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const WorkspaceLayout L = workspace_layout(FP8BQ_OP_CHANNEL_LINEAR, M, N, K);
+  uint8_t *q = static_cast<uint8_t *>(ws) + L.q;
+  float *s = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + L.s);
+  launch_quant_token(x, M, K, ldx, q, s, dev.num_sms, st);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e);
+  return gemm_channel_impl(q, s, w, s_w, bias, y, M, N, K, ws, FP8BQ_OP_CHANNEL_LINEAR, st, dev);
 }
 
 }  // extern "C"

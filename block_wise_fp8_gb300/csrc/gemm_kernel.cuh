@@ -13,16 +13,20 @@
 //                buffers so the MMA runs up to ACCB K blocks ahead of the promotion.
 //   kModeTensor  y = (sum_k q w) * s_x * s_w[p(j)]: full-K accumulation in TMEM,
 //                one scale product per column in the epilogue.
+//   kModeChannel y = (sum_k q w) * s_x[i] * s_w[j]: as kModeTensor, with one
+//                scale per token and per output channel ("SGLang 源码完全拆解
+//                (十九)", §一条 GEMM 的三种缩放组合, the M x N outer product).
 //   kModeMx      y = sum_g P_g * 2^(ua-127) * 2^(uw-127) with the block-scaled MMA
-//                (kind::mxf8f6f4, one UE8M0 scale per 32 K); the scale factors are
-//                written into TMEM by dedicated warps, so no dequantisation runs in
+//                (kind::mxf8f6f4, one UE8M0 scale per 32 K).  The codes arrive
+//                pre-arranged (one chunk per row tile and K block) with each
+//                operand stage; the MMA thread copies them into TMEM
+//                (tcgen05.cp) ahead of its MMAs, so no dequantisation runs in
 //                software ("GLM-5.3 推理全链路(十七)", §第7站).
 //
 // Roles (warp index):
 //   0            TMA producer: A and B tiles, 128 K per stage, 128B-swizzled.
 //   1            TMEM allocator and single-thread MMA issuer.
-//   2 .. 2+SFW   (MX only) scale-factor writers, one per TMEM lane quarter,
-//                loading the UE8M0 codes a few stages ahead.
+//   2            (block tiles) the second MMA issuer, alternate K blocks.
 //   rest         epilogue: TMEM -> registers -> promotion -> BF16 -> global.
 //
 // Tile forms:
@@ -725,7 +729,7 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
             store_row<C::kCPT>(y, acc, m, nbase, args);
           }
         } else {
-          // kModeTensor / kModeMx: one pass over the full-K accumulator
+          // kModeTensor / kModeChannel / kModeMx: one pass over the full-K accumulator
           const uint32_t b = uit % ACCB, ph = (uit / ACCB) & 1u;
           if (!warp_wait(&bars->tfull[b], ph, abort_flag, limit)) ok = false;
           if (named_bar_any(2, C::kEpiThreads, !ok || *abort_flag)) {
@@ -734,7 +738,10 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
           }
           tc_fence_after();
           const uint32_t tbase = tmem_base + lane_base + b * BN + col0;
-          const float sxs = (MODE == kModeTensor) ? __ldg(args.sx_scalar) : 1.0f;
+          // the activation factor: the per-tensor scale, or this row's token scale
+          const float sxs = (MODE == kModeTensor) ? __ldg(args.sx_scalar)
+                            : (MODE == kModeChannel) ? (m < args.M ? __ldg(args.sx + m) : 0.0f)
+                                                     : 1.0f;
 #pragma unroll
           for (int c = 0; c < C::kCPT / C::kCW; ++c) {
             uint32_t r[C::kCW];
@@ -769,6 +776,8 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
                   while (p < args.n_parts - 1 && n >= args.part_end[p]) ++p;
                   v[j] *= sxs * __ldg(args.sw_part + p);
                 }
+              } else if (MODE == kModeChannel) {
+                v[j] = (v[j] * sxs) * (n < args.N ? __ldg(args.sw + n) : 0.0f);
               }
               if (bias && n < args.N) v[j] += bf16_bits_to_float(bias[n]);
             }
@@ -839,12 +848,20 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
             tc_fence_before();
             __syncwarp();
             if (lane == 0) release_acc(b);
-            // one output partition per lane (weight row)
-            int p = 0;
-            while (p < args.n_parts - 1 && d_row >= args.part_end[p]) ++p;
-            const float f = __ldg(args.sx_scalar) * __ldg(args.sw_part + p);
+            if (MODE == kModeChannel) {
+              // lane = one output channel; columns = tokens, each with its scale
+              const float fw = d_row < args.N ? __ldg(args.sw + d_row) : 0.0f;
 #pragma unroll
-            for (int j = 0; j < C::kCPT; ++j) acc[j] = __uint_as_float(r[j]) * f;
+              for (int j = 0; j < C::kCPT; ++j)
+                acc[j] = (__uint_as_float(r[j]) * (j < args.M ? __ldg(args.sx + j) : 0.0f)) * fw;
+            } else {
+              // one output partition per lane (weight row)
+              int p = 0;
+              while (p < args.n_parts - 1 && d_row >= args.part_end[p]) ++p;
+              const float f = __ldg(args.sx_scalar) * __ldg(args.sw_part + p);
+#pragma unroll
+              for (int j = 0; j < C::kCPT; ++j) acc[j] = __uint_as_float(r[j]) * f;
+            }
           }
         }
 

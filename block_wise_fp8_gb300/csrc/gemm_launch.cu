@@ -179,11 +179,12 @@ WorkspaceLayout workspace_layout(int op, int64_t M, int64_t N, int64_t K) {
   const bool mx = (op == 2 || op == 3);
   if (M <= 64 && !mx) off += up(static_cast<size_t>(kMaxSplits) * M * N * 4);
   L.q = off;
-  const bool fused = (op == 1 || op == 3 || op == 5);
+  const bool fused = (op == 1 || op == 3 || op == 5 || op == 7);
   if (fused) off += up(static_cast<size_t>(M) * K);
   L.s = off;
   if (op == 1) off += up(static_cast<size_t>(M) * KB * 4);
   if (op == 3) off += up(static_cast<size_t>(M) * (K / 32));
+  if (op == 7) off += up(static_cast<size_t>(M) * 4);  // one FP32 scale per token
   L.sfa = off;
   if (mx) off += up(static_cast<size_t>(mx_sfa_bytes(M, K)));
   L.sfb = off;
@@ -220,9 +221,9 @@ int launch_gemm(const GemmArgs &a, const void *q_act, const void *w, const Devic
     sh.units = tiles * splits;
     const int bn = a.M <= 16 ? 16 : a.M <= 32 ? 32 : 64;
     sh.sx_stage = (a.mode == kModeBlock) ? bn * kps : 0;
-    *cuda_err = (a.mode == kModeBlock)
-                    ? run_block_swap(bn, a, q_act, w, sh, sh.units, st, &status)
-                    : run_tensor_swap(bn, a, q_act, w, sh, sh.units, st, &status);
+    *cuda_err = (a.mode == kModeBlock)     ? run_block_swap(bn, a, q_act, w, sh, sh.units, st, &status)
+                : (a.mode == kModeChannel) ? run_channel_swap(bn, a, q_act, w, sh, sh.units, st, &status)
+                                           : run_tensor_swap(bn, a, q_act, w, sh, sh.units, st, &status);
     return status;
   }
   if (a.mode == kModeMx) {
@@ -268,8 +269,9 @@ int launch_gemm(const GemmArgs &a, const void *q_act, const void *w, const Devic
   sh.units = sh.num_a_tiles * ((a.N + best_bn - 1) / best_bn);
   sh.sx_stage = 0;
   const int grid = sh.units < pairs ? sh.units : pairs;
-  *cuda_err = (a.mode == kModeBlock) ? run_block_pair(best_bn, a, q_act, w, sh, grid, st, &status)
-                                     : run_tensor_pair(best_bn, a, q_act, w, sh, grid, st, &status);
+  *cuda_err = (a.mode == kModeBlock)     ? run_block_pair(best_bn, a, q_act, w, sh, grid, st, &status)
+              : (a.mode == kModeChannel) ? run_channel_pair(best_bn, a, q_act, w, sh, grid, st, &status)
+                                         : run_tensor_pair(best_bn, a, q_act, w, sh, grid, st, &status);
   return status;
 }
 

@@ -153,6 +153,58 @@ __global__ void __launch_bounds__(kThreads) quant_mx_kernel(const uint8_t *__res
   }
 }
 
+// ---------------------------------------------------------------- per-token (per-row) quant
+// One scale per row, the group rule with the group spanning the row ("SGLang
+// 源码完全拆解(十九)", §激活量化: sglang_per_token_quant_fp8, one scale per
+// token; §per-channel 权重: per_token_group_quant_fp8 with group_size = K).
+// One CTA per row, persistent over rows: pass 1 reduces max|x| over the row,
+// pass 2 re-reads it (an L1 hit) and converts with the row's scale, 16
+// channels (two 16-byte words) per thread per step.  The warp maxima are
+// double-buffered by row parity, so one barrier per row suffices.
+__global__ void __launch_bounds__(kThreads) quant_token_kernel(const uint8_t *__restrict__ x,
+                                                               int64_t M, int K,
+                                                               int64_t ldx_bytes,
+                                                               uint8_t *__restrict__ q,
+                                                               float *__restrict__ s) {
+  __shared__ ScaleTable table;
+  __shared__ float red[2][kThreads / 32];
+  griddep_launch_dependents();
+  fill_scale_table(table);
+  __syncthreads();
+  griddep_wait();
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int C = K / 16;
+  int par = 0;
+  for (int64_t row = blockIdx.x; row < M; row += gridDim.x, par ^= 1) {
+    const uint8_t *xr = x + row * ldx_bytes;
+    float amax = 0.0f;
+    for (int c = t; c < C; c += kThreads) {
+      uint4 v[2];
+      v[0] = __ldg(reinterpret_cast<const uint4 *>(xr + c * 32));
+      v[1] = __ldg(reinterpret_cast<const uint4 *>(xr + c * 32 + 16));
+      float f[16];
+      unpack16(v, f);
+      amax = fmaxf(amax, amax16(f));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    if (lane == 0) red[par][warp] = amax;
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < kThreads / 32; ++i) amax = fmaxf(amax, red[par][i]);
+    const float2 sc = scale_of(table, amax);
+    for (int c = t; c < C; c += kThreads) {
+      uint4 v[2];
+      v[0] = __ldg(reinterpret_cast<const uint4 *>(xr + c * 32));
+      v[1] = __ldg(reinterpret_cast<const uint4 *>(xr + c * 32 + 16));
+      float f[16];
+      unpack16(v, f);
+      *reinterpret_cast<uint4 *>(q + row * K + c * 16) = quant16<1>(v, f, sc.x, sc.y);
+    }
+    if (t == 0) s[row] = sc.x;
+  }
+}
+
 // ---------------------------------------------------------------- static per-tensor quant
 // One thread per 16-channel chunk, persistent grid, next chunk loaded first.
 __global__ void __launch_bounds__(kThreads) quant_static_kernel(const uint8_t *__restrict__ x,
@@ -332,6 +384,13 @@ void launch_quant_mx(const void *x, int64_t M, int64_t K, int64_t ldx, void *q, 
                      int num_sms, cudaStream_t st) {
   launch_pdl(quant_mx_kernel, persistent_grid(quant_mx_kernel, M * (K / 32), kThreads / 2, num_sms), kThreads,
              0, st, static_cast<const uint8_t *>(x), M, static_cast<int>(K), ldx * 2,
+             static_cast<uint8_t *>(q), s);
+}
+
+void launch_quant_token(const void *x, int64_t M, int64_t K, int64_t ldx, void *q, float *s,
+                        int num_sms, cudaStream_t st) {
+  launch_pdl(quant_token_kernel, persistent_grid(quant_token_kernel, M, 1, num_sms), kThreads, 0, st,
+             static_cast<const uint8_t *>(x), M, static_cast<int>(K), ldx * 2,
              static_cast<uint8_t *>(q), s);
 }
 

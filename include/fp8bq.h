@@ -88,7 +88,9 @@ enum {
   FP8BQ_OP_MX_GEMM = 2,
   FP8BQ_OP_MX_LINEAR = 3,
   FP8BQ_OP_STATIC_GEMM = 4,
-  FP8BQ_OP_STATIC_LINEAR = 5
+  FP8BQ_OP_STATIC_LINEAR = 5,
+  FP8BQ_OP_CHANNEL_GEMM = 6,
+  FP8BQ_OP_CHANNEL_LINEAR = 7
 };
 
 /* ---------------------------------------------------------------- utility */
@@ -252,6 +254,34 @@ FP8BQ_API int fp8bq_static_linear(const void *x, int64_t ldx, const float *s_x,
                                   const void *bias, void *y, int64_t M,
                                   int64_t N, int64_t K, void *ws,
                                   size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------ channelwise path (W8A8) */
+
+/* Per-token dynamic quantisation: one FP32 scale per row,
+ * s[i] = max(max_k |x[i,k]|, 1e-10) / 448 and q = RNE_sat(x / s[i]) (binary32
+ * divisions) -- the group rule with the group spanning the row ("SGLang
+ * 源码完全拆解(十九)", §激活量化, sglang_per_token_quant_fp8).  Applied to a
+ * BF16 weight [N, K] it gives the per-channel weight scales (§per-channel 权重:
+ * per_token_group_quant_fp8 with group_size = K).  x: BF16 [M, K] pitch ldx;
+ * q: E4M3 [M, K]; s: FP32 [M].  K % 16 == 0. */
+FP8BQ_API int fp8bq_channel_quant_act(const void *x, int64_t M, int64_t K,
+                                      int64_t ldx, void *q, float *s,
+                                      void *stream);
+
+/* Channelwise GEMM: y[i, j] = BF16((sum_k q[i,k] w[j,k]) * s_x[i] * s_w[j] + bias[j])
+ * (§一条 GEMM 的三种缩放组合, the per-token x per-channel outer product of the
+ * scales, applied after the FP32 full-K sum).  s_x: FP32 [M]; s_w: FP32 [N]. */
+FP8BQ_API int fp8bq_channel_gemm(const void *q, const float *s_x, const void *w,
+                                 const float *s_w, const void *bias, void *y,
+                                 int64_t M, int64_t N, int64_t K, void *ws,
+                                 size_t ws_bytes, void *stream);
+
+/* Fused channelwise linear: fp8bq_channel_quant_act into the workspace, then
+ * fp8bq_channel_gemm. */
+FP8BQ_API int fp8bq_channel_linear(const void *x, int64_t ldx, const void *w,
+                                   const float *s_w, const void *bias, void *y,
+                                   int64_t M, int64_t N, int64_t K, void *ws,
+                                   size_t ws_bytes, void *stream);
 
 /* ------------------------------------------------ weight / calibration set-up */
 
