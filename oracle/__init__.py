@@ -78,6 +78,8 @@ _SIGS = {
     "orc_gemm_channel": (None, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P, ctypes.c_int]),
     "orc_gemm_channel_sampled": (None, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _I64,
                                         _P, ctypes.c_int]),
+    "orc_quant_ue8m0": (None, [_P, _I64, _I64, _I64, _I64, _P, _P]),
+    "orc_requant_weight_ue8m0": (None, [_P, _P, _I64, _I64, _I64, _I64, _P, _P]),
     "orc_e4m3_dot_int": (ctypes.c_int64, [_P, _P, _I64]),
     "orc_e4m3_dot_f64": (ctypes.c_double, [_P, _P, _I64]),
 }
@@ -392,3 +394,47 @@ def gemm_channel_sampled(qa, sa, qw, sw, rows, cols, bias=None,
     lib().orc_gemm_channel_sampled(_p(qa), _p(sa), _p(qw), _p(sw), _p(b), M, N, K, _p(rows),
                                    _p(cols), rows.size, _p(y), threads or default_threads())
     return y
+
+
+# --------------------------------------------------------------------------
+# block FP8 with UE8M0 (power-of-two) scales
+# --------------------------------------------------------------------------
+
+def quant_ue8m0(x, group: int = 128):
+    """Group quantisation with power-of-two scales -> (q [M,K], u [M,ceil(K/group)])."""
+    x = _c(x, np.uint16)
+    M, K = x.shape
+    G = -(-K // group)
+    q = np.empty((M, K), np.uint8)
+    u = np.empty((M, G), np.uint8)
+    lib().orc_quant_ue8m0(_p(x), M, K, K, group, _p(q), _p(u))
+    return q, u
+
+
+def requant_weight_ue8m0(q, s, bn: int = 128, bk: int = 128):
+    """FP32 block scales -> UE8M0 rounded up, codes re-encoded -> (q2 [N,K], u [NB,KB])."""
+    q = _c(q, np.uint8)
+    s = _c(s, np.float32)
+    N, K = q.shape
+    q2 = np.empty((N, K), np.uint8)
+    u = np.empty(s.shape, np.uint8)
+    lib().orc_requant_weight_ue8m0(_p(q), _p(s), N, K, bn, bk, _p(q2), _p(u))
+    return q2, u
+
+
+def ue8m0_to_f32(u) -> np.ndarray:
+    """UE8M0 codes 1..254 as the binary32 powers of two they stand for."""
+    u = np.asarray(u, np.uint8)
+    return ue8m0_decode(u).astype(np.float32)
+
+
+def gemm_block_ue8m0(qa, ua, qw, uw, bias=None, threads: int | None = None) -> np.ndarray:
+    """Block-scaled GEMM whose 128-block scales are powers of two (the block
+    definition with s = 2^(u - 127)), binary64."""
+    return gemm_block(qa, ue8m0_to_f32(ua), qw, ue8m0_to_f32(uw), bias=bias, threads=threads)
+
+
+def gemm_block_ue8m0_sampled(qa, ua, qw, uw, rows, cols, bias=None,
+                             threads: int | None = None) -> np.ndarray:
+    return gemm_block_sampled(qa, ue8m0_to_f32(ua), qw, ue8m0_to_f32(uw), rows, cols,
+                              bias=bias, threads=threads)

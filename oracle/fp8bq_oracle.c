@@ -589,3 +589,65 @@ void orc_gemm_channel_sampled(const uint8_t *qa, const float *sa,
   g.rows = rows; g.cols = cols; g.n = n;
   run_gemm(g, nthreads);
 }
+
+/* ======================================================================= */
+/* Block FP8 with UE8M0 (power-of-two) scales                               */
+/* ======================================================================= */
+
+/* Smallest e with 2^e >= r, for a positive finite binary64 r. */
+static int ceil_pow2_exponent(double r) {
+  int ex;
+  double f = frexp(r, &ex); /* r = f * 2^ex, f in [0.5, 1) */
+  return f == 0.5 ? ex - 1 : ex;
+}
+
+/* Per-token group quantisation with the scale restricted to a power of two
+ * ([SGL-19] §分块 GEMM 的后端分派: with act_scale_ue8m0 the activation
+ * quantiser keeps the per-token-group layout but limits each scale to 2^e).
+ * Reading: e is the smallest exponent keeping every value of the group within
+ * +-448, e = ceil(log2(max(amax, 1e-10) / 448)) with the binary32 division;
+ * u = e + 127; q = RNE_sat(x * 2^-e), an exact power-of-two scaling.  The last
+ * group may be partial.  u is [M][ceil(K/group)]. */
+void orc_quant_ue8m0(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
+                     int64_t group, uint8_t *q, uint8_t *u) {
+  int64_t G = (K + group - 1) / group;
+  for (int64_t i = 0; i < M; ++i) {
+    for (int64_t g = 0; g < G; ++g) {
+      int64_t k0 = g * group, k1 = k0 + group < K ? k0 + group : K;
+      float amax = 0.0f;
+      for (int64_t k = k0; k < k1; ++k) {
+        float a = fabsf(orc_bf16_to_f32(x[i * ldx + k]));
+        if (a > amax) amax = a;
+      }
+      volatile float floored = amax < 1e-10f ? 1e-10f : amax;
+      volatile float r = floored / 448.0f;
+      int e = ceil_pow2_exponent((double)r);
+      u[i * G + g] = (uint8_t)(e + 127);
+      for (int64_t k = k0; k < k1; ++k)
+        q[i * K + k] = orc_e4m3_encode(ldexp((double)orc_bf16_to_f32(x[i * ldx + k]), -e));
+    }
+  }
+}
+
+/* FP32 block scales of a quantised weight re-expressed as UE8M0 ([SGL-19]
+ * §分块路径的 process_weights_after_loading_block_quant: for the SM100 runner
+ * the FP32 block scale is requantised to a power-of-two scale, since only
+ * powers of two convert exactly in the kernel).  Reading: per bn x bk block,
+ * s' = 2^e with e = ceil(log2 s) (the nearest power of two at or above s, so
+ * no value grows), u = e + 127, and every code re-encoded from its value:
+ * q' = RNE_sat(dec(q) * s / s'), exact in binary64.  s is [ceil(N/bn)][ceil(K/bk)],
+ * u the same shape. */
+void orc_requant_weight_ue8m0(const uint8_t *q, const float *s, int64_t N, int64_t K,
+                              int64_t bn, int64_t bk, uint8_t *q2, uint8_t *u) {
+  int64_t NB = (N + bn - 1) / bn, KB = (K + bk - 1) / bk;
+  for (int64_t nb = 0; nb < NB; ++nb)
+    for (int64_t kb = 0; kb < KB; ++kb) {
+      double sv = (double)s[nb * KB + kb];
+      int e = ceil_pow2_exponent(sv);
+      u[nb * KB + kb] = (uint8_t)(e + 127);
+      double m = ldexp(sv, -e); /* s / s', in (1/2, 1] */
+      for (int64_t n = nb * bn; n < N && n < (nb + 1) * bn; ++n)
+        for (int64_t k = kb * bk; k < K && k < (kb + 1) * bk; ++k)
+          q2[n * K + k] = orc_e4m3_encode(orc_e4m3_decode(q[n * K + k]) * m);
+    }
+}

@@ -62,6 +62,14 @@ void orc_gemm_channel_sampled(const uint8_t *qa, const float *sa,
                               const int64_t *cols, int64_t n, double *y,
                               int nthreads);
 
+/* ---- block FP8 with UE8M0 scales ---------------------------------------- */
+/* Group quantisation with power-of-two scales: u[M][ceil(K/group)].          */
+void orc_quant_ue8m0(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
+                     int64_t group, uint8_t *q, uint8_t *u);
+/* FP32 block scales -> UE8M0 (rounded up), codes re-encoded per block.       */
+void orc_requant_weight_ue8m0(const uint8_t *q, const float *s, int64_t N, int64_t K,
+                              int64_t bn, int64_t bk, uint8_t *q2, uint8_t *u);
+
 /* ---- residual add + RMSNorm (the step before the activation quantiser) -- */
 /* binary64 -> BF16 (RNE, overflow to infinity).                             */
 uint16_t orc_bf16_from_f64(double v);
