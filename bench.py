@@ -16,7 +16,7 @@ Also reported, measured in the same run:
                inside the timed region;
   extra        decode (M in {1,8,32,64}), quantiser and fused residual-add +
                RMSNorm + quantisation GB/s against HBM, MXFP8, static
-               per-tensor and channelwise TFLOPS;
+               per-tensor, channelwise and block-with-UE8M0 TFLOPS;
   cpu_baseline the CPU oracle on a bounded sample of the same workload.
 
 L2 is flushed (256 MiB write) between timed steps; every step is timed with
@@ -568,6 +568,39 @@ def run_extra(fb, torch, dev, stream, hbm_peak, fp8_peak):
                                           "frac_hbm": round(bb / (t * 1e-3) / 1e9 / hbm_peak, 4)}
     out["channel_w8a8"] = ch
     del qw, sw, qws, sws
+
+    # block FP8 with UE8M0 scales on the block-scaled MMA, at the prefill shapes
+    ue = {}
+    M, K = si.PREFILL["M"], si.PREFILL["K"]
+    KB = K // 128
+    b = M * K * 3 + M * KB
+    ns = n_sets(b)
+    xs = _copies(to_dev(si.activations(M, K)), ns)
+    qs = [torch.empty(M, K, dtype=torch.uint8, device=dev) for _ in range(ns)]
+    us = [torch.empty(M, KB, dtype=torch.uint8, device=dev) for _ in range(ns)]
+    t = _time_graph(torch, [lambda i=i: fb.fp8bq_quant_act_ue8m0(xs[i], qs[i], us[i])
+                            for i in range(ns)], 2 * ns)
+    ue["quant_4096x6144"] = {"us": round(t * 1e3, 2), "gbs": round(b / (t * 1e-3) / 1e9, 1),
+                             "frac_hbm": round(b / (t * 1e-3) / 1e9 / hbm_peak, 4)}
+    qa, ua = qs[0], us[0]
+    del xs
+    for N in si.PREFILL["N_list"]:
+        wb = to_dev(si.weights(N, K))
+        qw = torch.empty(N, K, dtype=torch.uint8, device=dev)
+        sw = torch.empty(N // 128, KB, dtype=torch.float32, device=dev)
+        fb.fp8bq_quant_weight_block(wb, qw, sw)
+        uw = torch.empty(N // 128, KB, dtype=torch.uint8, device=dev)
+        fb.fp8bq_requant_weight_ue8m0(qw, sw, qw, uw)
+        del wb
+        y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        ws = fb.new_workspace(fb.OP_UE8M0_GEMM, M, N, K, device=dev)
+        t = _time_back_to_back(torch, stream, [lambda: fb.fp8bq_ue8m0_gemm(qa, ua, qw, uw, y, ws)], 20)
+        tf = 2.0 * M * N * K / (t * 1e-3) / 1e12
+        ue[f"gemm_{M}x{N}x{K}"] = {"us": round(t * 1e3, 2), "tflops": round(tf, 1),
+                                   "frac_fp8": round(tf / fp8_peak, 4)}
+        del qw, sw, uw, y
+    out["block_ue8m0"] = ue
+    del qs, us
 
     # residual add + RMSNorm + quantisation (the step before the linear):
     # x, residual in; updated residual, E4M3 codes (and group scales) out

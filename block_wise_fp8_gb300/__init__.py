@@ -25,6 +25,8 @@ __all__ = [
     "Fp8bqError", "SCALE_ROW_MAJOR", "SCALE_COL_MAJOR", "OP_GEMM", "OP_LINEAR",
     "OP_MX_GEMM", "OP_MX_LINEAR", "OP_STATIC_GEMM", "OP_STATIC_LINEAR", "OP_CHANNEL_GEMM",
     "OP_CHANNEL_LINEAR", "fp8bq_channel_quant_act", "fp8bq_channel_gemm", "fp8bq_channel_linear",
+    "OP_UE8M0_GEMM", "OP_UE8M0_LINEAR", "fp8bq_quant_act_ue8m0", "fp8bq_requant_weight_ue8m0",
+    "fp8bq_ue8m0_gemm", "fp8bq_ue8m0_linear",
     "library_path",
     "fp8bq_version", "fp8bq_status_string", "fp8bq_last_cuda_error",
     "fp8bq_workspace_bytes", "fp8bq_workspace_init", "fp8bq_poll_status",
@@ -38,7 +40,8 @@ __all__ = [
 
 SCALE_ROW_MAJOR, SCALE_COL_MAJOR = 0, 1
 (OP_GEMM, OP_LINEAR, OP_MX_GEMM, OP_MX_LINEAR, OP_STATIC_GEMM,
- OP_STATIC_LINEAR, OP_CHANNEL_GEMM, OP_CHANNEL_LINEAR) = range(8)
+ OP_STATIC_LINEAR, OP_CHANNEL_GEMM, OP_CHANNEL_LINEAR, OP_UE8M0_GEMM,
+ OP_UE8M0_LINEAR) = range(10)
 NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024      # FP8BQ_NOALLOC_SCRATCH_BYTES
 
 STATUS_NAMES = {0: "FP8BQ_OK", 1: "FP8BQ_ERR_NULL", 2: "FP8BQ_ERR_SHAPE",
@@ -84,6 +87,10 @@ def _load():
         "fp8bq_mx_linear": (I32, [P, I64, P, P, P, P, I64, I64, I64, P, SZ, P]),
         "fp8bq_static_quant_act": (I32, [P, I64, I64, I64, P, P, P]),
         "fp8bq_channel_quant_act": (I32, [P, I64, I64, I64, P, P, P]),
+        "fp8bq_quant_act_ue8m0": (I32, [P, I64, I64, I64, P, P, P]),
+        "fp8bq_requant_weight_ue8m0": (I32, [P, P, I64, I64, P, P, P]),
+        "fp8bq_ue8m0_gemm": (I32, [P, P, P, P, P, P, I64, I64, I64, P, SZ, P]),
+        "fp8bq_ue8m0_linear": (I32, [P, I64, P, P, P, P, I64, I64, I64, P, SZ, P]),
         "fp8bq_channel_gemm": (I32, [P, P, P, P, P, P, I64, I64, I64, P, SZ, P]),
         "fp8bq_channel_linear": (I32, [P, I64, P, P, P, P, I64, I64, I64, P, SZ, P]),
         "fp8bq_add_rmsnorm_quant_act": (I32, [P, I64, P, I64, P, P, F32, I64, I64, P, P, P,
@@ -268,6 +275,36 @@ def fp8bq_channel_linear(x, w, s_w, y, ws, bias=None, stream=None):
     _check(_lib.fp8bq_channel_linear(_ptr(x), _ld(x), _ptr(w), _ptr(s_w), _ptr(bias), _ptr(y),
                                      M, N, K, _ptr(ws), _nbytes(ws), _stream(stream)),
            "fp8bq_channel_linear")
+
+
+def fp8bq_quant_act_ue8m0(x, q, u, stream=None):
+    """Group-128 quantisation with power-of-two (UE8M0) scales."""
+    M, K = x.shape
+    _check(_lib.fp8bq_quant_act_ue8m0(_ptr(x), M, K, _ld(x), _ptr(q), _ptr(u), _stream(stream)),
+           "fp8bq_quant_act_ue8m0")
+
+
+def fp8bq_requant_weight_ue8m0(q, s_w, q_out, u_w, stream=None):
+    """FP32 128x128 block scales -> UE8M0 (rounded up), codes re-encoded."""
+    N, K = q.shape
+    _check(_lib.fp8bq_requant_weight_ue8m0(_ptr(q), _ptr(s_w), N, K, _ptr(q_out), _ptr(u_w),
+                                           _stream(stream)), "fp8bq_requant_weight_ue8m0")
+
+
+def fp8bq_ue8m0_gemm(q, u_x, w, u_w, y, ws, bias=None, stream=None):
+    M, K = q.shape
+    N = w.shape[0]
+    _check(_lib.fp8bq_ue8m0_gemm(_ptr(q), _ptr(u_x), _ptr(w), _ptr(u_w), _ptr(bias), _ptr(y),
+                                 M, N, K, _ptr(ws), _nbytes(ws), _stream(stream)),
+           "fp8bq_ue8m0_gemm")
+
+
+def fp8bq_ue8m0_linear(x, w, u_w, y, ws, bias=None, stream=None):
+    M, K = x.shape
+    N = w.shape[0]
+    _check(_lib.fp8bq_ue8m0_linear(_ptr(x), _ld(x), _ptr(w), _ptr(u_w), _ptr(bias), _ptr(y),
+                                   M, N, K, _ptr(ws), _nbytes(ws), _stream(stream)),
+           "fp8bq_ue8m0_linear")
 
 
 def fp8bq_add_rmsnorm_quant_act(x, gamma, eps: float, residual=None, residual_out=None,

@@ -47,6 +47,12 @@ void launch_quant_mx(const void *x, int64_t M, int64_t K, int64_t ldx, void *q, 
                      int num_sms, cudaStream_t st);
 void launch_quant_static(const void *x, int64_t M, int64_t K, int64_t ldx, const float *s,
                          void *q, int num_sms, cudaStream_t st);
+// Group-128 quantisation with power-of-two (UE8M0) scales, u[M][ceil(K/128)].
+void launch_quant_group_ue8m0(const void *x, int64_t M, int64_t K, int64_t ldx, void *q,
+                              uint8_t *u, int num_sms, cudaStream_t st);
+// FP32 128x128 weight block scales -> UE8M0 (rounded up), codes re-encoded.
+void launch_requant_ue8m0(const void *q, const float *s, int64_t N, int64_t K, void *q2, uint8_t *u,
+                          cudaStream_t st);
 // One scale per row: s[i] = max(amax_i, 1e-10) / 448, q = RNE_sat(x / s[i]).
 void launch_quant_token(const void *x, int64_t M, int64_t K, int64_t ldx, void *q, float *s,
                         int num_sms, cudaStream_t st);
@@ -123,6 +129,11 @@ inline int64_t mx_sfb_bytes(int64_t N, int64_t K) {
 // Rearranges s_x [M, K/32] and s_w [N, K/32] (row-major UE8M0) into chunks.
 void launch_mx_sf_tiles(const uint8_t *ux, int64_t M, const uint8_t *uw, int64_t N, int64_t K,
                         uint8_t *sfa, uint8_t *sfb, int num_sms, cudaStream_t st);
+// The same chunks from 128-wide block codes: s_x [M][ceil(K/128)] and s_w
+// [ceil(N/128)][ceil(K/128)], each code standing for four 32-groups (and for
+// the 128 weight rows of its block).
+void launch_ue8m0_sf_tiles(const uint8_t *ux, int64_t M, const uint8_t *uw, int64_t N, int64_t K,
+                           uint8_t *sfa, uint8_t *sfb, int num_sms, cudaStream_t st);
 WorkspaceLayout workspace_layout(int op, int64_t M, int64_t N, int64_t K);
 
 // Work decomposition of one GEMM launch.

@@ -160,14 +160,17 @@ int gemm_block_impl(const void *q, const float *s_x, int s_layout, const void *w
   return finish_launch(r, e);
 }
 
+// MXFP8 GEMM; `block128`: the scale codes are one per 128-wide K block (and per
+// 128 weight rows), the block-FP8-with-UE8M0 view of the same kernel.
 int gemm_mx_impl(const void *q, const uint8_t *s_x, const void *w, const uint8_t *s_w,
                  const void *bias, void *y, int64_t M, int64_t N, int64_t K, void *ws, int op,
-                 cudaStream_t st, const DeviceInfo &dev) {
+                 cudaStream_t st, const DeviceInfo &dev, bool block128 = false) {
   GemmArgs a = base_args(kModeMx, M, N, K, bias, y, ws, op);
   const WorkspaceLayout L = workspace_layout(op, M, N, K);
   uint8_t *sfa = static_cast<uint8_t *>(ws) + L.sfa;
   uint8_t *sfb = static_cast<uint8_t *>(ws) + L.sfb;
-  launch_mx_sf_tiles(s_x, M, s_w, N, K, sfa, sfb, dev.num_sms, st);
+  if (block128) launch_ue8m0_sf_tiles(s_x, M, s_w, N, K, sfa, sfb, dev.num_sms, st);
+  else launch_mx_sf_tiles(s_x, M, s_w, N, K, sfa, sfb, dev.num_sms, st);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);
   a.ux = sfa;  // the GEMM reads the chunks
@@ -277,7 +280,7 @@ const char *fp8bq_status_string(int s) {
 int fp8bq_last_cuda_error(void) { return g_last_cuda_error; }
 
 size_t fp8bq_workspace_bytes(int op, int64_t M, int64_t N, int64_t K) {
-  if (op < FP8BQ_OP_GEMM || op > FP8BQ_OP_CHANNEL_LINEAR || M < 0 || N < 1 || K < 1) return 256;
+  if (op < FP8BQ_OP_GEMM || op > FP8BQ_OP_UE8M0_LINEAR || M < 0 || N < 1 || K < 1) return 256;
   return workspace_layout(op, M, N, K).total;
 }
 
@@ -658,6 +661,69 @@ int fp8bq_channel_linear(const void *x, int64_t ldx, const void *w, const float 
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);
   return gemm_channel_impl(q, s, w, s_w, bias, y, M, N, K, ws, FP8BQ_OP_CHANNEL_LINEAR, st, dev);
+}
+
+// ------------------------------------------------------------------ block FP8 with UE8M0 scales
+
+int fp8bq_quant_act_ue8m0(const void *x, int64_t M, int64_t K, int64_t ldx, void *q, uint8_t *u,
+                          void *stream) {
+  if (M == 0) return empty_batch(K, 1);
+  if (!q || !u) return FP8BQ_ERR_NULL;
+  RETURN_IF(check_act(x, M, K, ldx, 16));
+  if (!aligned(q, 16)) return FP8BQ_ERR_ALIGN;
+  DeviceInfo dev;
+  RETURN_IF(device_info(&dev));
+  launch_quant_group_ue8m0(x, M, K, ldx, q, u, dev.num_sms, static_cast<cudaStream_t>(stream));
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? FP8BQ_OK : cuda_fail(e);
+}
+
+int fp8bq_requant_weight_ue8m0(const void *q, const float *s_w, int64_t N, int64_t K, void *q_out,
+                               uint8_t *u_w, void *stream) {
+  if (!q || !s_w || !q_out || !u_w) return FP8BQ_ERR_NULL;
+  if (N < 1 || K < 1 || N > (int64_t(1) << 31) - 1 || K > (int64_t(1) << 30)) return FP8BQ_ERR_SHAPE;
+  if (!aligned(s_w, 4)) return FP8BQ_ERR_ALIGN;
+  DeviceInfo dev;
+  RETURN_IF(device_info(&dev));
+  launch_requant_ue8m0(q, s_w, N, K, q_out, u_w, static_cast<cudaStream_t>(stream));
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? FP8BQ_OK : cuda_fail(e);
+}
+
+int fp8bq_ue8m0_gemm(const void *q, const uint8_t *u_x, const void *w, const uint8_t *u_w,
+                     const void *bias, void *y, int64_t M, int64_t N, int64_t K, void *ws,
+                     size_t ws_bytes, void *stream) {
+  if (M == 0) return empty_batch(K, N);
+  if (!q || !u_x || !w || !u_w || !y) return FP8BQ_ERR_NULL;
+  RETURN_IF(check_gemm_shape(M, N, K, 32));
+  if (!aligned(q, 16) || !aligned(w, 16) || !aligned(y, 16) || !aligned(bias, 2))
+    return FP8BQ_ERR_ALIGN;
+  RETURN_IF(check_ws(ws, ws_bytes, FP8BQ_OP_UE8M0_GEMM, M, N, K));
+  DeviceInfo dev;
+  RETURN_IF(device_info(&dev));
+  return gemm_mx_impl(q, u_x, w, u_w, bias, y, M, N, K, ws, FP8BQ_OP_UE8M0_GEMM,
+                      static_cast<cudaStream_t>(stream), dev, true);
+}
+
+int fp8bq_ue8m0_linear(const void *x, int64_t ldx, const void *w, const uint8_t *u_w,
+                       const void *bias, void *y, int64_t M, int64_t N, int64_t K, void *ws,
+                       size_t ws_bytes, void *stream) {
+  if (M == 0) return empty_batch(K, N);
+  if (!w || !u_w || !y) return FP8BQ_ERR_NULL;
+  RETURN_IF(check_act(x, M, K, ldx, 32));
+  RETURN_IF(check_gemm_shape(M, N, K, 32));
+  if (!aligned(w, 16) || !aligned(y, 16) || !aligned(bias, 2)) return FP8BQ_ERR_ALIGN;
+  RETURN_IF(check_ws(ws, ws_bytes, FP8BQ_OP_UE8M0_LINEAR, M, N, K));
+  DeviceInfo dev;
+  RETURN_IF(device_info(&dev));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const WorkspaceLayout L = workspace_layout(FP8BQ_OP_UE8M0_LINEAR, M, N, K);
+  uint8_t *q = static_cast<uint8_t *>(ws) + L.q;
+  uint8_t *u = static_cast<uint8_t *>(ws) + L.s;
+  launch_quant_group_ue8m0(x, M, K, ldx, q, u, dev.num_sms, st);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e);
+  return gemm_mx_impl(q, u, w, u_w, bias, y, M, N, K, ws, FP8BQ_OP_UE8M0_LINEAR, st, dev, true);
 }
 
 }  // extern "C"

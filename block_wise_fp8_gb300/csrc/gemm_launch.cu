@@ -176,15 +176,16 @@ WorkspaceLayout workspace_layout(int op, int64_t M, int64_t N, int64_t K) {
   L.counters = 256;
   size_t off = L.counters + up(static_cast<size_t>(NT) * 4);
   L.partials = off;
-  const bool mx = (op == 2 || op == 3);
+  const bool mx = (op == 2 || op == 3 || op == 8 || op == 9);  // MX GEMM (UE8M0 views too)
   if (M <= 64 && !mx) off += up(static_cast<size_t>(kMaxSplits) * M * N * 4);
   L.q = off;
-  const bool fused = (op == 1 || op == 3 || op == 5 || op == 7);
+  const bool fused = (op == 1 || op == 3 || op == 5 || op == 7 || op == 9);
   if (fused) off += up(static_cast<size_t>(M) * K);
   L.s = off;
   if (op == 1) off += up(static_cast<size_t>(M) * KB * 4);
   if (op == 3) off += up(static_cast<size_t>(M) * (K / 32));
   if (op == 7) off += up(static_cast<size_t>(M) * 4);  // one FP32 scale per token
+  if (op == 9) off += up(static_cast<size_t>(M) * KB);  // one UE8M0 code per 128-group
   L.sfa = off;
   if (mx) off += up(static_cast<size_t>(mx_sfa_bytes(M, K)));
   L.sfb = off;

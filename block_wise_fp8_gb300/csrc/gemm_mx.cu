@@ -26,6 +26,7 @@ struct SfJob {
   int tile_rows;     // rows per tile
   int blocks;        // 512-byte blocks per chunk (32 x 4 codes each)
   int64_t n;         // 16-byte chunk rows to write: tiles * KB * blocks * 32
+  int rdiv;          // rows sharing one code row (128 for 128 x 128 weight blocks)
 };
 
 // Four codes (K groups 4kb..4kb+3) of one row, little-endian; 0 past the row's end
@@ -42,8 +43,10 @@ __device__ __forceinline__ uint32_t sf_codes(const uint8_t *u, int64_t row, int 
 // One thread per 16-byte chunk row: chunk (t, kb), block h, row i holds the codes
 // of tile rows i + 32(4h + c), c = 0..3 (code 0 = 2^-127 outside the tile or the
 // matrix, where the operand's data are zero-filled).
+// g128: the codes are one per 128-wide K block (u[row / rdiv][kb], KB per row),
+// each standing for the four 32-groups of its block.
 __global__ void __launch_bounds__(256) mx_sf_tile_kernel(SfJob ja, SfJob jb, int G, int KB,
-                                                         int words) {
+                                                         int words, int g128) {
   griddep_launch_dependents();
   griddep_wait();
   const int64_t total = ja.n + jb.n;
@@ -63,7 +66,11 @@ __global__ void __launch_bounds__(256) mx_sf_tile_kernel(SfJob ja, SfJob jb, int
     for (int c = 0; c < 4; ++c) {
       const int local = i + 32 * (4 * h + c);
       const int64_t row = t * j.tile_rows + local;
-      v[c] = (local < j.tile_rows && row < j.rows) ? sf_codes(j.u, row, G, kb, words != 0) : 0u;
+      if (local < j.tile_rows && row < j.rows)
+        v[c] = g128 ? __ldg(j.u + (row / j.rdiv) * KB + kb) * 0x01010101u
+                    : sf_codes(j.u, row, G, kb, words != 0);
+      else
+        v[c] = 0u;
     }
     *reinterpret_cast<uint4 *>(j.out + ((t * KB + kb) * j.blocks + h) * 512 + 16 * i) =
         make_uint4(v[0], v[1], v[2], v[3]);
@@ -76,8 +83,8 @@ void launch_mx_sf_tiles(const uint8_t *ux, int64_t M, const uint8_t *uw, int64_t
                         uint8_t *sfa, uint8_t *sfb, int num_sms, cudaStream_t st) {
   const int G = static_cast<int>(K / 32);
   const int KB = static_cast<int>((K + 127) / 128);
-  SfJob ja{ux, sfa, M, 128, 1, (M + 127) / 128 * KB * 32};
-  SfJob jb{uw, sfb, N, kMxBN, kMxSfBBlocks, (N + kMxBN - 1) / kMxBN * KB * kMxSfBBlocks * 32};
+  SfJob ja{ux, sfa, M, 128, 1, (M + 127) / 128 * KB * 32, 1};
+  SfJob jb{uw, sfb, N, kMxBN, kMxSfBBlocks, (N + kMxBN - 1) / kMxBN * KB * kMxSfBBlocks * 32, 1};
   const bool words = (G % 4 == 0) && (reinterpret_cast<uintptr_t>(ux) & 3u) == 0 &&
                      (reinterpret_cast<uintptr_t>(uw) & 3u) == 0;
   const int64_t total = ja.n + jb.n;
@@ -85,7 +92,20 @@ void launch_mx_sf_tiles(const uint8_t *ux, int64_t M, const uint8_t *uw, int64_t
   if (grid > 4L * num_sms) grid = 4L * num_sms;
   if (grid < 1) grid = 1;
   launch_pdl(mx_sf_tile_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0, st, ja, jb, G,
-             KB, words ? 1 : 0);
+             KB, words ? 1 : 0, 0);
+}
+
+void launch_ue8m0_sf_tiles(const uint8_t *ux, int64_t M, const uint8_t *uw, int64_t N, int64_t K,
+                           uint8_t *sfa, uint8_t *sfb, int num_sms, cudaStream_t st) {
+  const int KB = static_cast<int>((K + 127) / 128);
+  SfJob ja{ux, sfa, M, 128, 1, (M + 127) / 128 * KB * 32, 1};
+  SfJob jb{uw, sfb, N, kMxBN, kMxSfBBlocks, (N + kMxBN - 1) / kMxBN * KB * kMxSfBBlocks * 32, 128};
+  const int64_t total = ja.n + jb.n;
+  int64_t grid = (total + 255) / 256;
+  if (grid > 4L * num_sms) grid = 4L * num_sms;
+  if (grid < 1) grid = 1;
+  launch_pdl(mx_sf_tile_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0, st, ja, jb, KB,
+             KB, 0, 1);
 }
 
 }  // namespace fp8bq

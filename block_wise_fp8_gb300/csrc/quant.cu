@@ -23,9 +23,14 @@ constexpr int kThreads = 256;
 // persistent: each warp takes 4 consecutive groups per step and walks the
 // groups with the grid's stride, loading its next chunk before converting the
 // current one, so two chunks per thread are in flight.
+// UE8M0: the scale is the power of two 2^e, e = ceil(log2(max(amax,1e-10)/448))
+// (the MXFP8 rule on a 128-channel group, "SGLang 源码完全拆解(十九)", §分块
+// GEMM 的后端分派, act_scale_ue8m0), stored as the code e + 127 in uint8 s[M][G].
+template <bool UE8M0>
 __global__ void __launch_bounds__(kThreads) quant_group128_kernel(
     const uint8_t *__restrict__ x, int64_t M, int K, int64_t ldx_bytes, int G,
-    uint8_t *__restrict__ q, float *__restrict__ s, int s_layout, int64_t lds) {
+    uint8_t *__restrict__ q, void *__restrict__ s_out, int s_layout, int64_t lds) {
+  float *s = static_cast<float *>(s_out);
   __shared__ ScaleTable table;
   griddep_launch_dependents();
   fill_scale_table(table);
@@ -70,12 +75,25 @@ __global__ void __launch_bounds__(kThreads) quant_group128_kernel(
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
     const float2 sc = scale_of(table, amax);
     const float sg = sc.x;
-    const uint4 out = quant16<1>(cur, f, sg, sc.y);
+    uint4 out;
+    uint32_t u = 0u;
+    if (UE8M0) {
+      const uint32_t rb = __float_as_uint(sg);                        // RN(max(amax,1e-10)/448)
+      u = (rb >> 23) + ((rb & 0x7FFFFFu) != 0u ? 1u : 0u);            // e + 127
+      const float inv = __uint_as_float((254u - u) << 23);            // 2^-e, exact
+      float t[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) t[i] = __fmul_rn(f[i], inv);
+      out = to_e4m3x16(t);
+    } else {
+      out = quant16<1>(cur, f, sg, sc.y);
+    }
     const int k = g * 128 + sub * 16;
     if (row < M) {
       if (k < K) *reinterpret_cast<uint4 *>(q + row * K + k) = out;
       if (sub == 0) {
-        if (s_layout == 0) s[row * lds + g] = sg;
+        if (UE8M0) static_cast<uint8_t *>(s_out)[row * G + g] = static_cast<uint8_t>(u);
+        else if (s_layout == 0) s[row * lds + g] = sg;
         else s[static_cast<int64_t>(g) * lds + row] = sg;
       }
     }
@@ -349,6 +367,35 @@ __global__ void absmax_finalize_kernel(float *s) {
   *s = __fdiv_rn(fmaxf(amax, kFloor), 448.0f);
 }
 
+// ---------------------------------------------------------------- FP32 -> UE8M0 weight requant
+// One CTA per 128 x 128 block (one-time weight preparation): the FP32 block
+// scale s becomes 2^e, e = ceil(log2 s) (the nearest power of two at or above
+// s, read from s's bits), and every code is re-encoded from its value,
+// q' = RNE_sat(dec(q) * s * 2^-e): the product of a 4-bit and a 24-bit
+// significand is exact in binary64, then rounded once to E4M3 ("SGLang 源码完全
+// 拆解(十九)", §分块路径的 process_weights_after_loading_block_quant).  q' may
+// be q itself (each code is read before it is written, by the same thread).
+__global__ void __launch_bounds__(kThreads) requant_ue8m0_kernel(const uint8_t *q, const float *__restrict__ s,
+                                                                 int N, int K, int KB, uint8_t *q2,
+                                                                 uint8_t *__restrict__ u) {
+  griddep_launch_dependents();
+  griddep_wait();
+  const int kb = blockIdx.x, nb = blockIdx.y;
+  const float sv = __ldg(s + static_cast<int64_t>(nb) * KB + kb);
+  const uint32_t sb = __float_as_uint(sv);  // a positive normal scale
+  const int e = static_cast<int>(sb >> 23) - 127 + ((sb & 0x7FFFFFu) != 0u ? 1 : 0);
+  const double m = static_cast<double>(sv) * ldexp(1.0, -e);  // s / 2^e, in (1/2, 1]
+  if (threadIdx.x == 0) u[static_cast<int64_t>(nb) * KB + kb] = static_cast<uint8_t>(e + 127);
+  const int rows = min(128, N - nb * 128), cols = min(128, K - kb * 128);
+  for (int idx = threadIdx.x; idx < rows * cols; idx += blockDim.x) {
+    const int r = idx / cols, c = idx - r * cols;
+    const int64_t off = static_cast<int64_t>(nb * 128 + r) * K + kb * 128 + c;
+    const __half_raw hr = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(q[off]), __NV_E4M3);
+    const double v = static_cast<double>(__half2float(__half(hr))) * m;
+    q2[off] = static_cast<uint8_t>(__nv_cvt_double_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
+  }
+}
+
 inline unsigned blocks_for(int64_t work, int per_block) {
   return static_cast<unsigned>((work + per_block - 1) / per_block);
 }
@@ -357,11 +404,12 @@ inline unsigned blocks_for(int64_t work, int per_block) {
 
 // Persistent grids: enough CTAs for the work, at most as many as fit on the
 // device at once (the kernel's occupancy, queried once per kernel).
-template <typename Kern>
-unsigned persistent_grid(Kern kern, int64_t work, int per_block, int num_sms) {
-  static int per_sm = [&] {
+template <auto KERN>
+unsigned persistent_grid(int64_t work, int per_block, int num_sms) {
+  // per kernel (the template argument is the kernel itself, not its type)
+  static int per_sm = [] {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, 0) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, KERN, kThreads, 0) != cudaSuccess ||
         n < 1)
       n = 1;
     return n;
@@ -375,28 +423,38 @@ void launch_quant_group(const void *x, int64_t M, int64_t K, int64_t ldx, void *
                         int s_layout, int num_sms, cudaStream_t st) {
   const int G = static_cast<int>((K + 127) / 128);
   const int64_t lds = s_layout == 0 ? G : ((M + 3) / 4) * 4;
-  launch_pdl(quant_group128_kernel, persistent_grid(quant_group128_kernel, M * G, kThreads / 8, num_sms), kThreads, 0,
+  launch_pdl(quant_group128_kernel<false>,
+             persistent_grid<quant_group128_kernel<false>>(M * G, kThreads / 8, num_sms), kThreads, 0,
              st, static_cast<const uint8_t *>(x), M, static_cast<int>(K), ldx * 2, G,
-             static_cast<uint8_t *>(q), s, s_layout, lds);
+             static_cast<uint8_t *>(q), static_cast<void *>(s), s_layout, lds);
+}
+
+void launch_quant_group_ue8m0(const void *x, int64_t M, int64_t K, int64_t ldx, void *q,
+                              uint8_t *u, int num_sms, cudaStream_t st) {
+  const int G = static_cast<int>((K + 127) / 128);
+  launch_pdl(quant_group128_kernel<true>,
+             persistent_grid<quant_group128_kernel<true>>(M * G, kThreads / 8, num_sms), kThreads, 0,
+             st, static_cast<const uint8_t *>(x), M, static_cast<int>(K), ldx * 2, G,
+             static_cast<uint8_t *>(q), static_cast<void *>(u), 0, static_cast<int64_t>(G));
 }
 
 void launch_quant_mx(const void *x, int64_t M, int64_t K, int64_t ldx, void *q, uint8_t *s,
                      int num_sms, cudaStream_t st) {
-  launch_pdl(quant_mx_kernel, persistent_grid(quant_mx_kernel, M * (K / 32), kThreads / 2, num_sms), kThreads,
+  launch_pdl(quant_mx_kernel, persistent_grid<quant_mx_kernel>(M * (K / 32), kThreads / 2, num_sms), kThreads,
              0, st, static_cast<const uint8_t *>(x), M, static_cast<int>(K), ldx * 2,
              static_cast<uint8_t *>(q), s);
 }
 
 void launch_quant_token(const void *x, int64_t M, int64_t K, int64_t ldx, void *q, float *s,
                         int num_sms, cudaStream_t st) {
-  launch_pdl(quant_token_kernel, persistent_grid(quant_token_kernel, M, 1, num_sms), kThreads, 0, st,
+  launch_pdl(quant_token_kernel, persistent_grid<quant_token_kernel>(M, 1, num_sms), kThreads, 0, st,
              static_cast<const uint8_t *>(x), M, static_cast<int>(K), ldx * 2,
              static_cast<uint8_t *>(q), s);
 }
 
 void launch_quant_static(const void *x, int64_t M, int64_t K, int64_t ldx, const float *s,
                          void *q, int num_sms, cudaStream_t st) {
-  launch_pdl(quant_static_kernel, persistent_grid(quant_static_kernel, M * (K / 16), kThreads, num_sms), kThreads, 0,
+  launch_pdl(quant_static_kernel, persistent_grid<quant_static_kernel>(M * (K / 16), kThreads, num_sms), kThreads, 0,
              st, static_cast<const uint8_t *>(x), M, static_cast<int>(K), ldx * 2, s,
              static_cast<uint8_t *>(q));
 }
@@ -408,6 +466,14 @@ void launch_quant_weight_block(const void *w, int64_t N, int64_t K, int64_t ldw,
   launch_pdl(quant_weight_block_kernel, dim3(KB, NB), kThreads, 0, st,
              static_cast<const uint8_t *>(w), static_cast<int>(N), static_cast<int>(K), ldw * 2,
              static_cast<uint8_t *>(q), s, KB);
+}
+
+void launch_requant_ue8m0(const void *q, const float *s, int64_t N, int64_t K, void *q2, uint8_t *u,
+                          cudaStream_t st) {
+  const int KB = static_cast<int>((K + 127) / 128);
+  const int NB = static_cast<int>((N + 127) / 128);
+  launch_pdl(requant_ue8m0_kernel, dim3(KB, NB), kThreads, 0, st, static_cast<const uint8_t *>(q), s,
+             static_cast<int>(N), static_cast<int>(K), KB, static_cast<uint8_t *>(q2), u);
 }
 
 void launch_absmax_scale(const void *x, int64_t rows, int64_t K, int64_t ldx, float *s,

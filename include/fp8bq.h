@@ -14,9 +14,13 @@
  *      the block-wise equation; §Triton 分块内核在做什么);
  *   3. the two fused: BF16 in, BF16 out (same page, §一次前向的完整时序);
  *   plus an MXFP8 variant ([1,32] blocks, UE8M0 scales; same page §checkpoint
- *   里的量化元数据 and "[SGLang] FP8" §4) and a static per-tensor variant
+ *   里的量化元数据 and "[SGLang] FP8" §4), a static per-tensor variant
  *   (one activation scale, one weight scale per output partition; "SGLang 源码完全
- *   拆解(十九)", §激活量化的三种选择 and "[SGLang] FP8" §5).
+ *   拆解(十九)", §激活量化的三种选择 and "[SGLang] FP8" §5), a channelwise
+ *   variant (per-token x per-channel scales; §一条 GEMM 的三种缩放组合), block
+ *   FP8 with power-of-two (UE8M0) scales run on the block-scaled MMA
+ *   (§分块 GEMM 的后端分派), and the residual add + RMSNorm that precedes the
+ *   activation quantiser, fused with it ("GLM-5.3 推理全链路(十七)", §第1站).
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -90,7 +94,9 @@ enum {
   FP8BQ_OP_STATIC_GEMM = 4,
   FP8BQ_OP_STATIC_LINEAR = 5,
   FP8BQ_OP_CHANNEL_GEMM = 6,
-  FP8BQ_OP_CHANNEL_LINEAR = 7
+  FP8BQ_OP_CHANNEL_LINEAR = 7,
+  FP8BQ_OP_UE8M0_GEMM = 8,
+  FP8BQ_OP_UE8M0_LINEAR = 9
 };
 
 /* ---------------------------------------------------------------- utility */
@@ -282,6 +288,43 @@ FP8BQ_API int fp8bq_channel_linear(const void *x, int64_t ldx, const void *w,
                                    const float *s_w, const void *bias, void *y,
                                    int64_t M, int64_t N, int64_t K, void *ws,
                                    size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------ block FP8 with UE8M0 scales */
+
+/* Group-128 activation quantisation with power-of-two scales ("SGLang 源码完全
+ * 拆解(十九)", §分块 GEMM 的后端分派: act_scale_ue8m0 keeps the per-token-group
+ * layout and limits each scale to 2^e): e = ceil(log2(max(amax, 1e-10) / 448))
+ * with the binary32 division, u = e + 127, q = RNE_sat(x * 2^-e).
+ * u: uint8 [M][ceil(K/128)]. */
+FP8BQ_API int fp8bq_quant_act_ue8m0(const void *x, int64_t M, int64_t K,
+                                    int64_t ldx, void *q, uint8_t *u,
+                                    void *stream);
+
+/* One-time weight preparation (§分块路径的 process_weights_after_loading_block_quant:
+ * FP32 block scales requantised to power-of-two UE8M0 for the block-scaled
+ * MMA): per 128 x 128 block, s' = 2^ceil(log2 s) (s > 0 finite), u_w = the code
+ * of s', and every code re-encoded, q' = RNE_sat(dec(q) * s / s') (exact in
+ * binary64, one rounding).  q: E4M3 [N, K]; s_w: FP32 [ceil(N/128)][ceil(K/128)];
+ * q_out: E4M3 [N, K] (may be q); u_w: uint8, the shape of s_w. */
+FP8BQ_API int fp8bq_requant_weight_ue8m0(const void *q, const float *s_w,
+                                         int64_t N, int64_t K, void *q_out,
+                                         uint8_t *u_w, void *stream);
+
+/* Block FP8 GEMM with UE8M0 128 x 128 block scales, run as an MXFP8 view on the
+ * block-scaled MMA (each code standing for four 32-groups): y = BF16(sum_b P_b *
+ * 2^(u_x[i][b]-127) * 2^(u_w[j/128][b]-127) + bias), FP32 accumulation over the
+ * whole K inside the MMA.  u_x: uint8 [M][ceil(K/128)]; u_w: uint8
+ * [ceil(N/128)][ceil(K/128)].  K % 32 == 0. */
+FP8BQ_API int fp8bq_ue8m0_gemm(const void *q, const uint8_t *u_x, const void *w,
+                               const uint8_t *u_w, const void *bias, void *y,
+                               int64_t M, int64_t N, int64_t K, void *ws,
+                               size_t ws_bytes, void *stream);
+
+/* Fused: fp8bq_quant_act_ue8m0 into the workspace, then fp8bq_ue8m0_gemm. */
+FP8BQ_API int fp8bq_ue8m0_linear(const void *x, int64_t ldx, const void *w,
+                                 const uint8_t *u_w, const void *bias, void *y,
+                                 int64_t M, int64_t N, int64_t K, void *ws,
+                                 size_t ws_bytes, void *stream);
 
 /* ------------------------------------------------ weight / calibration set-up */
 
