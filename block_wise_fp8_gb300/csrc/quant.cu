@@ -173,8 +173,8 @@ __global__ void __launch_bounds__(kThreads) quant_mx_kernel(const uint8_t *__res
 
 // ---------------------------------------------------------------- per-token (per-row) quant
 // One scale per row, the group rule with the group spanning the row ("SGLang
-// 源码完全拆解(十九)", §激活量化: sglang_per_token_quant_fp8, one scale per
-// token; §per-channel 权重: per_token_group_quant_fp8 with group_size = K).
+// 源码完全拆解(十九)", §激活量化的三种选择: sglang_per_token_quant_fp8, one scale per
+// token; §装载后的三个分支: per_token_group_quant_fp8 with group_size = K).
 // One CTA per row, persistent over rows: pass 1 reduces max|x| over the row,
 // pass 2 re-reads it (an L1 hit) and converts with the row's scale, 16
 // channels (two 16-byte words) per thread per step.  The warp maxima are
@@ -373,7 +373,7 @@ __global__ void absmax_finalize_kernel(float *s) {
 // s, read from s's bits), and every code is re-encoded from its value,
 // q' = RNE_sat(dec(q) * s * 2^-e): the product of a 4-bit and a 24-bit
 // significand is exact in binary64, then rounded once to E4M3 ("SGLang 源码完全
-// 拆解(十九)", §分块路径的 process_weights_after_loading_block_quant).  q' may
+// 拆解(十九)", §分块路径的后处理).  q' may
 // be q itself (each code is read before it is written, by the same thread).
 __global__ void __launch_bounds__(kThreads) requant_ue8m0_kernel(const uint8_t *q, const float *__restrict__ s,
                                                                  int N, int K, int KB, uint8_t *q2,

@@ -266,8 +266,8 @@ FP8BQ_API int fp8bq_static_linear(const void *x, int64_t ldx, const float *s_x,
 /* Per-token dynamic quantisation: one FP32 scale per row,
  * s[i] = max(max_k |x[i,k]|, 1e-10) / 448 and q = RNE_sat(x / s[i]) (binary32
  * divisions) -- the group rule with the group spanning the row ("SGLang
- * 源码完全拆解(十九)", §激活量化, sglang_per_token_quant_fp8).  Applied to a
- * BF16 weight [N, K] it gives the per-channel weight scales (§per-channel 权重:
+ * 源码完全拆解(十九)", §激活量化的三种选择, sglang_per_token_quant_fp8).  Applied to a
+ * BF16 weight [N, K] it gives the per-channel weight scales (§装载后的三个分支:
  * per_token_group_quant_fp8 with group_size = K).  x: BF16 [M, K] pitch ldx;
  * q: E4M3 [M, K]; s: FP32 [M].  K % 16 == 0. */
 FP8BQ_API int fp8bq_channel_quant_act(const void *x, int64_t M, int64_t K,
@@ -300,7 +300,7 @@ FP8BQ_API int fp8bq_quant_act_ue8m0(const void *x, int64_t M, int64_t K,
                                     int64_t ldx, void *q, uint8_t *u,
                                     void *stream);
 
-/* One-time weight preparation (§分块路径的 process_weights_after_loading_block_quant:
+/* One-time weight preparation (§分块路径的后处理:
  * FP32 block scales requantised to power-of-two UE8M0 for the block-scaled
  * MMA): per 128 x 128 block, s' = 2^ceil(log2 s) (s > 0 finite), u_w = the code
  * of s', and every code re-encoded, q' = RNE_sat(dec(q) * s / s') (exact in

@@ -630,7 +630,7 @@ void orc_quant_ue8m0(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
 }
 
 /* FP32 block scales of a quantised weight re-expressed as UE8M0 ([SGL-19]
- * §分块路径的 process_weights_after_loading_block_quant: for the SM100 runner
+ * §分块路径的后处理: for the SM100 runner
  * the FP32 block scale is requantised to a power-of-two scale, since only
  * powers of two convert exactly in the kernel).  Reading: per bn x bk block,
  * s' = 2^e with e = ceil(log2 s) (the nearest power of two at or above s, so

@@ -1,7 +1,7 @@
 """Pins of the channelwise (per-token activation x per-channel weight) oracle
 ("SGLang 源码完全拆解(十九)", §一条 GEMM 的三种缩放组合: for per-token +
 per-channel the output scale is the M x N outer product s_x[i] * s_w[j];
-§per-channel 权重: the weight scale is the group rule with group = K)."""
+§装载后的三个分支: the weight scale is the group rule with group = K)."""
 import numpy as np
 import pytest
 

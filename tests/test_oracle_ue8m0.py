@@ -1,6 +1,6 @@
 """Pins of the block-FP8-with-UE8M0 oracle ("SGLang 源码完全拆解(十九)",
 §分块 GEMM 的后端分派: act_scale_ue8m0 limits the per-token-group scale to a
-power of two; §分块路径的 process_weights_after_loading_block_quant: FP32 block
+power of two; §分块路径的后处理: FP32 block
 scales requantised to power-of-two UE8M0 for the SM100 runner)."""
 import numpy as np
 import pytest
