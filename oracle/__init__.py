@@ -80,6 +80,9 @@ _SIGS = {
                                         _P, ctypes.c_int]),
     "orc_quant_ue8m0": (None, [_P, _I64, _I64, _I64, _I64, _P, _P]),
     "orc_requant_weight_ue8m0": (None, [_P, _P, _I64, _I64, _I64, _I64, _P, _P]),
+    "orc_gemm_grouped": (None, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P, ctypes.c_int]),
+    "orc_gemm_grouped_sampled": (None, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _I64,
+                                        _P, ctypes.c_int]),
     "orc_e4m3_dot_int": (ctypes.c_int64, [_P, _P, _I64]),
     "orc_e4m3_dot_f64": (ctypes.c_double, [_P, _P, _I64]),
 }
@@ -438,3 +441,57 @@ def gemm_block_ue8m0_sampled(qa, ua, qw, uw, rows, cols, bias=None,
                              threads: int | None = None) -> np.ndarray:
     return gemm_block_sampled(qa, ue8m0_to_f32(ua), qw, ue8m0_to_f32(uw), rows, cols,
                               bias=bias, threads=threads)
+
+
+# --------------------------------------------------------------------------
+# grouped (MoE) block-scaled GEMM
+# --------------------------------------------------------------------------
+
+def row_expert_contiguous(offsets, T: int) -> np.ndarray:
+    """Expert of each row when rows are sorted by expert: rows offsets[e] ..
+    offsets[e+1]-1 belong to expert e; rows outside every range get -1."""
+    off = np.asarray(offsets, np.int64)
+    r = np.full(T, -1, np.int32)
+    for e in range(off.size - 1):
+        r[off[e]:off[e + 1]] = e
+    return r
+
+
+def row_expert_masked(masked_m, max_m: int) -> np.ndarray:
+    """Expert of each row of the masked layout [E, max_m, K]: the first
+    masked_m[e] rows of slot e belong to expert e, the rest to none (-1)."""
+    m = np.asarray(masked_m, np.int64)
+    r = np.full(m.size * max_m, -1, np.int32)
+    for e in range(m.size):
+        r[e * max_m:e * max_m + min(int(m[e]), max_m)] = e
+    return r
+
+
+def gemm_grouped(qa, sa, qw, sw, row_expert, threads: int | None = None) -> np.ndarray:
+    """y[i, j] = block GEMM element of row i with its expert's weight qw[e] [N,K]
+    and scale grid sw[e]; rows of no expert are NaN.  binary64."""
+    qa, qw = _c(qa, np.uint8), _c(qw, np.uint8)
+    sa, sw = _c(sa, np.float32), _c(sw, np.float32)
+    re = _c(row_expert, np.int32).ravel()
+    M, K = qa.shape
+    E, N, K2 = qw.shape
+    if K2 != K or re.size != M or sw.shape[0] != E:
+        raise ValueError("shape mismatch")
+    y = np.empty((M, N), np.float64)
+    lib().orc_gemm_grouped(_p(qa), _p(sa), _p(qw), _p(sw), _p(re), M, N, K, _p(y),
+                           threads or default_threads())
+    return y
+
+
+def gemm_grouped_sampled(qa, sa, qw, sw, row_expert, rows, cols,
+                         threads: int | None = None) -> np.ndarray:
+    qa, qw = _c(qa, np.uint8), _c(qw, np.uint8)
+    sa, sw = _c(sa, np.float32), _c(sw, np.float32)
+    re = _c(row_expert, np.int32).ravel()
+    rows, cols = _c(rows, np.int64), _c(cols, np.int64)
+    M, K = qa.shape
+    E, N, _ = qw.shape
+    y = np.empty(rows.size, np.float64)
+    lib().orc_gemm_grouped_sampled(_p(qa), _p(sa), _p(qw), _p(sw), _p(re), M, N, K, _p(rows),
+                                   _p(cols), rows.size, _p(y), threads or default_threads())
+    return y

@@ -258,7 +258,7 @@ double orc_e4m3_dot_f64(const uint8_t *a, const uint8_t *b, int64_t n) {
   return acc;
 }
 
-enum { KIND_BLOCK = 0, KIND_MX = 1, KIND_STATIC = 2, KIND_CHANNEL = 3 };
+enum { KIND_BLOCK = 0, KIND_MX = 1, KIND_STATIC = 2, KIND_CHANNEL = 3, KIND_GROUPED = 4 };
 
 typedef struct {
   int kind;
@@ -268,6 +268,7 @@ typedef struct {
   const uint8_t *ua, *uw;  /* MX scale codes */
   const int64_t *part_sizes;
   int n_parts;
+  const int32_t *row_expert; /* grouped: expert of each activation row, -1 = none */
   const uint16_t *bias;
   int64_t M, N, K, bn, bk;
   const int64_t *rows, *cols; /* sampled mode when non-NULL */
@@ -328,6 +329,21 @@ static double elem_channel(const gemm_job *g, int64_t i, int64_t j) {
   return acc * (double)g->sa[i] * (double)g->sw[j];
 }
 
+/* Grouped (MoE) element: the block-wise element of row i against the weight
+ * [N][K] and scale grid [ceil(N/bn)][ceil(K/bk)] of that row's expert
+ * ([SGL-19] §MoE:专家权重多一个维度: expert weights [E, N, K] with the block
+ * scales replicated per expert, [E, ceil(N/b_n), ceil(K/b_k)]; the grouped GEMM
+ * takes tokens sorted by expert).  Rows of no expert give NaN. */
+static double elem_grouped(const gemm_job *g, int64_t i, int64_t j) {
+  int32_t e = g->row_expert[i];
+  if (e < 0) return NAN;
+  int64_t KB = (g->K + g->bk - 1) / g->bk, NB = (g->N + g->bn - 1) / g->bn;
+  gemm_job ge = *g;
+  ge.qw = g->qw + (int64_t)e * g->N * g->K;
+  ge.sw = g->sw + (int64_t)e * NB * KB;
+  return elem_block(&ge, i, j);
+}
+
 static void *gemm_worker(void *arg) {
   const gemm_job *g = (const gemm_job *)arg;
   for (int64_t t = g->t0; t < g->t1; ++t) {
@@ -343,6 +359,7 @@ static void *gemm_worker(void *arg) {
     if (g->kind == KIND_BLOCK) y = elem_block(g, i, j);
     else if (g->kind == KIND_MX) y = elem_mx(g, i, j);
     else if (g->kind == KIND_CHANNEL) y = elem_channel(g, i, j);
+    else if (g->kind == KIND_GROUPED) y = elem_grouped(g, i, j);
     else y = elem_static(g, i, j);
     if (g->bias) y += (double)orc_bf16_to_f32(g->bias[j]); /* epilogue bias */
     g->y[t] = y;
@@ -650,4 +667,24 @@ void orc_requant_weight_ue8m0(const uint8_t *q, const float *s, int64_t N, int64
         for (int64_t k = kb * bk; k < K && k < (kb + 1) * bk; ++k)
           q2[n * K + k] = orc_e4m3_encode(orc_e4m3_decode(q[n * K + k]) * m);
     }
+}
+
+void orc_gemm_grouped(const uint8_t *qa, const float *sa, const uint8_t *qw,
+                      const float *sw, const int32_t *row_expert, int64_t M,
+                      int64_t N, int64_t K, double *y, int nthreads) {
+  gemm_job g = job0(KIND_GROUPED, M, N, K, y, NULL);
+  g.qa = qa; g.qw = qw; g.sa = sa; g.sw = sw; g.bn = 128; g.bk = 128;
+  g.row_expert = row_expert;
+  run_gemm(g, nthreads);
+}
+
+void orc_gemm_grouped_sampled(const uint8_t *qa, const float *sa, const uint8_t *qw,
+                              const float *sw, const int32_t *row_expert, int64_t M,
+                              int64_t N, int64_t K, const int64_t *rows,
+                              const int64_t *cols, int64_t n, double *y, int nthreads) {
+  gemm_job g = job0(KIND_GROUPED, M, N, K, y, NULL);
+  g.qa = qa; g.qw = qw; g.sa = sa; g.sw = sw; g.bn = 128; g.bk = 128;
+  g.row_expert = row_expert;
+  g.rows = rows; g.cols = cols; g.n = n;
+  run_gemm(g, nthreads);
 }

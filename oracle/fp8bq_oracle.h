@@ -62,6 +62,16 @@ void orc_gemm_channel_sampled(const uint8_t *qa, const float *sa,
                               const int64_t *cols, int64_t n, double *y,
                               int nthreads);
 
+/* Grouped (MoE) block-scaled GEMM: row i uses expert row_expert[i]'s weight
+ * qw[e] [N][K] and scales sw[e] [ceil(N/128)][ceil(K/128)]; -1 gives NaN.    */
+void orc_gemm_grouped(const uint8_t *qa, const float *sa, const uint8_t *qw,
+                      const float *sw, const int32_t *row_expert, int64_t M,
+                      int64_t N, int64_t K, double *y, int nthreads);
+void orc_gemm_grouped_sampled(const uint8_t *qa, const float *sa, const uint8_t *qw,
+                              const float *sw, const int32_t *row_expert, int64_t M,
+                              int64_t N, int64_t K, const int64_t *rows,
+                              const int64_t *cols, int64_t n, double *y, int nthreads);
+
 /* ---- block FP8 with UE8M0 scales ---------------------------------------- */
 /* Group quantisation with power-of-two scales: u[M][ceil(K/group)].          */
 void orc_quant_ue8m0(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
