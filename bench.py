@@ -602,6 +602,48 @@ def run_extra(fb, torch, dev, stream, hbm_peak, fp8_peak):
     out["block_ue8m0"] = ue
     del qs, us
 
+    # grouped (MoE) block GEMM: 32 local experts, 4096 routed rows with skewed
+    # routing, the w13 and w2 shapes.  Four weight sets are drawn and copied to
+    # fill the experts (distinct memory, so every expert's weight streams from
+    # HBM; together they exceed L2 several times over).
+    mo = si.MOE
+    E, T = mo["E"], mo["T"]
+    counts = si.expert_counts(T, E, mo["skew"])
+    off = torch.tensor(np.concatenate([[0], np.cumsum(counts)]).astype(np.int32), device=dev)
+    live = int((counts > 0).sum())
+    gr = {"experts": E, "rows": T, "max_rows": int(counts.max()), "min_rows": int(counts.min()),
+          "m_tiles_256": int(np.sum((counts + 255) // 256))}
+    for which, N, K in (("w13", 2 * mo["I"], mo["H"]), ("w2", mo["H"], mo["I"])):
+        KB, NB = K // 128, N // 128
+        qw = torch.empty(E, N, K, dtype=torch.uint8, device=dev)
+        sw = torch.empty(E, NB, KB, dtype=torch.float32, device=dev)
+        for e in range(4):
+            wb = to_dev(si.weights(N, K, base_seed=e))
+            fb.fp8bq_quant_weight_block(wb, qw[e], sw[e])
+            del wb
+        for e in range(4, E):
+            qw[e].copy_(qw[e % 4])
+            sw[e].copy_(sw[e % 4])
+        qa = torch.empty(T, K, dtype=torch.uint8, device=dev)
+        sa = torch.empty(T, KB, dtype=torch.float32, device=dev)
+        fb.fp8bq_quant_act(to_dev(si.activations(T, K)), qa, sa)
+        y = torch.empty(T, N, dtype=torch.bfloat16, device=dev)
+        ws = fb.new_workspace(fb.OP_GROUPED_GEMM, T, N, K, device=dev)
+        t = _time_back_to_back(torch, stream,
+                               [lambda: fb.fp8bq_grouped_gemm(qa, sa, qw, sw, off, y, ws)], 20)
+        flops = 2.0 * T * N * K
+        bb = live * (N * K + NB * KB * 4) + T * (K + KB * 4) + 2 * T * N
+        tf = flops / (t * 1e-3) / 1e12
+        gbs = bb / (t * 1e-3) / 1e9
+        # the bound: the larger of the HBM time and the FP8 tensor time
+        t_min = max(bb / (hbm_peak * 1e9), flops / (fp8_peak * 1e12))
+        gr[f"{which}_N{N}_K{K}"] = {"us": round(t * 1e3, 2), "tflops": round(tf, 1),
+                                    "gbs": round(gbs, 1), "frac_fp8": round(tf / fp8_peak, 4),
+                                    "frac_hbm": round(gbs / hbm_peak, 4),
+                                    "frac_roofline": round(t_min / (t * 1e-3), 4)}
+        del qw, sw, qa, sa, y
+    out["grouped_moe"] = gr
+
     # residual add + RMSNorm + quantisation (the step before the linear):
     # x, residual in; updated residual, E4M3 codes (and group scales) out
     norm = {}

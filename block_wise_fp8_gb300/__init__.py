@@ -27,6 +27,7 @@ __all__ = [
     "OP_CHANNEL_LINEAR", "fp8bq_channel_quant_act", "fp8bq_channel_gemm", "fp8bq_channel_linear",
     "OP_UE8M0_GEMM", "OP_UE8M0_LINEAR", "fp8bq_quant_act_ue8m0", "fp8bq_requant_weight_ue8m0",
     "fp8bq_ue8m0_gemm", "fp8bq_ue8m0_linear",
+    "OP_GROUPED_GEMM", "fp8bq_grouped_gemm", "fp8bq_grouped_gemm_masked",
     "library_path",
     "fp8bq_version", "fp8bq_status_string", "fp8bq_last_cuda_error",
     "fp8bq_workspace_bytes", "fp8bq_workspace_init", "fp8bq_poll_status",
@@ -41,7 +42,7 @@ __all__ = [
 SCALE_ROW_MAJOR, SCALE_COL_MAJOR = 0, 1
 (OP_GEMM, OP_LINEAR, OP_MX_GEMM, OP_MX_LINEAR, OP_STATIC_GEMM,
  OP_STATIC_LINEAR, OP_CHANNEL_GEMM, OP_CHANNEL_LINEAR, OP_UE8M0_GEMM,
- OP_UE8M0_LINEAR) = range(10)
+ OP_UE8M0_LINEAR, OP_GROUPED_GEMM) = range(11)
 NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024      # FP8BQ_NOALLOC_SCRATCH_BYTES
 
 STATUS_NAMES = {0: "FP8BQ_OK", 1: "FP8BQ_ERR_NULL", 2: "FP8BQ_ERR_SHAPE",
@@ -91,6 +92,9 @@ def _load():
         "fp8bq_requant_weight_ue8m0": (I32, [P, P, I64, I64, P, P, P]),
         "fp8bq_ue8m0_gemm": (I32, [P, P, P, P, P, P, I64, I64, I64, P, SZ, P]),
         "fp8bq_ue8m0_linear": (I32, [P, I64, P, P, P, P, I64, I64, I64, P, SZ, P]),
+        "fp8bq_grouped_gemm": (I32, [P, P, I32, P, P, P, I64, P, I64, I64, I64, P, SZ, P]),
+        "fp8bq_grouped_gemm_masked": (I32, [P, P, I32, P, P, P, I64, I64, P, I64, I64, P, SZ,
+                                            P]),
         "fp8bq_channel_gemm": (I32, [P, P, P, P, P, P, I64, I64, I64, P, SZ, P]),
         "fp8bq_channel_linear": (I32, [P, I64, P, P, P, P, I64, I64, I64, P, SZ, P]),
         "fp8bq_add_rmsnorm_quant_act": (I32, [P, I64, P, I64, P, P, F32, I64, I64, P, P, P,
@@ -305,6 +309,31 @@ def fp8bq_ue8m0_linear(x, w, u_w, y, ws, bias=None, stream=None):
     _check(_lib.fp8bq_ue8m0_linear(_ptr(x), _ld(x), _ptr(w), _ptr(u_w), _ptr(bias), _ptr(y),
                                    M, N, K, _ptr(ws), _nbytes(ws), _stream(stream)),
            "fp8bq_ue8m0_linear")
+
+
+# ---------------------------------------------------------------- grouped (MoE)
+
+def fp8bq_grouped_gemm(q, s_x, w, s_w, offsets, y, ws, s_layout: int = SCALE_ROW_MAJOR,
+                       stream=None):
+    """Rows offsets[e] .. offsets[e+1]-1 of q / y use expert e's weight w[e]
+    [N, K] and scale grid s_w[e]; offsets is a device int32 tensor [E+1]."""
+    M, K = q.shape
+    E, N, _ = w.shape
+    _check(_lib.fp8bq_grouped_gemm(_ptr(q), _ptr(s_x), s_layout, _ptr(w), _ptr(s_w),
+                                   _ptr(offsets), E, _ptr(y), M, N, K, _ptr(ws), _nbytes(ws),
+                                   _stream(stream)), "fp8bq_grouped_gemm")
+
+
+def fp8bq_grouped_gemm_masked(q, s_x, w, s_w, masked_m, y, ws, s_layout: int = SCALE_ROW_MAJOR,
+                              stream=None):
+    """q [E, max_m, K] (or [E*max_m, K]); the first masked_m[e] rows of slot e
+    use expert e's weight; masked_m is a device int32 tensor [E]."""
+    E, N, K = w.shape
+    max_m = q.numel() // (K * E) if E else 0
+    _check(_lib.fp8bq_grouped_gemm_masked(_ptr(q), _ptr(s_x), s_layout, _ptr(w), _ptr(s_w),
+                                          _ptr(masked_m), E, max_m, _ptr(y), N, K, _ptr(ws),
+                                          _nbytes(ws), _stream(stream)),
+           "fp8bq_grouped_gemm_masked")
 
 
 def fp8bq_add_rmsnorm_quant_act(x, gamma, eps: float, residual=None, residual_out=None,

@@ -14,6 +14,10 @@ constexpr int kBlockN = 128;  // rows of W sharing one weight scale
 constexpr int kMxGroup = 32;  // K elements per UE8M0 scale
 constexpr int kMaxParts = 64; // static path: maximum number of output partitions
 constexpr int kMxBN = 224;    // weight rows per MXFP8 tile (must match gemm_mx.cu)
+constexpr int kMaxExperts = 1024;  // grouped GEMM: most expert segments per call
+// grouped GEMM: shared memory of the per-CTA tile table (first m-tile, first
+// row and end row of every expert segment, int32)
+constexpr int kGroupTableBytes = (3 * kMaxExperts + 1) * 4;
 
 // Status values stored in the workspace status word (same numbers as fp8bq_status).
 constexpr uint32_t kStatusTimeout = 8;
@@ -96,6 +100,15 @@ struct GemmArgs {
   const void *bias;
   void *y;
   int y_tma;  // set by the launcher: Y is written with TMA stores
+  // grouped (MoE) form, g_experts > 0: A and Y rows are split into one segment
+  // per expert (contiguous: rows g_offsets[e] .. g_offsets[e+1]-1; masked: the
+  // first g_masked[e] of the g_max_m rows from e * g_max_m), B is [E * N, K]
+  // (expert e's weight at rows e * N) and s_w [E * ceil(N/128)][KB]
+  int g_experts;
+  const int *g_offsets;
+  const int *g_masked;
+  int g_max_m;
+  int g_tile_cap;  // most m-tiles the segments can hold (set by the launcher)
   // workspace
   uint32_t *status;
   uint32_t *counters;
@@ -168,6 +181,10 @@ bool cached_bf16_rows_map(CUtensorMap *m, const void *base, int64_t rows, int64_
 // or 64, and `grid` the number of CTAs.
 cudaError_t run_block_pair(int bn, const GemmArgs &a, const void *q, const void *w,
                            const LaunchShape &sh, int grid, cudaStream_t st, int *status);
+// Grouped block GEMM: 256 x 256 pair tiles (`grid` pairs) or single-CTA
+// 128 x 256 tiles (`grid` CTAs).
+cudaError_t run_block_grouped(bool pair, const GemmArgs &a, const void *q, const void *w,
+                              const LaunchShape &sh, int grid, cudaStream_t st, int *status);
 cudaError_t run_block_swap(int bn, const GemmArgs &a, const void *q, const void *w,
                            const LaunchShape &sh, int grid, cudaStream_t st, int *status);
 cudaError_t run_tensor_pair(int bn, const GemmArgs &a, const void *q, const void *w,

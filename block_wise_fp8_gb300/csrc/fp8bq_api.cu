@@ -210,6 +210,46 @@ int gemm_static_impl(const void *q, const float *s_x, const void *w, const float
 
 // An empty batch (M == 0) launches nothing; only the other extents are checked
 // and pointers may be NULL.
+// Grouped block-scaled GEMM over E experts.  The segment bounds stay on the
+// device (the routing kernel that wrote them ran on the stream before); the
+// launcher bounds the tiles they can hold from E, M and max_m alone.
+int gemm_grouped_impl(const void *q, const float *s_x, int s_layout, const void *w,
+                      const float *s_w, const int32_t *offsets, const int32_t *masked_m,
+                      int64_t E, int64_t max_m, void *y, int64_t M, int64_t N, int64_t K, void *ws,
+                      cudaStream_t st, const DeviceInfo &dev) {
+  GemmArgs a = base_args(kModeBlock, M, N, K, nullptr, y, ws, FP8BQ_OP_GROUPED_GEMM);
+  a.sx = s_x;
+  a.sx_layout = s_layout;
+  a.ldsx = s_layout == FP8BQ_SCALE_ROW_MAJOR ? static_cast<int>((K + 127) / 128)
+                                             : static_cast<int>((M + 3) / 4 * 4);
+  a.sw = s_w;
+  a.g_experts = static_cast<int>(E);
+  a.g_offsets = offsets;
+  a.g_masked = masked_m;
+  a.g_max_m = static_cast<int>(max_m);
+  cudaError_t e;
+  int r = launch_gemm(a, q, w, dev, st, &e);
+  return finish_launch(r, e);
+}
+
+// Checks shared by both grouped forms (M rows of A and Y in all).
+int check_grouped(const void *q, const float *s_x, int s_layout, const void *w, const float *s_w,
+                  const void *bounds, int64_t E, int64_t M, int64_t N, int64_t K, int64_t cap,
+                  void *y) {
+  if (!q || !s_x || !w || !s_w || !bounds || !y) return FP8BQ_ERR_NULL;
+  RETURN_IF(check_gemm_shape(M, N, K, 16));
+  if (E < 1 || E > kMaxExperts) return FP8BQ_ERR_SHAPE;
+  // expert rows E * N and (128-row) tile counts x weight tiles stay 32-bit
+  if (E * N > (int64_t(1) << 31) - 1 || cap * ((N + 255) / 256) > (int64_t(1) << 31) - 1)
+    return FP8BQ_ERR_SHAPE;
+  if (s_layout != FP8BQ_SCALE_ROW_MAJOR && s_layout != FP8BQ_SCALE_COL_MAJOR)
+    return FP8BQ_ERR_UNSUPPORTED;
+  if (!aligned(q, 16) || !aligned(w, 16) || !aligned(y, 16) || !aligned(s_x, 4) ||
+      !aligned(s_w, 4) || !aligned(bounds, 4))
+    return FP8BQ_ERR_ALIGN;
+  return FP8BQ_OK;
+}
+
 int empty_batch(int64_t K, int64_t N) { return (K >= 1 && N >= 1) ? FP8BQ_OK : FP8BQ_ERR_SHAPE; }
 
 int check_parts(const int64_t *parts, int n_parts, int64_t N) {
@@ -280,7 +320,7 @@ const char *fp8bq_status_string(int s) {
 int fp8bq_last_cuda_error(void) { return g_last_cuda_error; }
 
 size_t fp8bq_workspace_bytes(int op, int64_t M, int64_t N, int64_t K) {
-  if (op < FP8BQ_OP_GEMM || op > FP8BQ_OP_UE8M0_LINEAR || M < 0 || N < 1 || K < 1) return 256;
+  if (op < FP8BQ_OP_GEMM || op > FP8BQ_OP_GROUPED_GEMM || M < 0 || N < 1 || K < 1) return 256;
   return workspace_layout(op, M, N, K).total;
 }
 
@@ -724,6 +764,36 @@ int fp8bq_ue8m0_linear(const void *x, int64_t ldx, const void *w, const uint8_t 
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);
   return gemm_mx_impl(q, u, w, u_w, bias, y, M, N, K, ws, FP8BQ_OP_UE8M0_LINEAR, st, dev, true);
+}
+
+// ------------------------------------------------------------------ grouped (MoE)
+
+int fp8bq_grouped_gemm(const void *q, const float *s_x, int s_layout, const void *w,
+                       const float *s_w, const int32_t *offsets, int64_t E, void *y, int64_t M,
+                       int64_t N, int64_t K, void *ws, size_t ws_bytes, void *stream) {
+  RETURN_IF(check_grouped(q, s_x, s_layout, w, s_w, offsets, E, M, N, K, E + (M + 127) / 128, y));
+  RETURN_IF(check_ws(ws, ws_bytes, FP8BQ_OP_GROUPED_GEMM, M, N, K));
+  if (M == 0) return FP8BQ_OK;
+  DeviceInfo dev;
+  RETURN_IF(device_info(&dev));
+  return gemm_grouped_impl(q, s_x, s_layout, w, s_w, offsets, nullptr, E, 0, y, M, N, K, ws,
+                           static_cast<cudaStream_t>(stream), dev);
+}
+
+int fp8bq_grouped_gemm_masked(const void *q, const float *s_x, int s_layout, const void *w,
+                              const float *s_w, const int32_t *masked_m, int64_t E,
+                              int64_t max_m, void *y, int64_t N, int64_t K, void *ws,
+                              size_t ws_bytes, void *stream) {
+  if (max_m < 0 || max_m > ((int64_t(1) << 31) - 1) / (E > 0 ? E : 1)) return FP8BQ_ERR_SHAPE;
+  const int64_t M = E * max_m;
+  RETURN_IF(check_grouped(q, s_x, s_layout, w, s_w, masked_m, E, M, N, K,
+                          E * ((max_m + 127) / 128), y));
+  RETURN_IF(check_ws(ws, ws_bytes, FP8BQ_OP_GROUPED_GEMM, M, N, K));
+  if (M == 0) return FP8BQ_OK;
+  DeviceInfo dev;
+  RETURN_IF(device_info(&dev));
+  return gemm_grouped_impl(q, s_x, s_layout, w, s_w, nullptr, masked_m, E, max_m, y, M, N, K,
+                           ws, static_cast<cudaStream_t>(stream), dev);
 }
 
 }  // extern "C"

@@ -1,5 +1,6 @@
 // gemm_block.cu -- instantiations of the block-scaled (FP32 128x128 / 1x128
-// scales) FP8 GEMM: the pair prefill tiles and the swapped decode tiles.
+// scales) FP8 GEMM: the pair prefill tiles, the swapped decode tiles, and the
+// grouped (MoE) forms: 256 x 256 pair tiles and single-CTA 128 x 256 tiles.
 #include "gemm_kernel.cuh"
 
 namespace fp8bq {
@@ -8,6 +9,15 @@ cudaError_t run_block_pair(int bn, const GemmArgs &a, const void *q, const void 
                            const LaunchShape &sh, int grid, cudaStream_t st, int *status) {
   if (bn == 192) return run<kModeBlock, false, 192, 6, 12, 2, true>(a, q, w, sh, grid, st, status);
   return run<kModeBlock, false, 256, 5, 8, 2, true>(a, q, w, sh, grid, st, status);
+}
+
+cudaError_t run_block_grouped(bool pair, const GemmArgs &a, const void *q, const void *w,
+                              const LaunchShape &sh, int grid, cudaStream_t st, int *status) {
+  // single-CTA tiles: three 48 KB stages, with the Y staging boxes, the scale
+  // ring and the tile table, fill the 227 KB (a fourth stage in place of the
+  // staging, with Y stored row by row, measured no faster)
+  if (pair) return run<kModeBlock, false, 256, 5, 8, 2, true, true>(a, q, w, sh, grid, st, status);
+  return run<kModeBlock, false, 256, 3, 8, 2, false, true>(a, q, w, sh, grid, st, status);
 }
 
 cudaError_t run_block_swap(int bn, const GemmArgs &a, const void *q, const void *w,

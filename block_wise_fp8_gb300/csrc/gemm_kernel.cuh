@@ -65,7 +65,8 @@ constexpr uint32_t pow2_at_least(uint32_t v) {
   return p;
 }
 
-template <int MODE, bool SWAP, int BN, int STAGES, int EPI_WARPS, int ACCB, bool PAIR>
+template <int MODE, bool SWAP, int BN, int STAGES, int EPI_WARPS, int ACCB, bool PAIR,
+          bool GROUPED = false>
 struct Cfg {
   static constexpr int kMmaM = PAIR ? 256 : 128;     // rows of the MMA (both CTAs)
   static constexpr int kBrows = PAIR ? BN / 2 : BN;  // weight rows loaded by this CTA
@@ -83,10 +84,10 @@ struct Cfg {
   // block tiles: two MMA-issuing warps take alternate K blocks (disjoint TMEM
   // partial buffers), so one issues while the other waits on its barriers
   static constexpr int kIssuers = (MODE == kModeBlock) ? 2 : 1;
-  // block pair tiles keep the promoted FP32 accumulators in the epilogue warps'
-  // registers: warpgroup 0 (producer, the two issuers and one idle warp) hands
-  // registers to the epilogue warpgroups with setmaxnreg
-  static constexpr bool kRegSplit = (MODE == kModeBlock) && PAIR;
+  // block pair and normal tiles keep the promoted FP32 accumulators in the
+  // epilogue warps' registers: warpgroup 0 (producer, the two issuers and one
+  // idle warp) hands registers to the epilogue warpgroups with setmaxnreg
+  static constexpr bool kRegSplit = (MODE == kModeBlock) && !SWAP;
   static constexpr int kEpiBase = kRegSplit ? 4 : 1 + kIssuers;  // first epilogue warp
   static constexpr int kThreads = 32 * (kEpiBase + EPI_WARPS);
   // register budget: warps are dealt round-robin to the SM's four schedulers,
@@ -94,7 +95,9 @@ struct Cfg {
   // groups of four warps
   static constexpr int kBoundThreads = (kThreads + 127) / 128 * 128;
   static constexpr int kLaunchRegs = (65536 / kBoundThreads) / 8 * 8 < 248 ? (65536 / kBoundThreads) / 8 * 8 : 248;
-  static constexpr int kLowRegs = 32;   // warpgroup 0 after the split
+  // warpgroup 0 after the split (grouped launches: the producer and the
+  // issuers also walk the expert table)
+  static constexpr int kLowRegs = GROUPED ? 48 : 32;
   static constexpr int kHighRegsRaw =
       (kLaunchRegs * kBoundThreads - 128 * kLowRegs) / (kBoundThreads > 128 ? kBoundThreads - 128 : 1) / 8 * 8;
   static constexpr int kHighRegs = kHighRegsRaw < 248 ? kHighRegsRaw : 248;  // epilogue warpgroups
@@ -108,9 +111,9 @@ struct Cfg {
                              : (kCPT % 32 == 0) ? 32 : 16;
   // columns loaded per tcgen05.wait::ld in the block-tile promotion
   static constexpr int kLD = kRegSplit ? (kCPT < 64 ? kCPT : 64) : kCW;
-  // block pair tiles write Y with TMA stores from a per-warp staging area
-  // (32 rows x 64 BF16 columns per box, 128-byte swizzled)
-  static constexpr bool kTmaStoreY = (MODE == kModeBlock) && PAIR;
+  // block pair and normal tiles write Y with TMA stores from a per-warp
+  // staging area (32 rows x 64 BF16 columns per box, 128-byte swizzled)
+  static constexpr bool kTmaStoreY = (MODE == kModeBlock) && !SWAP;
   static constexpr int kYBoxCols = 64;
   static constexpr int kYBoxBytes = 32 * kYBoxCols * 2;
   // one box per epilogue warp; a thread's columns beyond one box go out in
@@ -118,10 +121,10 @@ struct Cfg {
   static constexpr int kYStageBytes = kTmaStoreY ? EPI_WARPS * kYBoxBytes : 0;
   static constexpr int kBbytes = kBrows * 128;
   static constexpr int kStageBytes = kAbytes + kBbytes;
-  // block pair tiles: promotion factors come through a shared-memory ring
-  // filled by the TMA producer, kScQuad K blocks per slot: s_x of this CTA's
-  // 128 rows and s_w of the tile's (at most two) 128-row weight blocks
-  static constexpr bool kScRing = (MODE == kModeBlock) && PAIR;
+  // block pair and normal tiles: promotion factors come through a shared-memory
+  // ring filled by the TMA producer, kScQuad K blocks per slot: s_x of this
+  // CTA's 128 rows and s_w of the tile's (at most two) 128-row weight blocks
+  static constexpr bool kScRing = (MODE == kModeBlock) && !SWAP;
   static constexpr int kScQuad = 4;
   static constexpr int kScSlots = kScRing ? 4 : 0;
   static constexpr int kScDiv = kScSlots > 0 ? kScSlots : 1;  // ring index divisor
@@ -226,40 +229,64 @@ struct Unit {
   int b_row0;       // first B row of the tile (the epilogue's first weight column)
   int b_load_row0;  // first B row this CTA loads (pair tiles: its half)
   int kb0, kb1, split, tile;
+  int row_end;      // rows of A at or past this one are not the tile's (M, or the segment end)
+  int expert;       // grouped form: the tile's expert (0 otherwise)
+  int sw_row0;      // row of the tile's first 128-row weight block in s_w
 };
 
-template <bool SWAP, bool PAIR>
+// Grouped form: the m-tile table of one launch, built by every CTA in shared
+// memory as three int arrays back to back: start [E+1], begin [E], end [E].
+// Expert e owns m-tiles start[e] .. start[e+1]-1 and rows begin[e] .. end[e]-1.
+// experts == 0 for plain GEMMs.
+struct GroupTable {
+  const int *start;
+  int experts;
+};
+
+template <bool SWAP, bool PAIR, bool GROUPED>
 __device__ __forceinline__ Unit decode_unit(int u, int num_a_tiles, int splits, int kps, int KB,
-                                            int bn, uint32_t rank) {
+                                            int bn, uint32_t rank, int M, int N,
+                                            const GroupTable &gt) {
   Unit r;
-  if (PAIR) {
-    // A = tokens (256 per pair tile, 128 per CTA), B = bn weight rows (bn/2 per CTA)
+  r.row_end = M;
+  r.expert = 0;
+  if (!SWAP) {
+    // A = tokens (256 per pair tile, 128 per CTA), B = bn weight rows (pair
+    // tiles: bn/2 per CTA); M fastest so concurrently running tiles share
+    // weight tiles in L2
+    constexpr int kTileRows = PAIR ? 2 * kBM : kBM;
     const int mt = u % num_a_tiles, nt = u / num_a_tiles;
     r.tile = u;
     r.split = 0;
-    r.a_row0 = mt * 2 * kBM + static_cast<int>(rank) * kBM;
+    int row0 = mt * kTileRows;
+    if (GROUPED) {
+      // the expert e with start[e] <= mt < start[e+1] (it has at least one tile)
+      int lo = 0, hi = gt.experts;
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (gt.start[mid] <= mt) lo = mid;
+        else hi = mid;
+      }
+      r.expert = lo;
+      const int *begin = gt.start + gt.experts + 1;
+      row0 = begin[lo] + (mt - gt.start[lo]) * kTileRows;
+      r.row_end = begin[gt.experts + lo];
+    }
+    r.a_row0 = row0 + static_cast<int>(rank) * kBM;
     r.b_row0 = nt * bn;
-    r.b_load_row0 = r.b_row0 + static_cast<int>(rank) * (bn / 2);
+    r.b_load_row0 = r.expert * N + r.b_row0 + (PAIR ? static_cast<int>(rank) * (bn / 2) : 0);
+    r.sw_row0 = r.expert * ((N + kBlockN - 1) / kBlockN) + r.b_row0 / kBlockN;
     r.kb0 = 0;
     r.kb1 = KB;
     return r;
   }
-  if (SWAP) {
-    // A = weight rows (128 per tile), B = all tokens; units = tiles x splits
-    r.tile = u / splits;
-    r.split = u - r.tile * splits;
-    r.a_row0 = r.tile * kBM;
-    r.b_row0 = 0;
-  } else {
-    // A = tokens (128 per tile), B = weight rows (bn per tile); M fastest so
-    // concurrently running CTAs share weight tiles in L2
-    const int mt = u % num_a_tiles, nt = u / num_a_tiles;
-    r.tile = u;
-    r.split = 0;
-    r.a_row0 = mt * kBM;
-    r.b_row0 = nt * bn;
-  }
-  r.b_load_row0 = r.b_row0;
+  // swapped: A = weight rows (128 per tile), B = all tokens; units = tiles x splits
+  r.tile = u / splits;
+  r.split = u - r.tile * splits;
+  r.a_row0 = r.tile * kBM;
+  r.b_row0 = 0;
+  r.b_load_row0 = 0;
+  r.sw_row0 = 0;
   r.kb0 = r.split * kps;
   r.kb1 = min(KB, r.kb0 + kps);
   return r;
@@ -294,15 +321,15 @@ __device__ __forceinline__ void store_row(uint16_t *y, const float *v, int m, in
 
 // One CTA per SM.  Registers are split over the SM's four schedulers, so the
 // per-thread budget is set by the scheduler holding the most warps.
-template <int MODE, bool SWAP, int BN, int STAGES, int EPI_WARPS, int ACCB, bool PAIR>
-__global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, PAIR>::kBoundThreads, 1)
+template <int MODE, bool SWAP, int BN, int STAGES, int EPI_WARPS, int ACCB, bool PAIR, bool GROUPED>
+__global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, PAIR, GROUPED>::kBoundThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmY,
                     const __grid_constant__ CUtensorMap tmSx,
                     const __grid_constant__ CUtensorMap tmSw,
                     const __grid_constant__ GemmArgs args, const LaunchShape shape) {
-  using C = Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, PAIR>;
+  using C = Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, PAIR, GROUPED>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -371,9 +398,12 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
   // tiles; L2 is the point of coherence, so a prefetch cannot make a later load
   // see stale data even if the preceding kernel writes those weights.
   griddep_launch_dependents();
-  if (warp == 0 && lane == 0 && cl_id < shape.units) {
-    const Unit w0 = decode_unit<SWAP, PAIR>(cl_id, shape.num_a_tiles, shape.splits, shape.kps,
-                                            shape.KB, BN, rank);
+  GroupTable gt{nullptr, 0};
+  // (grouped launches learn their tiles only from the segment bounds, which the
+  // preceding kernel may write: no prefetch)
+  if (!GROUPED && warp == 0 && lane == 0 && cl_id < shape.units) {
+    const Unit w0 = decode_unit<SWAP, PAIR, GROUPED>(cl_id, shape.num_a_tiles, shape.splits, shape.kps,
+                                            shape.KB, BN, rank, args.M, args.N, gt);
     const int npf = min(w0.kb1 - w0.kb0, SWAP ? 64 : 8);
     for (int i = 0; i < npf; ++i) {
       if (SWAP) tma_prefetch_l2_2d(&tmA, (w0.kb0 + i) * 128, w0.a_row0);
@@ -381,6 +411,58 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
     }
   }
   griddep_wait();
+
+  int units = shape.units, num_a = shape.num_a_tiles;
+  if (GROUPED) {
+    // grouped form: every CTA turns the expert segments into its own copy of
+    // the m-tile table (256-row pair tiles or 128-row tiles, a segment's last
+    // tile ragged).  Bounds
+    // are clamped into [0, M], so no copy or store leaves A or Y whatever the
+    // offsets hold.
+    const int E = args.g_experts;
+    int *gs = reinterpret_cast<int *>(sx_stage);
+    int *gb = gs + E + 1;
+    int *ge = gb + E;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+      int b, en;
+      if (args.g_offsets) {
+        b = args.g_offsets[e];
+        en = args.g_offsets[e + 1];
+      } else {
+        b = e * args.g_max_m;
+        en = b + min(max(args.g_masked[e], 0), args.g_max_m);
+      }
+      b = min(max(b, 0), args.M);
+      en = min(max(en, b), args.M);
+      gb[e] = b;
+      ge[e] = en;
+      const int len = en - b;
+      constexpr int kTileRows = PAIR ? 2 * kBM : kBM;
+      gs[e + 1] = len / kTileRows + (len % kTileRows != 0);
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // inclusive scan of the tile counts, 32 experts per step
+      int carry = 0;
+      for (int base = 0; base < E; base += 32) {
+        const int e = base + lane;
+        int v = e < E ? gs[e + 1] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int t = __shfl_up_sync(0xffffffffu, v, o);
+          if (lane >= o) v += t;
+        }
+        if (e < E) gs[e + 1] = v + carry;
+        carry += __shfl_sync(0xffffffffu, v, 31);
+      }
+      if (lane == 0) gs[0] = 0;
+    }
+    __syncthreads();
+    gt = GroupTable{gs, E};
+    // never more tiles than the host sized the grid and the table for
+    num_a = min(gs[E], args.g_tile_cap);
+    units = num_a * ((args.N + BN - 1) / BN);
+  }
 
   if (C::kRegSplit) {
     if (warp < 4) setmaxnreg_dec<C::kLowRegs>();
@@ -399,8 +481,8 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
         uint32_t it = 0, sq = 0;
         bool ok = true;
         const bool sc_tma = C::kScRing && args.sc_tma;
-        for (int u = cl_id; ok && u < shape.units; u += cl_num) {
-          const Unit w = decode_unit<SWAP, PAIR>(u, shape.num_a_tiles, shape.splits, shape.kps, KB, BN, rank);
+        for (int u = cl_id; ok && u < units; u += cl_num) {
+          const Unit w = decode_unit<SWAP, PAIR, GROUPED>(u, num_a, shape.splits, shape.kps, KB, BN, rank, args.M, args.N, gt);
           for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
             if (sc_tma && (kb - w.kb0) % C::kScQuad == 0) {
               // promotion factors of K blocks kb .. kb+3: this CTA's s_x rows and
@@ -414,7 +496,7 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
               mbar_arrive_expect_tx(&bars->sc_full[q], C::kScXBytes + C::kScWBytes);
               if (args.sx_layout == 0) tma_load_2d(slot, &tmSx, &bars->sc_full[q], kb, w.a_row0);
               else tma_load_2d(slot, &tmSx, &bars->sc_full[q], w.a_row0, kb);
-              tma_load_2d(slot + C::kScXBytes, &tmSw, &bars->sc_full[q], kb, w.b_row0 / kBlockN);
+              tma_load_2d(slot + C::kScXBytes, &tmSw, &bars->sc_full[q], kb, w.sw_row0);
               sc_issued |= 1u << q;
               sc_phase_bits = (sc_phase_bits & ~(1u << q)) | (qph << q);
               ++sq;
@@ -480,8 +562,8 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
       if (lane == 0 && (!PAIR || leader)) {
         uint32_t it = 0, uit = 0;
         bool ok = true;
-        for (int u = cl_id; ok && u < shape.units; u += cl_num, ++uit) {
-          const Unit w = decode_unit<SWAP, PAIR>(u, shape.num_a_tiles, shape.splits, shape.kps, KB, BN, rank);
+        for (int u = cl_id; ok && u < units; u += cl_num, ++uit) {
+          const Unit w = decode_unit<SWAP, PAIR, GROUPED>(u, num_a, shape.splits, shape.kps, KB, BN, rank, args.M, args.N, gt);
           if (MODE != kModeBlock) {
             const uint32_t b = uit % ACCB, ph = (uit / ACCB) & 1u;
             if (!mbar_wait(&bars->tempty[b], ph ^ 1u, abort_flag, limit)) {
@@ -584,8 +666,8 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
     const uint16_t *bias = static_cast<const uint16_t *>(args.bias);
     uint32_t kit = 0, uit = 0, sq = 0;
     bool ok = true;
-    for (int u = cl_id; u < shape.units; u += cl_num, ++uit) {
-      const Unit w = decode_unit<SWAP, PAIR>(u, shape.num_a_tiles, shape.splits, shape.kps, KB, BN, rank);
+    for (int u = cl_id; u < units; u += cl_num, ++uit) {
+      const Unit w = decode_unit<SWAP, PAIR, GROUPED>(u, num_a, shape.splits, shape.kps, KB, BN, rank, args.M, args.N, gt);
       const int d_row = w.a_row0 + 32 * quarter + lane;  // row of D held by this thread
       const int col0 = cg * C::kCPT;                     // first D column of this thread
 
@@ -597,7 +679,7 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
           float acc[C::kCPT];
 #pragma unroll
           for (int j = 0; j < C::kCPT; ++j) acc[j] = 0.0f;
-          const bool row_ok = m < args.M;
+          const bool row_ok = m < w.row_end;
           // one K block: wait for its partial, read it from TMEM, hand the
           // buffer back to the MMA issuer, promote it with factor f
           auto promote = [&](float f) -> bool {
@@ -667,7 +749,7 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
           } else {
             // factors loaded by each thread two K blocks ahead
             const int nb = min(nbase / kBlockN, NBLK - 1);
-            const float *swrow = args.sw + static_cast<int64_t>(nb) * KB;
+            const float *swrow = args.sw + (static_cast<int64_t>(w.expert) * NBLK + nb) * KB;
             auto sx_at = [&](int kb) -> float {
               if (!row_ok || kb >= w.kb1) return 0.0f;
               return __ldg(args.sx + (args.sx_layout == 0
@@ -696,13 +778,16 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
             for (int j = 0; j < C::kCPT; ++j)
               if (nbase + j < args.N) acc[j] += bf16_bits_to_float(bias[nbase + j]);
           }
-          if (C::kTmaStoreY && args.y_tma) {
+          // a TMA box writes all of its 32 rows that lie inside Y: only where
+          // they all belong to the tile (the grouped form's segments end
+          // anywhere) does the warp use one
+          const int row0 = w.a_row0 + 32 * quarter;
+          if (C::kTmaStoreY && args.y_tma && (row0 + 32 <= w.row_end || w.row_end == args.M)) {
             // BF16 rows into this warp's staging box (16-byte chunk c of row r
             // at chunk position c ^ (r % 8): the 128-byte swizzle the tensor map
             // names, and conflict-free), then one TMA store per 64 columns.
             // Before each refill the previous store must have finished reading.
             uint8_t *stg = y_stage + ew * C::kYBoxBytes;
-            const int row0 = w.a_row0 + 32 * quarter;
 #pragma unroll
             for (int bx = 0; bx < C::kCPT / C::kYBoxCols; ++bx) {
               if (lane == 0) bulk_wait_group_read0();
@@ -720,12 +805,12 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
               }
               fence_proxy_async_smem();
               __syncwarp();
-              if (lane == 0 && row0 < args.M && nbase + bx * C::kYBoxCols < args.N) {
+              if (lane == 0 && row0 < w.row_end && nbase + bx * C::kYBoxCols < args.N) {
                 tma_store_2d(&tmY, stg, nbase + bx * C::kYBoxCols, row0);
                 bulk_commit_group();
               }
             }
-          } else if (m < args.M) {
+          } else if (m < w.row_end) {
             store_row<C::kCPT>(y, acc, m, nbase, args);
           }
         } else {
@@ -740,7 +825,7 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
           const uint32_t tbase = tmem_base + lane_base + b * BN + col0;
           // the activation factor: the per-tensor scale, or this row's token scale
           const float sxs = (MODE == kModeTensor) ? __ldg(args.sx_scalar)
-                            : (MODE == kModeChannel) ? (m < args.M ? __ldg(args.sx + m) : 0.0f)
+                            : (MODE == kModeChannel) ? (m < w.row_end ? __ldg(args.sx + m) : 0.0f)
                                                      : 1.0f;
 #pragma unroll
           for (int c = 0; c < C::kCPT / C::kCW; ++c) {
@@ -781,7 +866,7 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
               }
               if (bias && n < args.N) v[j] += bf16_bits_to_float(bias[n]);
             }
-            if (m < args.M) store_row<C::kCW>(y, v, m, nbase + c * C::kCW, args);
+            if (m < w.row_end) store_row<C::kCW>(y, v, m, nbase + c * C::kCW, args);
           }
         }
       } else {
@@ -952,10 +1037,16 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
 // Launches one variant.  `grid` counts CTAs for single-CTA tiles and clusters
 // for pair tiles; for pair tiles it is clamped to the clusters the device can
 // hold at once, so the persistent grid is a single wave.
-template <int MODE, bool SWAP, int BN, int STAGES, int EPI_WARPS, int ACCB, bool PAIR>
+template <int MODE, bool SWAP, int BN, int STAGES, int EPI_WARPS, int ACCB, bool PAIR,
+          bool GROUPED = false>
 cudaError_t run(const GemmArgs &a, const void *q_act, const void *w, const LaunchShape &sh,
                 int grid, cudaStream_t st, int *status) {
-  using C = Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, PAIR>;
+  using C = Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, PAIR, GROUPED>;
+  static_assert(!GROUPED || (MODE == kModeBlock && !SWAP), "grouped: block tiles");
+  if (GROUPED != (a.g_experts > 0)) {
+    *status = 4;  // FP8BQ_ERR_UNSUPPORTED: grouped arguments to a plain variant or back
+    return cudaSuccess;
+  }
   CUtensorMap ta, tb, ty, tsx, tsw;
   std::memset(&ty, 0, sizeof ty);
   std::memset(&tsx, 0, sizeof tsx);
@@ -970,12 +1061,17 @@ cudaError_t run(const GemmArgs &a, const void *q_act, const void *w, const Launc
     // s_x: row-major [M][KB] in [128 rows x 4 K blocks] boxes, or column-major
     // [KB][ldsx] in [4 K blocks x 128 rows] boxes; s_w [NB][KB] in [2 x 4] boxes
     const int KB = (a.K + 127) / 128, NB = (a.N + kBlockN - 1) / kBlockN;
-    const bool sx_ok = al16(a.sx) && a.ldsx % 4 == 0 &&
+    // column-major s_x puts the token row on the box's inner coordinate, which
+    // must be a multiple of 4 floats: grouped tiles start at any row, so they
+    // take the per-thread path there
+    const bool sx_ok = al16(a.sx) && a.ldsx % 4 == 0 && (a.sx_layout == 0 || a.g_experts == 0) &&
                        (a.sx_layout == 0
                             ? cached_f32_map(&tsx, a.sx, a.M, KB, a.ldsx, C::kScQuad, kBM)
                             : cached_f32_map(&tsx, a.sx, KB, a.ldsx, a.ldsx, kBM, C::kScQuad));
+    const int experts = a.g_experts > 0 ? a.g_experts : 1;
     const bool sw_ok = al16(a.sw) && KB % 4 == 0 &&
-                       cached_f32_map(&tsw, a.sw, NB, KB, KB, C::kScQuad, 2);
+                       cached_f32_map(&tsw, a.sw, static_cast<int64_t>(NB) * experts, KB, KB,
+                                      C::kScQuad, 2);
     args.sc_tma = (sx_ok && sw_ok) ? 1 : 0;
   }
   if (MODE == kModeMx) {
@@ -993,22 +1089,33 @@ cudaError_t run(const GemmArgs &a, const void *q_act, const void *w, const Launc
   const void *a_ptr = SWAP ? w : q_act;
   const void *b_ptr = SWAP ? q_act : w;
   const int64_t a_rows = SWAP ? a.N : a.M;
-  const int64_t b_rows = SWAP ? a.M : a.N;
+  // grouped form: all experts' weights as one [E * N, K] operand
+  const int64_t b_rows = SWAP ? a.M : static_cast<int64_t>(a.N) * (a.g_experts > 0 ? a.g_experts : 1);
   if (!cached_kmajor_map(&ta, a_ptr, a_rows, a.K, kBM) ||
       !cached_kmajor_map(&tb, b_ptr, b_rows, a.K, C::kBrows)) {
     *status = 4;  // FP8BQ_ERR_UNSUPPORTED: tensor map rejected
     return cudaSuccess;
   }
   const size_t smem = C::kFixedSmem + static_cast<size_t>(sh.sx_stage) * sizeof(float);
-  auto kern = fp8_gemm_kernel<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, PAIR>;
-  // the opt-in shared-memory limit is raised once per variant (to the largest
-  // request it can see: the fixed part plus the biggest s_x staging buffer)
+  auto kern = fp8_gemm_kernel<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, PAIR, GROUPED>;
+  // the opt-in shared-memory limit is raised once per variant to the largest
+  // request it can see: the fixed part plus the biggest s_x staging buffer
+  // (swapped tiles) or, where it fits in 227 KB, the grouped form's tile table
+  // (pair tiles)
+  constexpr size_t kSmemCap = 227 * 1024;
+  constexpr size_t kTail = SWAP ? size_t(BN) * 64 * sizeof(float)
+                           : GROUPED ? kGroupTableBytes
+                                                                                     : 0;
+  static_assert(C::kFixedSmem + kTail <= kSmemCap, "shared memory");
+  if (smem > C::kFixedSmem + kTail) {
+    *status = 4;  // FP8BQ_ERR_UNSUPPORTED: the variant has no room for this request
+    return cudaSuccess;
+  }
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [&] {
-    const size_t max_smem = C::kFixedSmem + (SWAP ? size_t(BN) * 64 * sizeof(float) : 0);
     attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(max_smem));
+                                    static_cast<int>(C::kFixedSmem + kTail));
   });
   cudaError_t e = attr_err;
   if (e != cudaSuccess) return e;

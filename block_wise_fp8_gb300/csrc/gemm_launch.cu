@@ -177,7 +177,8 @@ WorkspaceLayout workspace_layout(int op, int64_t M, int64_t N, int64_t K) {
   size_t off = L.counters + up(static_cast<size_t>(NT) * 4);
   L.partials = off;
   const bool mx = (op == 2 || op == 3 || op == 8 || op == 9);  // MX GEMM (UE8M0 views too)
-  if (M <= 64 && !mx) off += up(static_cast<size_t>(kMaxSplits) * M * N * 4);
+  const bool grouped = (op == 10);  // pair tiles at every M: no split-K partials
+  if (M <= 64 && !mx && !grouped) off += up(static_cast<size_t>(kMaxSplits) * M * N * 4);
   L.q = off;
   const bool fused = (op == 1 || op == 3 || op == 5 || op == 7 || op == 9);
   if (fused) off += up(static_cast<size_t>(M) * K);
@@ -200,6 +201,36 @@ int launch_gemm(const GemmArgs &a, const void *q_act, const void *w, const Devic
   int status = 0;
   LaunchShape sh{};
   sh.KB = (a.K + 127) / 128;
+  if (a.g_experts > 0) {
+    // grouped (MoE) form: block tiles over the table each CTA builds from the
+    // segment bounds, m-tiles fastest (the tiles of one expert and weight tile
+    // run side by side and share it in L2).  Each segment rounds up to whole
+    // m-tiles, so with few rows per expert the padding decides the tensor
+    // work: 128-row single-CTA tiles while the mean segment is at most 512 rows
+    // (and always for the masked layout, whose slots are mostly unfilled),
+    // 256-row pair tiles above.  The host knows only a bound on the tile
+    // count, so the persistent grid covers that bound and CTAs without work
+    // leave at once.
+    if (a.mode != kModeBlock || a.g_experts > kMaxExperts) return 4;
+    const bool masked = a.g_offsets == nullptr;
+    const bool pair = !masked && a.M > 512L * a.g_experts;
+    const int rows = pair ? 256 : 128;
+    GemmArgs g = a;
+    // each segment has at most one ragged tile
+    g.g_tile_cap = masked ? a.g_experts * ((a.g_max_m + rows - 1) / rows)
+                          : a.g_experts + (a.M + rows - 1) / rows;
+    const int slots = pair ? dev.num_sms / 2 : dev.num_sms;
+    const long units_cap = static_cast<long>(g.g_tile_cap) * ((a.N + 255) / 256);
+    sh.num_a_tiles = 0;
+    sh.units = 0;
+    sh.splits = 1;
+    sh.kps = sh.KB;
+    sh.sx_stage = 3 * a.g_experts + 1;  // the table, in 4-byte words
+    const int grid = static_cast<int>(units_cap < slots ? units_cap : slots);
+    if (grid == 0) return 0;
+    *cuda_err = run_block_grouped(pair, g, q_act, w, sh, grid, st, &status);
+    return status;
+  }
   const bool swap = (a.mode != kModeMx) && a.M <= 64;
   if (swap) {
     // decode: weight rows on the MMA's M side, tokens on its N side, K split so

@@ -19,8 +19,10 @@
  *   拆解(十九)", §激活量化的三种选择 and "[SGLang] FP8" §5), a channelwise
  *   variant (per-token x per-channel scales; §一条 GEMM 的三种缩放组合), block
  *   FP8 with power-of-two (UE8M0) scales run on the block-scaled MMA
- *   (§分块 GEMM 的后端分派), and the residual add + RMSNorm that precedes the
- *   activation quantiser, fused with it ("GLM-5.3 推理全链路(十七)", §第1站).
+ *   (§分块 GEMM 的后端分派), the residual add + RMSNorm that precedes the
+ *   activation quantiser, fused with it ("GLM-5.3 推理全链路(十七)", §第1站),
+ *   and the grouped (MoE) block GEMM over experts' weights [E, N, K]
+ *   ("SGLang 源码完全拆解(十九)", §MoE:专家权重多一个维度).
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -96,7 +98,8 @@ enum {
   FP8BQ_OP_CHANNEL_GEMM = 6,
   FP8BQ_OP_CHANNEL_LINEAR = 7,
   FP8BQ_OP_UE8M0_GEMM = 8,
-  FP8BQ_OP_UE8M0_LINEAR = 9
+  FP8BQ_OP_UE8M0_LINEAR = 9,
+  FP8BQ_OP_GROUPED_GEMM = 10 /* both grouped forms; M = rows of A and Y in all */
 };
 
 /* ---------------------------------------------------------------- utility */
@@ -325,6 +328,50 @@ FP8BQ_API int fp8bq_ue8m0_linear(const void *x, int64_t ldx, const void *w,
                                  const uint8_t *u_w, const void *bias, void *y,
                                  int64_t M, int64_t N, int64_t K, void *ws,
                                  size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------ grouped (MoE) block FP8 */
+
+/* Block-scaled FP8 GEMM over E experts at once ("SGLang 源码完全拆解(十九)",
+ * §MoE:专家权重多一个维度: expert weights carry a leading expert dimension,
+ * w [E, N, K] with one FP32 128 x 128 scale grid per expert, s_w
+ * [E][ceil(N/128)][ceil(K/128)]; the grouped GEMM takes the activation rows
+ * sorted by expert, a contiguous layout that the dispatch step produces).
+ * Rows offsets[e] .. offsets[e+1]-1 of q, s_x and y belong to expert e:
+ *
+ *   y[i][j] = BF16(sum_b P_b * s_x[i][b] * s_w[e][j/128][b]),  e the expert of row i,
+ *
+ * with the arithmetic of fp8bq_gemm.  q: E4M3 [M, K] (the M sorted rows);
+ * s_x: FP32 [M][ceil(K/128)] or column-major [ceil(K/128)][round_up(M,4)];
+ * y: BF16 [M, N].  offsets: DEVICE int32 [E+1], non-decreasing, offsets[0] >= 0,
+ * offsets[E] <= M; it is read by the kernel (written, e.g., by a routing
+ * kernel earlier on the stream), so the host never synchronises.  Rows outside
+ * every segment are not written.  Bounds outside [0, M] are clamped on the
+ * device; decreasing offsets make overlapping segments, whose rows then get
+ * unspecified values (nothing outside q, s_x, w, s_w, y is accessed).
+ * 1 <= E <= 1024, E * N < 2^31.  No bias (the pages' expert weights carry
+ * none).  For a fused gate/up weight with intermediate size I_p per shard the
+ * scale rows follow j/128, which is the pages' per-shard rounding when I_p is a
+ * multiple of 128; otherwise pad each shard to a multiple of 128 rows.
+ * Workspace: fp8bq_workspace_bytes(FP8BQ_OP_GROUPED_GEMM, M, N, K). */
+FP8BQ_API int fp8bq_grouped_gemm(const void *q, const float *s_x, int s_layout,
+                                 const void *w, const float *s_w,
+                                 const int32_t *offsets, int64_t E, void *y,
+                                 int64_t M, int64_t N, int64_t K, void *ws,
+                                 size_t ws_bytes, void *stream);
+
+/* The masked form of the same GEMM: A is [E, max_m, K] (rows e * max_m ..
+ * e * max_m + masked_m[e] - 1 are expert e's, the rest of each slot unused),
+ * y [E, max_m, N], s_x over the E * max_m rows as above.  masked_m: DEVICE
+ * int32 [E], each clamped to [0, max_m] on the device.  Unused rows are not
+ * written.  Workspace: fp8bq_workspace_bytes(FP8BQ_OP_GROUPED_GEMM,
+ * E * max_m, N, K). */
+FP8BQ_API int fp8bq_grouped_gemm_masked(const void *q, const float *s_x,
+                                        int s_layout, const void *w,
+                                        const float *s_w,
+                                        const int32_t *masked_m, int64_t E,
+                                        int64_t max_m, void *y, int64_t N,
+                                        int64_t K, void *ws, size_t ws_bytes,
+                                        void *stream);
 
 /* ------------------------------------------------ weight / calibration set-up */
 

@@ -8,7 +8,8 @@ Recipe (identical on every machine that runs the same numpy):
   * splitmix64 as a counter-based generator: output i of stream s is
     mix64(seed_s + (i + 1) * 0x9E3779B97F4A7C15), seed_s = base_seed + s.
     Streams: 0 = activations X, 1 = weights W, 2 = calibration batch,
-    3 = outlier-channel pick, 4 = residual stream, 5 = norm gains.
+    3 = outlier-channel pick, 4 = residual stream, 5 = norm gains,
+    6 = MoE routing.
   * uniform u = (z >> 11) * 2^-53; normal by Box-Muller (cosine branch), element
     e using outputs 2e and 2e+1: sqrt(-2 ln(1 - u0)) * cos(2 pi u1).
   * value = sigma * normal, times `outlier_scale` on the outlier channels, then
@@ -18,6 +19,11 @@ Recipe (identical on every machine that runs the same numpy):
   * residual stream: sigma 4, the outlier channels x20 (the large channels of
     a transformer's residual stream); norm gains: exp(0.5 * normal), a
     positive log-normal spread around 1.
+  * MoE routing (rows per local expert): T routed rows each pick expert
+    perm[r] with probability proportional to (r + 1)^-skew, r the inverse-CDF
+    rank of a stream-6 uniform and perm a Fisher-Yates shuffle of the experts
+    driven by the same stream (after the T row draws); skew 0.5 gives hot
+    experts at about 3x the mean load and cold ones at about 0.5x.
 
 BF16 tensors are returned as numpy.uint16 bit patterns, row-major.
 """
@@ -34,6 +40,7 @@ _M2 = np.uint64(0x94D049BB133111EB)
 
 STREAM_X, STREAM_W, STREAM_CALIB, STREAM_OUTLIER = 0, 1, 2, 3
 STREAM_RES, STREAM_GAIN = 4, 5
+STREAM_ROUTE = 6
 
 
 def _mix64(z: np.ndarray) -> np.ndarray:
@@ -167,6 +174,21 @@ def norm_gain(K: int, base_seed: int = 0) -> np.ndarray:
     return f32_to_bf16_bits(np.exp(0.5 * z).astype(np.float32))
 
 
+def expert_counts(T: int, E: int, skew: float = 0.5, base_seed: int = 0) -> np.ndarray:
+    """Rows per expert (int64 [E], summing to T) for T routed rows."""
+    seed = base_seed + STREAM_ROUTE
+    p = np.arange(1, E + 1, dtype=np.float64) ** -skew
+    cdf = np.cumsum(p / p.sum())
+    u = _uniform(splitmix64(seed, 0, T))
+    rank = np.minimum(np.searchsorted(cdf, u, side="right"), E - 1)
+    perm = np.arange(E)
+    z = splitmix64(seed, T, E)
+    for i in range(E - 1, 0, -1):
+        j = int(z[i] % np.uint64(i + 1))
+        perm[i], perm[j] = perm[j], perm[i]
+    return np.bincount(perm[rank], minlength=E).astype(np.int64)
+
+
 # Shapes of the five workloads.
 TINY = dict(M=16, K=256, N=384)
 DECODE = dict(K=6144, N=6144, M_list=(1, 8, 32, 64))
@@ -177,3 +199,7 @@ MXFP8 = dict(M=2048, K=7168, N=4096)
 NORM = dict(M_list=(1, 512, 4096), K_list=(6144, 4096), eps=1e-5)
 STATIC = dict(M_list=(1, 512, 4096), K=4096, N=14336, parts=(4096, 4096, 6144),
               calib_rows=256)
+# grouped (MoE) experts: hidden size H, intermediate size I per expert, E local
+# experts (256 routed experts over 8 expert-parallel ranks), T routed rows per
+# rank; w13 is [E, 2I, H] (N = 2I, K = H), w2 is [E, H, I] (N = H, K = I)
+MOE = dict(E=32, H=7168, I=2048, T=4096, skew=0.5)

@@ -137,3 +137,39 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
             importlib.import_module("block_wise_fp8_gb300")
     finally:
         sys.modules["block_wise_fp8_gb300"] = saved
+
+
+def test_grouped_gemm_validation():
+    """Both grouped forms reject bad arguments before any CUDA call."""
+    ws_small = 256
+    ok = dict(q=P(A), sx=P(A), lay=0, w=P(A), sw=P(A), off=P(A), E=4, y=P(A), M=512, N=256,
+              K=256, ws=P(A), wsb=1 << 20, st=None)
+    call = lambda d: L.fp8bq_grouped_gemm(d["q"], d["sx"], d["lay"], d["w"], d["sw"], d["off"],
+                                          d["E"], d["y"], d["M"], d["N"], d["K"], d["ws"],
+                                          d["wsb"], d["st"])
+    assert call({**ok, "off": None}) == 1
+    assert call({**ok, "w": None}) == 1
+    assert call({**ok, "E": 0}) == 2
+    assert call({**ok, "E": 1025}) == 2
+    assert call({**ok, "E": 1 << 20, "N": 1 << 12}) == 2
+    assert call({**ok, "K": 200}) == 3
+    assert call({**ok, "off": P(A + 2)}) == 3
+    assert call({**ok, "y": P(A + 8)}) == 3
+    assert call({**ok, "lay": 5}) == 4
+    assert call({**ok, "wsb": ws_small - 1}) == 6
+    assert call({**ok, "ws": None}) == 6
+    assert call({**ok, "M": 0}) == 0                     # nothing to compute
+    assert fb.fp8bq_workspace_bytes(fb.OP_GROUPED_GEMM, 512, 256, 256) <= 1 << 20
+    # no split-K partials at small row counts: the grouped form always uses pair tiles
+    assert fb.fp8bq_workspace_bytes(fb.OP_GROUPED_GEMM, 8, 6144, 6144) < 8 * 6144 * 4
+
+    okm = dict(q=P(A), sx=P(A), lay=0, w=P(A), sw=P(A), mm=P(A), E=4, max_m=128, y=P(A), N=256,
+               K=256, ws=P(A), wsb=1 << 20, st=None)
+    callm = lambda d: L.fp8bq_grouped_gemm_masked(d["q"], d["sx"], d["lay"], d["w"], d["sw"],
+                                                  d["mm"], d["E"], d["max_m"], d["y"], d["N"],
+                                                  d["K"], d["ws"], d["wsb"], d["st"])
+    assert callm({**okm, "mm": None}) == 1
+    assert callm({**okm, "max_m": -1}) == 2
+    assert callm({**okm, "E": 2000}) == 2
+    assert callm({**okm, "E": 2, "max_m": 1 << 31}) == 2   # E * max_m overflows 32 bits
+    assert callm({**okm, "max_m": 0}) == 0
