@@ -16,8 +16,11 @@ Also reported, measured in the same run:
                inside the timed region;
   extra        decode (M in {1,8,32,64}), quantiser and fused residual-add +
                RMSNorm + quantisation GB/s against HBM, MXFP8, static
-               per-tensor, channelwise and block-with-UE8M0 TFLOPS;
+               per-tensor, channelwise and block-with-UE8M0 TFLOPS, and the
+               grouped (MoE) GEMM against its HBM / FP8 roofline;
   cpu_baseline the CPU oracle on a bounded sample of the same workload.
+`--profile-case <case>` runs only a few launches of one kernel (MXFP8, UE8M0,
+channelwise GEMM, norm + quantisation, grouped w13 / w2) for ncu captures.
 
 L2 is flushed (256 MiB write) between timed steps; every step is timed with
 CUDA events on the launching stream, synchronised on both sides.
@@ -58,8 +61,8 @@ FP8_PER_BF16 = 2.0   # nominal dense FP8 / BF16 tensor rate
 # digest is recorded; anything else reports null.
 NCU_TRAFFIC = {
     # profiles/block_gemm_prefill_4096x24576x6144.md (N = 24576 launch)
-    "source_sha256": "4ae53f595a1dc7f5cbc29b5803fd598cd952b385c327e60650bf60927e4476e9",
-    "bytes_per_launch": 191881984 + 176778496,
+    "source_sha256": "f5c1767be033c0eb28144da5d4bf0f44080329f4cf0fe7dddb55304a32e88bbf",
+    "bytes_per_launch": 189151488 + 177110016,
 }
 
 
@@ -749,6 +752,78 @@ def run_reference(args):
     }), flush=True)
 
 
+PROFILE_CASES = ("mx", "norm_group", "norm_static", "grouped_w13", "grouped_w2", "channel",
+                 "ue8m0")
+
+
+def run_profile_case(case: str, launches: int = 3):
+    """A few launches of one kernel at its workload shape and nothing else, for
+    an ncu capture (no timing, no JSON line).  Operand values are random codes
+    and scales drawn on the device: counters do not depend on them."""
+    import torch
+    sys.path.insert(0, ROOT)
+    import block_wise_fp8_gb300 as fb
+    dev = torch.device("cuda")
+    torch.manual_seed(0)
+    codes = lambda *shape: torch.randint(0, 0x7E, shape, dtype=torch.uint8, device=dev)
+    if case in ("mx", "ue8m0"):
+        M, K, N = (si.MXFP8["M"], si.MXFP8["K"], si.MXFP8["N"]) if case == "mx" else \
+                  (PREFILL_M, PREFILL_K, PREFILL_NS[1])
+        G = K // 32 if case == "mx" else K // 128
+        q, w = codes(M, K), codes(N, K)
+        u = torch.randint(120, 130, (M, G), dtype=torch.uint8, device=dev)
+        uw = torch.randint(120, 130, (N if case == "mx" else N // 128, G), dtype=torch.uint8,
+                           device=dev)
+        y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        op = fb.OP_MX_GEMM if case == "mx" else fb.OP_UE8M0_GEMM
+        ws = fb.new_workspace(op, M, N, K, device=dev)
+        fn = (lambda: fb.fp8bq_mx_gemm(q, u, w, uw, y, ws)) if case == "mx" else \
+             (lambda: fb.fp8bq_ue8m0_gemm(q, u, w, uw, y, ws))
+    elif case == "channel":
+        M, K, N = PREFILL_M, PREFILL_K, PREFILL_NS[1]
+        q, w = codes(M, K), codes(N, K)
+        sx = torch.rand(M, device=dev) + 0.5
+        sw = torch.rand(N, device=dev) * 1e-3
+        y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        ws = fb.new_workspace(fb.OP_CHANNEL_GEMM, M, N, K, device=dev)
+        fn = lambda: fb.fp8bq_channel_gemm(q, sx, w, sw, y, ws)
+    elif case.startswith("norm"):
+        static = case == "norm_static"
+        M, K = (4096, 4096) if static else (4096, 6144)
+        to_dev = lambda b: torch.from_numpy(b.view(np.int16)).to(dev).view(torch.bfloat16)
+        x, r = to_dev(si.activations(M, K)), to_dev(si.residual_stream(M, K))
+        g = to_dev(si.norm_gain(K))
+        ro = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
+        q = torch.empty(M, K, dtype=torch.uint8, device=dev)
+        eps = si.NORM["eps"]
+        if static:
+            s_n = torch.full((1,), 0.05, dtype=torch.float32, device=dev)
+            fn = lambda: fb.fp8bq_add_rmsnorm_static_quant_act(x, g, eps, s_n, q, residual=r,
+                                                               residual_out=ro)
+        else:
+            s = torch.empty(M, K // 128, dtype=torch.float32, device=dev)
+            fn = lambda: fb.fp8bq_add_rmsnorm_quant_act(x, g, eps, residual=r, residual_out=ro,
+                                                        q=q, s=s)
+    elif case.startswith("grouped"):
+        mo = si.MOE
+        E, T = mo["E"], mo["T"]
+        N, K = (2 * mo["I"], mo["H"]) if case == "grouped_w13" else (mo["H"], mo["I"])
+        counts = si.expert_counts(T, E, mo["skew"])
+        off = torch.tensor(np.concatenate([[0], np.cumsum(counts)]).astype(np.int32), device=dev)
+        qw, qa = codes(E, N, K), codes(T, K)
+        sw = torch.rand(E, N // 128, K // 128, device=dev) * 1e-3
+        sa = torch.rand(T, K // 128, device=dev) + 0.5
+        y = torch.empty(T, N, dtype=torch.bfloat16, device=dev)
+        ws = fb.new_workspace(fb.OP_GROUPED_GEMM, T, N, K, device=dev)
+        fn = lambda: fb.fp8bq_grouped_gemm(qa, sa, qw, sw, off, y, ws)
+    else:
+        raise SystemExit(f"unknown profile case {case}")
+    for _ in range(launches):
+        fn()
+    torch.cuda.synchronize()
+    print(f"profile case {case}: {launches} launches", file=sys.stderr)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -759,7 +834,12 @@ def main(argv=None):
     ap.add_argument("--ref-rows", type=int, default=2)
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--profile-case", choices=PROFILE_CASES,
+                    help="only run a few launches of one kernel (for ncu captures)")
     args = ap.parse_args(argv)
+    if args.profile_case:
+        run_profile_case(args.profile_case)
+        return
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     if args.impl == "reference":
