@@ -252,10 +252,17 @@ __device__ __forceinline__ Unit decode_unit(int u, int num_a_tiles, int splits, 
   r.expert = 0;
   if (!SWAP) {
     // A = tokens (256 per pair tile, 128 per CTA), B = bn weight rows (pair
-    // tiles: bn/2 per CTA); M fastest so concurrently running tiles share
-    // weight tiles in L2
+    // tiles: bn/2 per CTA).  Plain GEMMs walk M fastest, so concurrently
+    // running tiles share the (large) weight tiles in L2.  Grouped GEMMs walk
+    // the weight tiles fastest: a wave then covers all weight tiles of a few
+    // m-tiles, so each m-tile's activation rows and the weight tiles of an
+    // expert's consecutive m-tiles are shared by tiles running side by side,
+    // rather than re-read from DRAM every wave as the weight stream evicts
+    // them
     constexpr int kTileRows = PAIR ? 2 * kBM : kBM;
-    const int mt = u % num_a_tiles, nt = u / num_a_tiles;
+    const int n_tiles = (N + bn - 1) / bn;
+    const int mt = GROUPED ? u / n_tiles : u % num_a_tiles;
+    const int nt = GROUPED ? u - mt * n_tiles : u / num_a_tiles;
     r.tile = u;
     r.split = 0;
     int row0 = mt * kTileRows;

@@ -203,8 +203,8 @@ int launch_gemm(const GemmArgs &a, const void *q_act, const void *w, const Devic
   sh.KB = (a.K + 127) / 128;
   if (a.g_experts > 0) {
     // grouped (MoE) form: block tiles over the table each CTA builds from the
-    // segment bounds, m-tiles fastest (the tiles of one expert and weight tile
-    // run side by side and share it in L2).  Each segment rounds up to whole
+    // segment bounds, weight tiles fastest (the tiles of one m-tile run side by
+    // side and share its activation rows in L2).  Each segment rounds up to whole
     // m-tiles, so with few rows per expert the padding decides the tensor
     // work: 128-row single-CTA tiles while the mean segment is at most 512 rows
     // (and always for the masked layout, whose slots are mostly unfilled),
