@@ -16,8 +16,10 @@ Also reported, measured in the same run:
                inside the timed region;
   extra        decode (M in {1,8,32,64}), quantiser and fused residual-add +
                RMSNorm + quantisation GB/s against HBM, MXFP8, static
-               per-tensor, channelwise and block-with-UE8M0 TFLOPS, and the
-               grouped (MoE) GEMM against its HBM / FP8 roofline;
+               per-tensor, channelwise and block-with-UE8M0 TFLOPS, the
+               grouped (MoE) GEMM against its HBM / FP8 roofline, and as
+               context the vendor's plain per-tensor FP8 GEMM (cuBLASLt via
+               torch._scaled_mm), which has no block scales to promote;
   cpu_baseline the CPU oracle on a bounded sample of the same workload.
 `--profile-case <case>` runs only a few launches of one kernel (MXFP8, UE8M0,
 channelwise GEMM, norm + quantisation, grouped w13 / w2) for ncu captures.
@@ -173,6 +175,11 @@ class ClockSampler:
 # our arm
 # ---------------------------------------------------------------------------
 
+def pcts(v):
+    """10th, 50th and 90th percentile of a list of times (ms)."""
+    return [round(float(x), 4) for x in np.percentile(np.asarray(v, np.float64), [10, 50, 90])]
+
+
 def run_ours(args):
     import torch
     world, rank, local = dist_env()
@@ -250,9 +257,11 @@ def run_ours(args):
             ends[i].record(stream)
         torch.cuda.synchronize()
         barrier(world)
-    ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends))
-    gemm_ms = [sum(gev[i][j][0].elapsed_time(gev[i][j][1]) for i in range(args.steps))
-               / args.steps for j in range(len(layers))]
+    step_list = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = sum(step_list)
+    gemm_lists = [[gev[i][j][0].elapsed_time(gev[i][j][1]) for i in range(args.steps)]
+                  for j in range(len(layers))]
+    gemm_ms = [sum(g) / args.steps for g in gemm_lists]
     for L in layers:
         if fb.fp8bq_poll_status(L["ws"]) != 0:
             raise RuntimeError("device wait timed out in the timed region")
@@ -269,7 +278,8 @@ def run_ours(args):
                 "unit": "TFLOP/s", "frac": round(achieved / fp8_peak, 4), "traffic": traffic,
                 "kernel": f"block-scaled GEMM {M}x{layers[j]['N']}x{K}",
                 "peak_source": f"{peak_src}: 2 x bf16 burst {peaks['bf16_tflops']} TFLOP/s",
-                "gemm_ms": {str(L["N"]): round(t, 4) for L, t in zip(layers, gemm_ms)}}
+                "gemm_ms": {str(L["N"]): round(t, 4) for L, t in zip(layers, gemm_ms)},
+                "gemm_ms_p10_p50_p90": {str(L["N"]): pcts(g) for L, g in zip(layers, gemm_lists)}}
 
     # ---- e2e through fp8bq_linear with host buffers
     e2e = run_e2e(fb, torch, dev, stream, layers, x, args, world, rank)
@@ -292,6 +302,7 @@ def run_ours(args):
                    "l2": "flushed between timed steps (256 MiB write)"},
         "roofline": roofline,
         "e2e": e2e,
+        "step_ms_p10_p50_p90": pcts(step_list),
         "gpu_launches": 3 * args.steps,
         "clocks": clk.summary(),
         "extra": extra,
@@ -390,6 +401,25 @@ def _time_graph(torch, fns, per_graph, reps=20):
 
 def _copies(t, n):
     return [t] + [t.clone() for _ in range(n - 1)]
+
+
+def vendor_fp8_reference(torch, dev, stream, fp8_peak):
+    res = {"what": "torch._scaled_mm (cuBLASLt), E4M3 x E4M3, per-tensor FP32 scales, BF16 out"}
+    try:
+        for name, (M, N, K) in (("prefill_4096x24576x6144", (PREFILL_M, PREFILL_NS[1], PREFILL_K)),
+                                ("square_8192", (8192, 8192, 8192))):
+            a = torch.randint(0, 0x7E, (M, K), dtype=torch.uint8, device=dev).view(torch.float8_e4m3fn)
+            b = torch.randint(0, 0x7E, (N, K), dtype=torch.uint8, device=dev).view(torch.float8_e4m3fn)
+            one = torch.ones((), dtype=torch.float32, device=dev)
+            f = lambda: torch._scaled_mm(a, b.t(), scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+            t = _time_back_to_back(torch, stream, [f], 20)
+            tf = 2.0 * M * N * K / (t * 1e-3) / 1e12
+            res[name] = {"us": round(t * 1e3, 2), "tflops": round(tf, 1),
+                         "frac_fp8": round(tf / fp8_peak, 4)}
+            del a, b
+    except Exception as e:  # noqa: BLE001 - context figure only
+        res["unavailable"] = f"{type(e).__name__}: {str(e)[:160]}"
+    return res
 
 
 def run_extra(fb, torch, dev, stream, hbm_peak, fp8_peak):
@@ -646,6 +676,11 @@ def run_extra(fb, torch, dev, stream, hbm_peak, fp8_peak):
                                     "frac_roofline": round(t_min / (t * 1e-3), 4)}
         del qw, sw, qa, sa, y
     out["grouped_moe"] = gr
+
+    # context only (not a denominator): the vendor's plain FP8 GEMM with
+    # per-tensor scales (cuBLASLt through torch._scaled_mm) at the prefill shape
+    # and at 8192^3; it has no per-block promotion to do
+    out["vendor_fp8_gemm"] = vendor_fp8_reference(torch, dev, stream, fp8_peak)
 
     # residual add + RMSNorm + quantisation (the step before the linear):
     # x, residual in; updated residual, E4M3 codes (and group scales) out

@@ -28,6 +28,7 @@ __all__ = [
     "OP_UE8M0_GEMM", "OP_UE8M0_LINEAR", "fp8bq_quant_act_ue8m0", "fp8bq_requant_weight_ue8m0",
     "fp8bq_ue8m0_gemm", "fp8bq_ue8m0_linear",
     "OP_GROUPED_GEMM", "fp8bq_grouped_gemm", "fp8bq_grouped_gemm_masked",
+    "fp8bq_check_scales",
     "library_path",
     "fp8bq_version", "fp8bq_status_string", "fp8bq_last_cuda_error",
     "fp8bq_workspace_bytes", "fp8bq_workspace_init", "fp8bq_poll_status",
@@ -93,6 +94,7 @@ def _load():
         "fp8bq_ue8m0_gemm": (I32, [P, P, P, P, P, P, I64, I64, I64, P, SZ, P]),
         "fp8bq_ue8m0_linear": (I32, [P, I64, P, P, P, P, I64, I64, I64, P, SZ, P]),
         "fp8bq_grouped_gemm": (I32, [P, P, I32, P, P, P, I64, P, I64, I64, I64, P, SZ, P]),
+        "fp8bq_check_scales": (I32, [P, I64, P, P, P, P]),
         "fp8bq_grouped_gemm_masked": (I32, [P, P, I32, P, P, P, I64, I64, P, I64, I64, P, SZ,
                                             P]),
         "fp8bq_channel_gemm": (I32, [P, P, P, P, P, P, I64, I64, I64, P, SZ, P]),
@@ -309,6 +311,21 @@ def fp8bq_ue8m0_linear(x, w, u_w, y, ws, bias=None, stream=None):
     _check(_lib.fp8bq_ue8m0_linear(_ptr(x), _ld(x), _ptr(w), _ptr(u_w), _ptr(bias), _ptr(y),
                                    M, N, K, _ptr(ws), _nbytes(ws), _stream(stream)),
            "fp8bq_ue8m0_linear")
+
+
+def fp8bq_check_scales(s, scratch=None, stream=None) -> dict:
+    """Counts unusable FP32 scales in a device tensor: the unloaded sentinel
+    (-FLT_MAX), NaN / inf, other values <= 0; and the first bad flat index."""
+    if scratch is None:
+        scratch = torch.empty(4, dtype=torch.int64, device=s.device)
+    counts = (ctypes.c_int64 * 3)()
+    first = ctypes.c_int64()
+    _check(_lib.fp8bq_check_scales(_ptr(s), s.numel(), _ptr(scratch),
+                                   ctypes.c_void_p(ctypes.addressof(counts)),
+                                   ctypes.c_void_p(ctypes.addressof(first)), _stream(stream)),
+           "fp8bq_check_scales")
+    return {"sentinel": counts[0], "nonfinite": counts[1], "nonpositive": counts[2],
+            "first_bad": first.value}
 
 
 # ---------------------------------------------------------------- grouped (MoE)

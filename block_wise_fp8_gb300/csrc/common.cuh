@@ -70,6 +70,11 @@ void launch_quant_weight_block(const void *w, int64_t N, int64_t K, int64_t ldw,
                                float *s, cudaStream_t st);
 void launch_absmax_scale(const void *x, int64_t rows, int64_t K, int64_t ldx, float *s,
                          int num_sms, cudaStream_t st);
+// Counts unusable FP32 scales (out[0] the sentinel -FLT_MAX, out[1] NaN / inf,
+// out[2] other values <= 0) and the smallest bad index (out[3]; above every
+// index when there is none).  `out` is device memory of 4 words.
+void launch_check_scales(const float *s, int64_t n, unsigned long long *out, int num_sms,
+                         cudaStream_t st);
 
 // ---------------------------------------------------------------- GEMM
 

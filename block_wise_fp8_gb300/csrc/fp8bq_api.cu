@@ -614,6 +614,33 @@ int fp8bq_absmax_scale(const void *x, int64_t rows, int64_t K, int64_t ldx, floa
   return e == cudaSuccess ? FP8BQ_OK : cuda_fail(e);
 }
 
+int fp8bq_check_scales(const float *s, int64_t n, void *scratch, int64_t *counts_host,
+                       int64_t *first_bad_host, void *stream) {
+  if (!counts_host || !first_bad_host) return FP8BQ_ERR_NULL;
+  if (n < 0) return FP8BQ_ERR_SHAPE;
+  if (n > 0 && (!s || !scratch)) return FP8BQ_ERR_NULL;
+  if (!aligned(s, 4) || !aligned(scratch, 8)) return FP8BQ_ERR_ALIGN;
+  if (n == 0) {
+    counts_host[0] = counts_host[1] = counts_host[2] = 0;
+    *first_bad_host = -1;
+    return FP8BQ_OK;
+  }
+  DeviceInfo dev;
+  RETURN_IF(device_info(&dev));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  unsigned long long *out = static_cast<unsigned long long *>(scratch);
+  launch_check_scales(s, n, out, dev.num_sms, st);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e);
+  unsigned long long h[4];
+  e = cudaMemcpyAsync(h, out, sizeof h, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e);
+  for (int k = 0; k < 3; ++k) counts_host[k] = static_cast<int64_t>(h[k]);
+  *first_bad_host = h[3] < static_cast<unsigned long long>(n) ? static_cast<int64_t>(h[3]) : -1;
+  return FP8BQ_OK;
+}
+
 // ------------------------------------------------------------------ no-allocation GEMM
 
 // fp8bq_gemm with the library's fixed scratch array in place of a caller

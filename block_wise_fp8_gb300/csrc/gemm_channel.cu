@@ -6,8 +6,8 @@ namespace fp8bq {
 
 cudaError_t run_channel_pair(int bn, const GemmArgs &a, const void *q, const void *w,
                              const LaunchShape &sh, int grid, cudaStream_t st, int *status) {
-  if (bn == 192) return run<kModeChannel, false, 192, 7, 8, 2, true>(a, q, w, sh, grid, st, status);
-  return run<kModeChannel, false, 256, 6, 8, 2, true>(a, q, w, sh, grid, st, status);
+  if (bn == 192) return run<kModeChannel, false, 192, 8, 8, 2, true>(a, q, w, sh, grid, st, status);
+  return run<kModeChannel, false, 256, 7, 8, 2, true>(a, q, w, sh, grid, st, status);
 }
 
 cudaError_t run_channel_swap(int bn, const GemmArgs &a, const void *q, const void *w,

@@ -8,6 +8,8 @@
 // 基本公式; "GLM-5.3 推理全链路(十七)", §第1站, s_g = max|x|/448, q = round(x/s_g)).
 #include <cuda_fp8.h>
 
+#include <climits>
+
 #include "common.cuh"
 #include "ptx.cuh"
 #include "quant_math.cuh"
@@ -396,6 +398,43 @@ __global__ void __launch_bounds__(kThreads) requant_ue8m0_kernel(const uint8_t *
   }
 }
 
+// Scale check: per entry, the class of an unusable dequantisation multiplier
+// (the unloaded sentinel -FLT_MAX, NaN or infinity, any other value <= 0);
+// counts added into out[0..2], the smallest bad index min-ed into out[3].
+__global__ void __launch_bounds__(kThreads) check_scales_kernel(const float *__restrict__ s,
+                                                                 int64_t n,
+                                                                 unsigned long long *out) {
+  griddep_launch_dependents();
+  griddep_wait();
+  unsigned long long c[3] = {0, 0, 0};
+  long long first = LLONG_MAX;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += stride) {
+    const float v = s[i];
+    const uint32_t b = __float_as_uint(v);
+    const bool sentinel = b == 0xff7fffffu;
+    const bool nonfinite = (b & 0x7f800000u) == 0x7f800000u;
+    const bool nonpositive = !sentinel && !nonfinite && !(v > 0.0f);
+    c[0] += sentinel;
+    c[1] += nonfinite;
+    c[2] += nonpositive;
+    if ((sentinel || nonfinite || nonpositive) && i < first) first = i;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+    for (int k = 0; k < 3; ++k) c[k] += __shfl_xor_sync(0xffffffffu, c[k], o);
+    first = min(first, __shfl_xor_sync(0xffffffffu, first, o));
+  }
+  if ((threadIdx.x & 31) == 0) {
+#pragma unroll
+    for (int k = 0; k < 3; ++k)
+      if (c[k]) atomicAdd(out + k, c[k]);
+    if (first != LLONG_MAX) atomicMin(reinterpret_cast<long long *>(out + 3), first);
+  }
+}
+
 inline unsigned blocks_for(int64_t work, int per_block) {
   return static_cast<unsigned>((work + per_block - 1) / per_block);
 }
@@ -474,6 +513,18 @@ void launch_requant_ue8m0(const void *q, const float *s, int64_t N, int64_t K, v
   const int NB = static_cast<int>((N + 127) / 128);
   launch_pdl(requant_ue8m0_kernel, dim3(KB, NB), kThreads, 0, st, static_cast<const uint8_t *>(q), s,
              static_cast<int>(N), static_cast<int>(K), KB, static_cast<uint8_t *>(q2), u);
+}
+
+void launch_check_scales(const float *s, int64_t n, unsigned long long *out, int num_sms,
+                         cudaStream_t st) {
+  // counts to 0, first index to 0x7f7f7f7f7f7f7f7f (above any index)
+  cudaMemsetAsync(out, 0, 3 * sizeof(unsigned long long), st);
+  cudaMemsetAsync(out + 3, 0x7f, sizeof(unsigned long long), st);
+  unsigned grid = blocks_for(n, kThreads * 4);
+  const unsigned cap = static_cast<unsigned>(num_sms) * 4u;
+  if (grid > cap) grid = cap;
+  if (grid == 0) grid = 1;
+  launch_pdl(check_scales_kernel, grid, kThreads, 0, st, s, n, out);
 }
 
 void launch_absmax_scale(const void *x, int64_t rows, int64_t K, int64_t ldx, float *s,

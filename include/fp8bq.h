@@ -387,6 +387,24 @@ FP8BQ_API int fp8bq_quant_weight_block(const void *w, int64_t N, int64_t K,
 FP8BQ_API int fp8bq_absmax_scale(const void *x, int64_t rows, int64_t K,
                                  int64_t ldx, float *s, void *stream);
 
+/* Debug helper for scales that come from outside the library (a checkpoint,
+ * a caller's calibration): classifies the entries of a device FP32 scale array
+ * that are not usable dequantisation multipliers.  "SGLang 源码完全拆解(十九)",
+ * §scale 的初始值不是零: every scale is registered at the sentinel
+ * torch.finfo(float32).min and only a checkpoint entry overwrites it, so a
+ * scale still holding the sentinel was never loaded.
+ *   counts_host[0]  entries equal to the sentinel -FLT_MAX (bits 0xff7fffff)
+ *   counts_host[1]  NaN or infinite entries
+ *   counts_host[2]  other entries <= 0 (zero, -0 or negative multipliers)
+ *   *first_bad_host the smallest index in any class, or -1
+ * s: n FP32 values (any layout; n >= 0; s may be NULL when n == 0).  scratch:
+ * 32 bytes of device memory, 8-byte aligned, overwritten.  Host outputs are
+ * written after the call synchronises `stream`.  No GEMM entry point calls
+ * this: the check is for loading time, not the forward path. */
+FP8BQ_API int fp8bq_check_scales(const float *s, int64_t n, void *scratch,
+                                 int64_t *counts_host, int64_t *first_bad_host,
+                                 void *stream);
+
 #ifdef __cplusplus
 }
 #endif

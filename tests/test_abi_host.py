@@ -173,3 +173,21 @@ def test_grouped_gemm_validation():
     assert callm({**okm, "E": 2000}) == 2
     assert callm({**okm, "E": 2, "max_m": 1 << 31}) == 2   # E * max_m overflows 32 bits
     assert callm({**okm, "max_m": 0}) == 0
+
+
+def test_check_scales_validation():
+    import ctypes as C
+    counts = (C.c_int64 * 3)(7, 7, 7)
+    first = C.c_int64(7)
+    cp, fp = C.c_void_p(C.addressof(counts)), C.c_void_p(C.addressof(first))
+    f = L.fp8bq_check_scales
+    assert f(P(A), 16, P(A), None, fp, None) == 1
+    assert f(P(A), 16, P(A), cp, None, None) == 1
+    assert f(None, 16, P(A), cp, fp, None) == 1
+    assert f(P(A), 16, None, cp, fp, None) == 1
+    assert f(P(A), -1, P(A), cp, fp, None) == 2
+    assert f(P(A + 2), 16, P(A), cp, fp, None) == 3
+    assert f(P(A), 16, P(A + 4), cp, fp, None) == 3
+    # an empty array: nothing is bad, nothing is launched
+    assert f(None, 0, None, cp, fp, None) == 0
+    assert list(counts) == [0, 0, 0] and first.value == -1
