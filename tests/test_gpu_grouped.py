@@ -85,6 +85,21 @@ def test_grouped_leading_gap_and_col_major_scales():
     _check_rows(y, oracle.gemm_grouped(qa, sa, qw, sw, re), re, "grouped gap col-major")
 
 
+@pytest.mark.parametrize("layout", [fb.SCALE_ROW_MAJOR, fb.SCALE_COL_MAJOR])
+def test_grouped_long_segments_pair_tiles(layout):
+    """More than 512 rows per expert on average: 256-row pair tiles, with a
+    3-row segment and segments ending inside both halves of a pair tile."""
+    counts, N, K = [1100, 3, 900, 130], 384, 512
+    T = sum(counts) + 5
+    assert T > 512 * len(counts)
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    qa, sa, sa_dev = _acts(T, K, seed=21, layout=layout)
+    qw, sw = _experts(len(counts), N, K, seed=23)
+    re = oracle.row_expert_contiguous(off, T)
+    y = _run_contiguous(qa, sa_dev, qw, sw, off, layout=layout)
+    _check_rows(y, oracle.gemm_grouped(qa, sa, qw, sw, re), re, f"grouped pair layout={layout}")
+
+
 def test_grouped_many_experts():
     """70 experts: the tile scan runs over three 32-expert steps."""
     E, T, N, K = 70, 900, 128, 128
