@@ -118,6 +118,7 @@ struct GemmArgs {
   uint32_t *status;
   uint32_t *counters;
   float *partials;
+  int64_t partials_bytes;  // room behind `partials` (0: no split tail tiles)
   uint64_t wait_limit_ns;
   // fault injection for the timeout tests (0 in normal use): CTA 0 issues no
   // copy for its first K block, so the waits on that stage run out
@@ -152,7 +153,13 @@ void launch_mx_sf_tiles(const uint8_t *ux, int64_t M, const uint8_t *uw, int64_t
 // the 128 weight rows of its block).
 void launch_ue8m0_sf_tiles(const uint8_t *ux, int64_t M, const uint8_t *uw, int64_t N, int64_t K,
                            uint8_t *sfa, uint8_t *sfb, int num_sms, cudaStream_t st);
-WorkspaceLayout workspace_layout(int op, int64_t M, int64_t N, int64_t K);
+// Block pair tiles whose K range is split (the last wave's tiles): each split
+// publishes its CTA's promoted 128 x 256 FP32 accumulators (128 KB).  At most
+// kMaxTailItems splits per launch (more than the clusters a GB300 holds).
+constexpr int kMaxTailItems = 80;
+constexpr int64_t kTailItemBytes = 2 * 128 * 256 * 4;  // both CTAs of a pair
+// `tail`: reserve the split-tail partials (block GEMM and linear, M > 64)
+WorkspaceLayout workspace_layout(int op, int64_t M, int64_t N, int64_t K, bool tail = true);
 
 // Work decomposition of one GEMM launch.
 struct LaunchShape {
@@ -162,6 +169,13 @@ struct LaunchShape {
   int kps;          // K blocks per split
   int KB;           // ceil(K / 128)
   int sx_stage;     // floats of shared memory staging s_x (swapped block form)
+  // block pair tiles: the first full_units units are whole tiles; the tiles
+  // after them (the last, partly filled wave) are split over tail_splits K
+  // ranges of tail_kps blocks each, one unit per range (full_units = units
+  // and tail_splits = 1 when nothing is split)
+  int full_units;
+  int tail_splits;
+  int tail_kps;
 };
 
 // K-major E4M3 matrix [rows, K] (pitch K bytes) as a TMA map with a

@@ -112,8 +112,10 @@ int check_ws(void *ws, size_t ws_bytes, int op, int64_t M, int64_t N, int64_t K)
   return FP8BQ_OK;
 }
 
+// `tail`: the workspace holds the split tail tiles' partials (every caller
+// workspace does; the fixed scratch of fp8bq_gemm_noalloc does not)
 GemmArgs base_args(int mode, int64_t M, int64_t N, int64_t K, const void *bias, void *y,
-                   void *ws, int op) {
+                   void *ws, int op, bool tail = true) {
   GemmArgs a;
   std::memset(&a, 0, sizeof a);
   a.mode = mode;
@@ -122,11 +124,12 @@ GemmArgs base_args(int mode, int64_t M, int64_t N, int64_t K, const void *bias, 
   a.K = static_cast<int>(K);
   a.bias = bias;
   a.y = y;
-  const WorkspaceLayout L = workspace_layout(op, M, N, K);
+  const WorkspaceLayout L = workspace_layout(op, M, N, K, tail);
   uint8_t *w = static_cast<uint8_t *>(ws);
   a.status = reinterpret_cast<uint32_t *>(w + L.status);
   a.counters = reinterpret_cast<uint32_t *>(w + L.counters);
   a.partials = reinterpret_cast<float *>(w + L.partials);
+  a.partials_bytes = static_cast<int64_t>(L.q - L.partials);
   a.wait_limit_ns = wait_limit_ns();
   a.fault_skip_first_load = fault_skip_first_load();
   return a;
@@ -148,8 +151,8 @@ int finish_launch(int st, cudaError_t e) {
 
 int gemm_block_impl(const void *q, const float *s_x, int s_layout, const void *w,
                     const float *s_w, const void *bias, void *y, int64_t M, int64_t N, int64_t K,
-                    void *ws, int op, cudaStream_t st, const DeviceInfo &dev) {
-  GemmArgs a = base_args(kModeBlock, M, N, K, bias, y, ws, op);
+                    void *ws, int op, cudaStream_t st, const DeviceInfo &dev, bool tail = true) {
+  GemmArgs a = base_args(kModeBlock, M, N, K, bias, y, ws, op, tail);
   a.sx = s_x;
   a.sx_layout = s_layout;
   a.ldsx = s_layout == FP8BQ_SCALE_ROW_MAJOR ? static_cast<int>((K + 127) / 128)
@@ -656,8 +659,9 @@ int fp8bq_gemm_noalloc(const void *q, const float *s_x, int s_layout, const void
   if (!aligned(q, 16) || !aligned(w, 16) || !aligned(y, 16) || !aligned(s_x, 4) ||
       !aligned(s_w, 4) || !aligned(bias, 2))
     return FP8BQ_ERR_ALIGN;
-  // the scratch is laid out exactly like an fp8bq_gemm workspace of this shape
-  const WorkspaceLayout L = workspace_layout(FP8BQ_OP_GEMM, M, N, K);
+  // the scratch is laid out like an fp8bq_gemm workspace of this shape without
+  // the split tail tiles' partials (those tiles then run whole)
+  const WorkspaceLayout L = workspace_layout(FP8BQ_OP_GEMM, M, N, K, false);
   if (L.total > static_cast<size_t>(FP8BQ_NOALLOC_SCRATCH_BYTES)) return FP8BQ_ERR_WORKSPACE;
   DeviceInfo dev;
   RETURN_IF(device_info(&dev));
@@ -673,7 +677,7 @@ int fp8bq_gemm_noalloc(const void *q, const float *s_x, int s_layout, const void
   e = cudaMemsetAsync(scratch, 0, L.partials, st);
   if (e != cudaSuccess) return cuda_fail(e);
   return gemm_block_impl(q, s_x, s_layout, w, s_w, bias, y, M, N, K, scratch, FP8BQ_OP_GEMM, st,
-                         dev);
+                         dev, false);
 }
 
 

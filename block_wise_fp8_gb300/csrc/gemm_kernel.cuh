@@ -246,10 +246,28 @@ struct GroupTable {
 template <bool SWAP, bool PAIR, bool GROUPED>
 __device__ __forceinline__ Unit decode_unit(int u, int num_a_tiles, int splits, int kps, int KB,
                                             int bn, uint32_t rank, int M, int N,
-                                            const GroupTable &gt) {
+                                            const GroupTable &gt, const LaunchShape &sh) {
   Unit r;
   r.row_end = M;
   r.expert = 0;
+  if (!SWAP && !GROUPED && sh.tail_splits > 1 && u >= sh.full_units) {
+    // a K range of a split tail tile: `tile` numbers the split tiles (their
+    // counters), `split` the range
+    const int v = u - sh.full_units;
+    const int ti = v / sh.tail_splits;
+    const int t = sh.full_units + ti;
+    const int mt = t % num_a_tiles, nt = t / num_a_tiles;
+    constexpr int kTileRows = PAIR ? 2 * kBM : kBM;
+    r.tile = ti;
+    r.split = v - ti * sh.tail_splits;
+    r.a_row0 = mt * kTileRows + static_cast<int>(rank) * kBM;
+    r.b_row0 = nt * bn;
+    r.b_load_row0 = r.b_row0 + (PAIR ? static_cast<int>(rank) * (bn / 2) : 0);
+    r.sw_row0 = r.b_row0 / kBlockN;
+    r.kb0 = r.split * sh.tail_kps;
+    r.kb1 = min(KB, r.kb0 + sh.tail_kps);
+    return r;
+  }
   if (!SWAP) {
     // A = tokens (256 per pair tile, 128 per CTA), B = bn weight rows (pair
     // tiles: bn/2 per CTA).  Plain GEMMs walk M fastest, so concurrently
@@ -410,7 +428,7 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
   // preceding kernel may write: no prefetch)
   if (!GROUPED && warp == 0 && lane == 0 && cl_id < shape.units) {
     const Unit w0 = decode_unit<SWAP, PAIR, GROUPED>(cl_id, shape.num_a_tiles, shape.splits, shape.kps,
-                                            shape.KB, BN, rank, args.M, args.N, gt);
+                                            shape.KB, BN, rank, args.M, args.N, gt, shape);
     const int npf = min(w0.kb1 - w0.kb0, SWAP ? 64 : 8);
     for (int i = 0; i < npf; ++i) {
       if (SWAP) tma_prefetch_l2_2d(&tmA, (w0.kb0 + i) * 128, w0.a_row0);
@@ -489,7 +507,7 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
         bool ok = true;
         const bool sc_tma = C::kScRing && args.sc_tma;
         for (int u = cl_id; ok && u < units; u += cl_num) {
-          const Unit w = decode_unit<SWAP, PAIR, GROUPED>(u, num_a, shape.splits, shape.kps, KB, BN, rank, args.M, args.N, gt);
+          const Unit w = decode_unit<SWAP, PAIR, GROUPED>(u, num_a, shape.splits, shape.kps, KB, BN, rank, args.M, args.N, gt, shape);
           for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
             if (sc_tma && (kb - w.kb0) % C::kScQuad == 0) {
               // promotion factors of K blocks kb .. kb+3: this CTA's s_x rows and
@@ -570,7 +588,7 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
         uint32_t it = 0, uit = 0;
         bool ok = true;
         for (int u = cl_id; ok && u < units; u += cl_num, ++uit) {
-          const Unit w = decode_unit<SWAP, PAIR, GROUPED>(u, num_a, shape.splits, shape.kps, KB, BN, rank, args.M, args.N, gt);
+          const Unit w = decode_unit<SWAP, PAIR, GROUPED>(u, num_a, shape.splits, shape.kps, KB, BN, rank, args.M, args.N, gt, shape);
           if (MODE != kModeBlock) {
             const uint32_t b = uit % ACCB, ph = (uit / ACCB) & 1u;
             if (!mbar_wait(&bars->tempty[b], ph ^ 1u, abort_flag, limit)) {
@@ -674,7 +692,7 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
     uint32_t kit = 0, uit = 0, sq = 0;
     bool ok = true;
     for (int u = cl_id; u < units; u += cl_num, ++uit) {
-      const Unit w = decode_unit<SWAP, PAIR, GROUPED>(u, num_a, shape.splits, shape.kps, KB, BN, rank, args.M, args.N, gt);
+      const Unit w = decode_unit<SWAP, PAIR, GROUPED>(u, num_a, shape.splits, shape.kps, KB, BN, rank, args.M, args.N, gt, shape);
       const int d_row = w.a_row0 + 32 * quarter + lane;  // row of D held by this thread
       const int col0 = cg * C::kCPT;                     // first D column of this thread
 
@@ -779,6 +797,51 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
           if (named_bar_any(2, C::kEpiThreads, !ok || *abort_flag)) {
             ok = false;
             break;
+          }
+          if (!GROUPED && shape.tail_splits > 1 && u >= shape.full_units) {
+            // a split tail tile: publish this range's promoted accumulators
+            // (column-major 256 x 128 per CTA, so a warp's stores are 128
+            // contiguous bytes); the last split to arrive sums all ranges in
+            // split order (its own from registers) and stores Y.  The barrier
+            // orders the stores before the counter's release; the last CTA's
+            // acquire on the same counter makes every split's partial visible.
+            const int row = 32 * quarter + lane;
+            const int64_t blk = 128 * 256;
+            float *mine = args.partials + (static_cast<int64_t>(w.tile) * shape.tail_splits + w.split) * 2 * blk +
+                          rank * blk;
+#pragma unroll
+            for (int j = 0; j < C::kCPT; ++j) __stcg(mine + (col0 + j) * 128 + row, acc[j]);
+            named_bar_sync(2, C::kEpiThreads);
+            if (et == 0) {
+              const uint32_t prev = atom_add_acq_rel_gpu(args.counters + 2 * w.tile + rank, 1u);
+              bars->is_last = (prev == static_cast<uint32_t>(shape.tail_splits - 1)) ? 1u : 0u;
+            }
+            named_bar_sync(2, C::kEpiThreads);
+            if (!bars->is_last) continue;
+            const float *base = args.partials + static_cast<int64_t>(w.tile) * shape.tail_splits * 2 * blk +
+                                rank * blk + col0 * 128 + row;
+#pragma unroll
+            for (int c = 0; c < C::kCPT / 32; ++c) {
+              float sum[32];
+#pragma unroll
+              for (int j = 0; j < 32; ++j) sum[j] = 0.0f;
+              for (int sp = 0; sp < shape.tail_splits; ++sp) {
+                if (sp == w.split) {
+#pragma unroll
+                  for (int j = 0; j < 32; ++j) sum[j] += acc[c * 32 + j];
+                } else {
+                  const float *src = base + static_cast<int64_t>(sp) * 2 * blk + (c * 32) * 128;
+                  float v[32];
+#pragma unroll
+                  for (int j = 0; j < 32; ++j) v[j] = __ldcg(src + j * 128);
+#pragma unroll
+                  for (int j = 0; j < 32; ++j) sum[j] += v[j];
+                }
+              }
+#pragma unroll
+              for (int j = 0; j < 32; ++j) acc[c * 32 + j] = sum[j];
+            }
+            if (et == 0) args.counters[2 * w.tile + rank] = 0u;  // ready for the next call
           }
           if (bias) {
 #pragma unroll
@@ -1041,6 +1104,29 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
   }
 }
 
+// The last wave of block pair tiles: the tiles left after the full waves of
+// `clusters` occupy only some of them.  When they fill at most half, each is
+// split into up to 4 K ranges (multiples of 4 blocks: the promotion factors
+// arrive four K blocks per TMA box) that run on otherwise idle clusters; the
+// last range of a tile to finish sums the others' promoted partials in range
+// order.  Needs room for the partials in the workspace.
+inline void split_tail_tiles(LaunchShape &sh, int clusters, int64_t partials_bytes) {
+  const int T = sh.units % clusters;
+  if (T == 0 || 2 * T > clusters) return;
+  int S = clusters / T;
+  if (S > 4) S = 4;
+  if (S > sh.KB / 4) S = sh.KB / 4;
+  if (S < 2) return;
+  const int kps = ((sh.KB + S - 1) / S + 3) / 4 * 4;
+  S = (sh.KB + kps - 1) / kps;
+  const int64_t items = static_cast<int64_t>(T) * S;
+  if (S < 2 || items > kMaxTailItems || items * kTailItemBytes > partials_bytes) return;
+  sh.full_units = sh.units - T;
+  sh.tail_splits = S;
+  sh.tail_kps = kps;
+  sh.units = sh.full_units + T * S;
+}
+
 // Launches one variant.  `grid` counts CTAs for single-CTA tiles and clusters
 // for pair tiles; for pair tiles it is clamped to the clusters the device can
 // hold at once, so the persistent grid is a single wave.
@@ -1168,8 +1254,10 @@ cudaError_t run(const GemmArgs &a, const void *q_act, const void *w, const Launc
     max_clusters = n > 0 ? n : 1;
   }
   const int clusters = grid < max_clusters ? grid : max_clusters;
+  LaunchShape shx = sh;
+  if (MODE == kModeBlock && !GROUPED) split_tail_tiles(shx, clusters, args.partials_bytes);
   cfg.gridDim = dim3(2 * clusters, 1, 1);
-  e = cudaLaunchKernelEx(&cfg, kern, ta, tb, ty, tsx, tsw, args, sh);
+  e = cudaLaunchKernelEx(&cfg, kern, ta, tb, ty, tsx, tsw, args, shx);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -167,18 +167,28 @@ bool cached_bf16_rows_map(CUtensorMap *m, const void *base, int64_t rows, int64_
 
 // [status word | split-K tile counters | split-K FP32 partials | fused: Q | fused: scales |
 //  MX: activation and weight scale-factor chunks]
-WorkspaceLayout workspace_layout(int op, int64_t M, int64_t N, int64_t K) {
+WorkspaceLayout workspace_layout(int op, int64_t M, int64_t N, int64_t K, bool tail) {
   auto up = [](size_t v) { return (v + 255) / 256 * 256; };
   WorkspaceLayout L{};
   const int64_t KB = (K + 127) / 128;
   const int64_t NT = (N + 127) / 128;
   L.status = 0;
   L.counters = 256;
-  size_t off = L.counters + up(static_cast<size_t>(NT) * 4);
+  // one counter per 128 output columns (split-K decode tiles), and two per
+  // split tail tile of the block pair form
+  size_t off = L.counters + up(static_cast<size_t>(NT > 2 * kMaxTailItems ? NT : 2 * kMaxTailItems) * 4);
   L.partials = off;
   const bool mx = (op == 2 || op == 3 || op == 8 || op == 9);  // MX GEMM (UE8M0 views too)
   const bool grouped = (op == 10);  // pair tiles at every M: no split-K partials
-  if (M <= 64 && !mx && !grouped) off += up(static_cast<size_t>(kMaxSplits) * M * N * 4);
+  const bool block = (op == 0 || op == 1);
+  if (M <= 64 && !mx && !grouped) {
+    off += up(static_cast<size_t>(kMaxSplits) * M * N * 4);
+  } else if (block && tail) {
+    // split tail tiles: at most one split per pair tile, and kMaxTailItems
+    const int64_t tiles = (M + 255) / 256 * ((N + 255) / 256);
+    const int64_t items = tiles < kMaxTailItems ? tiles : kMaxTailItems;
+    off += up(static_cast<size_t>(items * kTailItemBytes));
+  }
   L.q = off;
   const bool fused = (op == 1 || op == 3 || op == 5 || op == 7 || op == 9);
   if (fused) off += up(static_cast<size_t>(M) * K);
@@ -300,6 +310,9 @@ int launch_gemm(const GemmArgs &a, const void *q_act, const void *w, const Devic
   sh.kps = sh.KB;
   sh.units = sh.num_a_tiles * ((a.N + best_bn - 1) / best_bn);
   sh.sx_stage = 0;
+  sh.full_units = sh.units;
+  sh.tail_splits = 1;
+  sh.tail_kps = sh.KB;
   const int grid = sh.units < pairs ? sh.units : pairs;
   *cuda_err = (a.mode == kModeBlock)     ? run_block_pair(best_bn, a, q_act, w, sh, grid, st, &status)
               : (a.mode == kModeChannel) ? run_channel_pair(best_bn, a, q_act, w, sh, grid, st, &status)

@@ -49,7 +49,11 @@
  *  - GEMM and linear entry points take a workspace `ws` of at least
  *    fp8bq_workspace_bytes(op, M, N, K) bytes, 256-byte aligned, zeroed once
  *    with fp8bq_workspace_init before its first use.  The library keeps it in a
- *    valid state between calls.  Calls that share a workspace must not overlap
+ *    valid state between calls.  Besides a status word and tile counters it
+ *    holds FP32 partial sums: the split-K decode tiles' (M <= 64) and, for the
+ *    block GEMM and linear above 64 rows, those of the last wave's tiles,
+ *    which run split into K ranges on otherwise idle SMs (256 KB per split,
+ *    at most 80 splits: up to 20 MB).  Calls that share a workspace must not overlap
  *    on the GPU (same stream, or ordered by events).
  *  - Every device-side wait is bounded: a wait that runs out sets a status word
  *    in the workspace, the kernel exits cleanly, and fp8bq_poll_status reports
@@ -159,12 +163,16 @@ FP8BQ_API int fp8bq_linear(const void *x, int64_t ldx, const void *w,
  * In place of `ws` it uses one array of FP8BQ_NOALLOC_SCRATCH_BYTES that the
  * library holds in device memory on every GPU that loads it, until the process
  * exits; it calls no allocating routine.
- *  - Limit: shapes whose fp8bq_workspace_bytes(FP8BQ_OP_GEMM, M, N, K) exceeds
- *    FP8BQ_NOALLOC_SCRATCH_BYTES are rejected with FP8BQ_ERR_WORKSPACE before
- *    anything is launched.  For M > 64 that is a status word and one counter
- *    per 128 output columns, so every N up to about 5 * 10^8 fits; for
- *    M <= 64 it adds FP32 split-K partials (32 * M * N bytes), so M * N must
- *    stay below about 524,000: every M <= 64 at N = 6144, M <= 16 at N = 24576.
+ *  - Limit: the scratch holds the workspace of fp8bq_gemm at this shape
+ *    without the split tail tiles' partials (below), and shapes that need more
+ *    than FP8BQ_NOALLOC_SCRATCH_BYTES are rejected with FP8BQ_ERR_WORKSPACE
+ *    before anything is launched.  For M > 64 that is a status word and one
+ *    counter per 128 output columns (at least 160), so every N up to about
+ *    5 * 10^8 fits; for M <= 64 it adds FP32 split-K partials (32 * M * N
+ *    bytes), so M * N must stay below about 524,000: every M <= 64 at
+ *    N = 6144, M <= 16 at N = 24576.  Without the partials, the last wave's
+ *    tiles run whole: results agree with fp8bq_gemm's within the GEMM
+ *    tolerance, not bit for bit.
  *  - Set-up: the first call on a device, with that device current, looks up
  *    the array's device address (cudaGetSymbolAddress) and keeps it; make that
  *    first call before any stream capture begins.  A failed look-up returns

@@ -116,6 +116,23 @@ def test_split_k_reduction_is_deterministic():
     assert np.array_equal(ys[0], ys[1]) and np.array_equal(ys[1], ys[2])
 
 
+@pytest.mark.parametrize("M,N,K", [(300, 1000, 6016), (512, 768, 1152), (256, 512, 2048)])
+@pytest.mark.parametrize("layout", [fb.SCALE_ROW_MAJOR, fb.SCALE_COL_MAJOR])
+def test_gemm_split_tail_tiles(M, N, K, layout):
+    """Few pair tiles against many clusters: the tiles are split into K ranges
+    (47 K blocks in 4 ranges with a short last one; 9 in ranges of 8 and 1) and
+    the last range to finish sums the promoted partials.  With a bias, which
+    only the summing range adds; three calls on one workspace agree bit for bit
+    (the sum runs in range order)."""
+    qa, sa = oracle.quant_group(si.activations(M, K, base_seed=M))
+    qw, sw = _weights(N, K)
+    bias = si.f32_to_bf16_bits(np.linspace(-3, 3, N).astype(np.float32))
+    ws = fb.new_workspace(fb.OP_GEMM, M, N, K)
+    ys = [_gemm(qa, sa, qw, sw, bias=bias, layout=layout, ws=ws) for _ in range(3)]
+    check_close(ys[0], oracle.gemm_block(qa, sa, qw, sw, bias=bias), f"split tail {M}x{N}x{K}")
+    assert np.array_equal(ys[0], ys[1]) and np.array_equal(ys[1], ys[2])
+
+
 @pytest.mark.parametrize("M,N,K", [(16, 384, 256), (1, 6144, 6144), (64, 6144, 6144),
                                    (300, 384, 256), (4096, 6144, 6144)])
 def test_linear_matches_oracle(M, N, K):
