@@ -168,13 +168,18 @@ __device__ __forceinline__ void add_square_general(uint64_t &acc, uint32_t &lost
   }
 }
 
-// The thread's sum in the general form, over its n 16-byte chunks.
-__device__ __noinline__ void thread_sum_general(const uint4 *r, int n, int Et, uint64_t &acc,
-                                                uint32_t &lost) {
+// The thread's sum in the general form, over its CH 16-byte chunks.  Inline
+// and unrolled: a call taking the chunks by address would keep them in local
+// memory for every row, not only for rows that take this branch.
+template <int CH>
+__device__ __forceinline__ void thread_sum_general(const uint4 (&r)[CH], int Et, uint64_t &acc,
+                                                   uint32_t &lost) {
   acc = 0ull;
   lost = 0u;
-  for (int c = 0; c < n; ++c) {
+#pragma unroll
+  for (int c = 0; c < CH; ++c) {
     const uint32_t w[4] = {r[c].x, r[c].y, r[c].z, r[c].w};
+#pragma unroll
     for (int i = 0; i < 8; ++i)
       add_square_general(acc, lost, (i & 1) ? (w[i >> 1] >> 16) : (w[i >> 1] & 0xFFFFu), Et);
   }
@@ -310,7 +315,7 @@ __global__ void __launch_bounds__(THREADS, THREADS == 256 ? 3 : 1) add_rmsnorm_k
         lost = far ? static_cast<uint32_t>(CH * 8) : 0u;  // < 1 unit per term
         within20 = !far;
       } else {  // a thread whose values all lie below 2^-99: the general form
-        thread_sum_general(r, CH, Et, acc, lost);
+        thread_sum_general<CH>(r, Et, acc, lost);
       }
     }
     // ---- block sum.  1: the row's largest exponent Eb (non-finite rows 256 / 257)
