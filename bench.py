@@ -63,8 +63,8 @@ FP8_PER_BF16 = 2.0   # nominal dense FP8 / BF16 tensor rate
 # digest is recorded; anything else reports null.
 NCU_TRAFFIC = {
     # profiles/block_gemm_prefill_4096x24576x6144.md (N = 24576 launch)
-    "source_sha256": "f5c1767be033c0eb28144da5d4bf0f44080329f4cf0fe7dddb55304a32e88bbf",
-    "bytes_per_launch": 189151488 + 177110016,
+    "source_sha256": "5bb460394ed7aa3d3039ec507b68553d98354dfdde2628dad18e87c0a1b6d723",
+    "bytes_per_launch": 188578816 + 184211712,
 }
 
 
