@@ -63,18 +63,22 @@ FP8_PER_BF16 = 2.0   # nominal dense FP8 / BF16 tensor rate
 # digest is recorded; anything else reports null.
 NCU_TRAFFIC = {
     # profiles/block_gemm_prefill_4096x24576x6144.md (N = 24576 launch)
-    "source_sha256": "5bb460394ed7aa3d3039ec507b68553d98354dfdde2628dad18e87c0a1b6d723",
+    "source_sha256": "f96432eca197b43f8e4d177ae74bc77675338b77b40858dda547a02ca78fc638",
     "bytes_per_launch": 188578816 + 184211712,
 }
 
 
 def kernel_source_digest() -> str:
+    """SHA-256 of the GEMM kernel sources with // comments and blank lines
+    removed: any change to the code invalidates the recorded traffic, a change
+    to the comments alone does not."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "block_wise_fp8_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
         if f.startswith("gemm") or f in ("ptx.cuh", "common.cuh"):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(f.encode() + fh.read())
+            with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+                code = [l.split("//", 1)[0].rstrip() for l in fh]
+            h.update(f.encode() + "\n".join(l for l in code if l).encode())
     return h.hexdigest()
 
 

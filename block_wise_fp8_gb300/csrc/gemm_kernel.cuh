@@ -35,11 +35,20 @@
 //           128 token rows and half of the BN weight rows, the even CTA issues the
 //           MMAs, each CTA's TMEM receives its 128 rows of the result and its own
 //           epilogue promotes and stores them.  Persistent clusters walk the tiles
-//           M-fastest so concurrent clusters share weight tiles in L2.
+//           M-fastest so concurrent clusters share weight tiles in L2.  Block
+//           tiles of a last, partly filled wave are split into K ranges on idle
+//           clusters; the last range to finish sums the promoted partials in
+//           range order (split_tail_tiles).
 //   normal  the same with one CTA: UMMA M = 128 tokens, UMMA N = BN weight rows.
 //   swap    UMMA M = 128 weight rows, UMMA N = BN tokens (decode, M <= 64), with
 //           split-K across CTAs and a deterministic last-CTA reduction in
 //           ascending split order.
+//   grouped (GROUPED instances, block pair or normal) the MoE form: A and Y rows
+//           are split into per-expert segments whose bounds the kernel reads
+//           from the device; every CTA builds the m-tile table in shared
+//           memory, tiles stop at their segment's end, and B / s_w are the
+//           expert's slices of [E * N, K] and [E * ceil(N/128), KB]
+//           ("SGLang 源码完全拆解(十九)", §MoE:专家权重多一个维度).
 //
 // Every wait is bounded (see ptx.cuh); a CTA that gives up records a timeout in
 // the workspace status word, lets its in-flight copies and MMAs land, frees its
