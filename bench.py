@@ -678,7 +678,28 @@ def run_extra(fb, torch, dev, stream, hbm_peak, fp8_peak):
                                     "gbs": round(gbs, 1), "frac_fp8": round(tf / fp8_peak, 4),
                                     "frac_hbm": round(gbs / hbm_peak, 4),
                                     "frac_roofline": round(t_min / (t * 1e-3), 4)}
-        del qw, sw, qa, sa, y
+        del qa, sa, y
+        if which == "w13":
+            # decode-time MoE in the masked layout: 256 routed rows over the 32
+            # experts, slots of 64 rows; the launch streams every expert's
+            # weights once for a few rows each
+            Td, max_m = 256, 64
+            cd = np.minimum(si.expert_counts(Td, E, mo["skew"], base_seed=1), max_m)
+            mm = torch.tensor(cd.astype(np.int32), device=dev)
+            qd = torch.randint(0, 0x7E, (E * max_m, K), dtype=torch.uint8, device=dev)
+            sd = torch.rand(E * max_m, KB, device=dev) + 0.5
+            yd = torch.empty(E * max_m, N, dtype=torch.bfloat16, device=dev)
+            wsd = fb.new_workspace(fb.OP_GROUPED_GEMM, E * max_m, N, K, device=dev)
+            t = _time_back_to_back(torch, stream,
+                                   [lambda: fb.fp8bq_grouped_gemm_masked(qd, sd, qw, sw, mm, yd, wsd)],
+                                   20)
+            live_d = int((cd > 0).sum())
+            bd = live_d * (N * K + NB * KB * 4) + int(cd.sum()) * (K + KB * 4 + 2 * N)
+            gr[f"masked_decode_{which}_rows{int(cd.sum())}_slots{max_m}"] = {
+                "us": round(t * 1e3, 2), "gbs": round(bd / (t * 1e-3) / 1e9, 1),
+                "frac_hbm": round(bd / (t * 1e-3) / 1e9 / hbm_peak, 4)}
+            del qd, sd, yd
+        del qw, sw
     out["grouped_moe"] = gr
 
     # context only (not a denominator): the vendor's plain FP8 GEMM with
