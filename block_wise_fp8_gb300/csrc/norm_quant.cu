@@ -211,6 +211,15 @@ __global__ void __launch_bounds__(THREADS, THREADS == 256 ? 3 : 1) add_rmsnorm_k
     no_abort = 0u;
     fence_mbar_init();
   }
+  // before the preceding kernel completes: an L2 prefetch of this CTA's first
+  // row (L2 is the point of coherence, so the row copies after the wait still
+  // see whatever that kernel writes)
+  if (blockIdx.x < a.M) {
+    for (uint32_t off = static_cast<uint32_t>(t) * 128u; off < row_bytes; off += THREADS * 128u) {
+      prefetch_l2(a.x + blockIdx.x * a.ldx_bytes + off);
+      if (a.res) prefetch_l2(a.res + blockIdx.x * a.ldr_bytes + off);
+    }
+  }
   if (QMODE == 1) fill_scale_table(table);
   __syncthreads();
   griddep_wait();

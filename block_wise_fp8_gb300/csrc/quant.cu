@@ -35,9 +35,6 @@ __global__ void __launch_bounds__(kThreads) quant_group128_kernel(
   float *s = static_cast<float *>(s_out);
   __shared__ ScaleTable table;
   griddep_launch_dependents();
-  fill_scale_table(table);
-  __syncthreads();
-  griddep_wait();
   const int lane = threadIdx.x & 31, sub = lane & 7;
   const int64_t total = M * G;
   const int64_t step = static_cast<int64_t>(gridDim.x) * (kThreads / 8);  // groups per step
@@ -46,6 +43,14 @@ __global__ void __launch_bounds__(kThreads) quant_group128_kernel(
   // (row, group) of this thread's group, advanced by (drow, dg) per step
   int64_t row = gid / G;
   int g = static_cast<int>(gid - row * G);
+  // Before the preceding kernel has completed, only an L2 prefetch of this
+  // thread's first chunk: L2 is the point of coherence, so a later load still
+  // sees whatever that kernel writes there
+  if (row < M && g * 128 + sub * 16 < K)
+    prefetch_l2(x + row * ldx_bytes + static_cast<int64_t>(g * 128 + sub * 16) * 2);
+  fill_scale_table(table);
+  __syncthreads();
+  griddep_wait();
   const int64_t drow = step / G;
   const int dg = static_cast<int>(step - drow * G);
   auto load = [&](int64_t r, int gg, uint4 (&v)[2]) {
@@ -118,9 +123,6 @@ __global__ void __launch_bounds__(kThreads) quant_mx_kernel(const uint8_t *__res
                                                             uint8_t *__restrict__ s) {
   __shared__ ScaleTable table;
   griddep_launch_dependents();
-  fill_scale_table(table);
-  __syncthreads();
-  griddep_wait();
   const int G = K / 32;
   const int lane = threadIdx.x & 31, sub = lane & 1;
   const int64_t total = M * G;
@@ -129,6 +131,11 @@ __global__ void __launch_bounds__(kThreads) quant_mx_kernel(const uint8_t *__res
   const int64_t gid = warp_g0 + (lane >> 1);
   int64_t row = gid / G;
   int g = static_cast<int>(gid - row * G);
+  // before the preceding kernel completes: an L2 prefetch of the first chunk
+  if (row < M) prefetch_l2(x + row * ldx_bytes + static_cast<int64_t>(g * 32 + sub * 16) * 2);
+  fill_scale_table(table);
+  __syncthreads();
+  griddep_wait();
   const int64_t drow = step / G;
   const int dg = static_cast<int>(step - drow * G);
   auto load = [&](int64_t r, int gg, uint4 (&v)[2]) {
@@ -189,11 +196,15 @@ __global__ void __launch_bounds__(kThreads) quant_token_kernel(const uint8_t *__
   __shared__ ScaleTable table;
   __shared__ float red[2][kThreads / 32];
   griddep_launch_dependents();
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int C = K / 16;
+  // before the preceding kernel completes: an L2 prefetch of the first row
+  // (one 128-byte line per four 32-byte chunks)
+  if (blockIdx.x < M)
+    for (int c = 4 * t; c < C; c += 4 * kThreads) prefetch_l2(x + blockIdx.x * ldx_bytes + c * 32);
   fill_scale_table(table);
   __syncthreads();
   griddep_wait();
-  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  const int C = K / 16;
   int par = 0;
   for (int64_t row = blockIdx.x; row < M; row += gridDim.x, par ^= 1) {
     const uint8_t *xr = x + row * ldx_bytes;
@@ -233,13 +244,16 @@ __global__ void __launch_bounds__(kThreads) quant_static_kernel(const uint8_t *_
                                                                 const float *__restrict__ s_ptr,
                                                                 uint8_t *__restrict__ q) {
   griddep_launch_dependents();
-  griddep_wait();
   const int C = K / 16;
   const int64_t total = M * C;
   const int64_t step = static_cast<int64_t>(gridDim.x) * kThreads;
   const int64_t cid0 = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
   int64_t row = cid0 / C;
   int c = static_cast<int>(cid0 - row * C);
+  // before the preceding kernel completes: an L2 prefetch of the first chunk
+  // (the scale, which that kernel may write, is read after the wait)
+  if (row < M) prefetch_l2(x + row * ldx_bytes + static_cast<int64_t>(c) * 32);
+  griddep_wait();
   const int64_t drow = step / C;
   const int dc = static_cast<int>(step - drow * C);
   const StaticScale sc = static_scale(__ldg(s_ptr));

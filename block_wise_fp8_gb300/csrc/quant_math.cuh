@@ -27,6 +27,11 @@ __device__ __forceinline__ void unpack16(const uint4 (&v)[2], float (&f)[16]) {
   }
 }
 
+// Prefetch the cache line holding `p` into L2 (no data returned).
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 __device__ __forceinline__ uint4 ld_stream(const void *p) {
   uint4 r;
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
