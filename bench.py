@@ -22,7 +22,8 @@ Also reported, measured in the same run:
                torch._scaled_mm), which has no block scales to promote;
   cpu_baseline the CPU oracle on a bounded sample of the same workload.
 `--profile-case <case>` runs only a few launches of one kernel (MXFP8, UE8M0,
-channelwise GEMM, norm + quantisation, grouped w13 / w2) for ncu captures.
+channelwise, static and decode GEMMs, group-128 quantisation, norm +
+quantisation, grouped w13 / w2) for ncu captures.
 
 L2 is flushed (256 MiB write) between timed steps; every step is timed with
 CUDA events on the launching stream, synchronised on both sides.
@@ -828,7 +829,7 @@ def run_reference(args):
 
 
 PROFILE_CASES = ("mx", "norm_group", "norm_static", "grouped_w13", "grouped_w2", "channel",
-                 "ue8m0")
+                 "ue8m0", "quant_group", "decode_m1", "decode_m64", "static_4096")
 
 
 def run_profile_case(case: str, launches: int = 3):
@@ -879,6 +880,28 @@ def run_profile_case(case: str, launches: int = 3):
             s = torch.empty(M, K // 128, dtype=torch.float32, device=dev)
             fn = lambda: fb.fp8bq_add_rmsnorm_quant_act(x, g, eps, residual=r, residual_out=ro,
                                                         q=q, s=s)
+    elif case == "quant_group":
+        M, K = PREFILL_M, PREFILL_K
+        x = torch.randn(M, K, device=dev).to(torch.bfloat16)
+        q = torch.empty(M, K, dtype=torch.uint8, device=dev)
+        sx = torch.empty(M, K // 128, dtype=torch.float32, device=dev)
+        fn = lambda: fb.fp8bq_quant_act(x, q, sx)
+    elif case.startswith("decode"):
+        M, K, N = int(case[len("decode_m"):]), si.DECODE["K"], si.DECODE["N"]
+        q, w = codes(M, K), codes(N, K)
+        sx = torch.rand(M, K // 128, device=dev) + 0.5
+        sw = torch.rand(N // 128, K // 128, device=dev) * 1e-3
+        y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        ws = fb.new_workspace(fb.OP_GEMM, M, N, K, device=dev)
+        fn = lambda: fb.fp8bq_gemm(q, sx, w, sw, y, ws)
+    elif case == "static_4096":
+        M, K, N = 4096, si.STATIC["K"], si.STATIC["N"]
+        q, w = codes(M, K), codes(N, K)
+        sxs = torch.full((1,), 0.01, dtype=torch.float32, device=dev)
+        sp = torch.rand(len(si.STATIC["parts"]), device=dev) * 1e-3
+        y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        ws = fb.new_workspace(fb.OP_STATIC_GEMM, M, N, K, device=dev)
+        fn = lambda: fb.fp8bq_static_gemm(q, sxs, w, sp, list(si.STATIC["parts"]), y, ws)
     elif case.startswith("grouped"):
         mo = si.MOE
         E, T = mo["E"], mo["T"]
