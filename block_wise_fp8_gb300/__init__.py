@@ -330,12 +330,19 @@ def fp8bq_check_scales(s, scratch=None, stream=None) -> dict:
 
 # ---------------------------------------------------------------- grouped (MoE)
 
+def _device_int32(t, n: int, what: str):
+    """The segment bounds are read by the kernel: a CUDA int32 tensor of n values."""
+    if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == torch.int32
+            and t.is_contiguous() and t.numel() == n):
+        raise ValueError(f"{what} must be a contiguous CUDA int32 tensor with {n} values")
+
 def fp8bq_grouped_gemm(q, s_x, w, s_w, offsets, y, ws, s_layout: int = SCALE_ROW_MAJOR,
                        stream=None):
     """Rows offsets[e] .. offsets[e+1]-1 of q / y use expert e's weight w[e]
     [N, K] and scale grid s_w[e]; offsets is a device int32 tensor [E+1]."""
     M, K = q.shape
     E, N, _ = w.shape
+    _device_int32(offsets, E + 1, "offsets")
     _check(_lib.fp8bq_grouped_gemm(_ptr(q), _ptr(s_x), s_layout, _ptr(w), _ptr(s_w),
                                    _ptr(offsets), E, _ptr(y), M, N, K, _ptr(ws), _nbytes(ws),
                                    _stream(stream)), "fp8bq_grouped_gemm")
@@ -347,6 +354,7 @@ def fp8bq_grouped_gemm_masked(q, s_x, w, s_w, masked_m, y, ws, s_layout: int = S
     use expert e's weight; masked_m is a device int32 tensor [E]."""
     E, N, K = w.shape
     max_m = q.numel() // (K * E) if E else 0
+    _device_int32(masked_m, E, "masked_m")
     _check(_lib.fp8bq_grouped_gemm_masked(_ptr(q), _ptr(s_x), s_layout, _ptr(w), _ptr(s_w),
                                           _ptr(masked_m), E, max_m, _ptr(y), N, K, _ptr(ws),
                                           _nbytes(ws), _stream(stream)),

@@ -191,3 +191,15 @@ def test_check_scales_validation():
     # an empty array: nothing is bad, nothing is launched
     assert f(None, 0, None, cp, fp, None) == 0
     assert list(counts) == [0, 0, 0] and first.value == -1
+
+
+def test_grouped_binding_rejects_host_bounds():
+    """The segment bounds are read on the device: the binding refuses host tensors."""
+    import torch
+    q = torch.empty(0, dtype=torch.uint8)
+    with pytest.raises(ValueError):
+        fb.fp8bq_grouped_gemm(q.view(0, 16), None, torch.empty(2, 16, 16, dtype=torch.uint8), None,
+                              torch.zeros(3, dtype=torch.int32), None, None)
+    with pytest.raises(ValueError):
+        fb.fp8bq_grouped_gemm_masked(q, None, torch.empty(2, 16, 16, dtype=torch.uint8), None,
+                                     torch.zeros(2, dtype=torch.int32), None, None)
