@@ -65,8 +65,8 @@ FP8_PER_BF16 = 2.0   # nominal dense FP8 / BF16 tensor rate
 # digest is recorded; anything else reports null.
 NCU_TRAFFIC = {
     # profiles/block_gemm_prefill_4096x24576x6144.md (N = 24576 launch)
-    "source_sha256": "f96432eca197b43f8e4d177ae74bc77675338b77b40858dda547a02ca78fc638",
-    "bytes_per_launch": 188578816 + 184211712,
+    "source_sha256": "c48a2742778cea355671fb70e17df2f824239a693113053e2d8b52efe912b2b6",
+    "bytes_per_launch": 186639104 + 184989696,
 }
 
 

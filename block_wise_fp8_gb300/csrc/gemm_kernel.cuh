@@ -1254,14 +1254,19 @@ cudaError_t run(const GemmArgs &a, const void *q_act, const void *w, const Launc
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  static int max_clusters = 0;  // per variant; the library targets one device type
-  if (max_clusters == 0) {
-    cfg.gridDim = dim3(2 * grid, 1, 1);
+  // clusters the device holds at once, queried once per variant (the library
+  // targets one device type); thread-safe like the attribute set-up above
+  static std::once_flag occ_once;
+  static int max_clusters = 0;
+  static cudaError_t occ_err = cudaSuccess;
+  std::call_once(occ_once, [&] {
+    cudaLaunchConfig_t q = cfg;
+    q.gridDim = dim3(2 * grid, 1, 1);
     int n = 0;
-    e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
-    if (e != cudaSuccess) return e;
+    occ_err = cudaOccupancyMaxActiveClusters(&n, kern, &q);
     max_clusters = n > 0 ? n : 1;
-  }
+  });
+  if (occ_err != cudaSuccess) return occ_err;
   const int clusters = grid < max_clusters ? grid : max_clusters;
   LaunchShape shx = sh;
   if (MODE == kModeBlock && !GROUPED) split_tail_tiles(shx, clusters, args.partials_bytes);
