@@ -65,8 +65,8 @@ FP8_PER_BF16 = 2.0   # nominal dense FP8 / BF16 tensor rate
 # digest is recorded; anything else reports null.
 NCU_TRAFFIC = {
     # profiles/block_gemm_prefill_4096x24576x6144.md (N = 24576 launch)
-    "source_sha256": "c48a2742778cea355671fb70e17df2f824239a693113053e2d8b52efe912b2b6",
-    "bytes_per_launch": 186639104 + 184989696,
+    "source_sha256": "f563fb4d3ff93d95ce8bc40722abd36acee0104de5653dd5258ee7d6774f8309",
+    "bytes_per_launch": 188697856 + 184808960,
 }
 
 

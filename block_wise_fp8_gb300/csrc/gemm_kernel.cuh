@@ -1114,7 +1114,9 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
 }
 
 // The last wave of block pair tiles: the tiles left after the full waves of
-// `clusters` occupy only some of them.  When they fill at most half, each is
+// `clusters` (the clusters the device holds at once) occupy only some of them;
+// with fewer tiles than clusters, that is every tile.  When they fill at most
+// half, each is
 // split into up to 4 K ranges (multiples of 4 blocks: the promotion factors
 // arrive four K blocks per TMA box) that run on otherwise idle clusters; the
 // last range of a tile to finish sums the others' promoted partials in range
@@ -1267,9 +1269,16 @@ cudaError_t run(const GemmArgs &a, const void *q_act, const void *w, const Launc
     max_clusters = n > 0 ? n : 1;
   });
   if (occ_err != cudaSuccess) return occ_err;
-  const int clusters = grid < max_clusters ? grid : max_clusters;
+  // block tiles: the last wave (all of them when there are fewer tiles than
+  // the device holds clusters) may be split over idle clusters; the grid then
+  // covers the split units
   LaunchShape shx = sh;
-  if (MODE == kModeBlock && !GROUPED) split_tail_tiles(shx, clusters, args.partials_bytes);
+  int want = grid;
+  if (MODE == kModeBlock && !GROUPED) {
+    split_tail_tiles(shx, max_clusters, args.partials_bytes);
+    if (shx.units > want) want = shx.units;
+  }
+  const int clusters = want < max_clusters ? want : max_clusters;
   cfg.gridDim = dim3(2 * clusters, 1, 1);
   e = cudaLaunchKernelEx(&cfg, kern, ta, tb, ty, tsx, tsw, args, shx);
   if (e != cudaSuccess) return e;

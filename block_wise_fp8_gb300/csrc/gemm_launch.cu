@@ -184,9 +184,10 @@ WorkspaceLayout workspace_layout(int op, int64_t M, int64_t N, int64_t K, bool t
   if (M <= 64 && !mx && !grouped) {
     off += up(static_cast<size_t>(kMaxSplits) * M * N * 4);
   } else if (block && tail) {
-    // split tail tiles: at most one split per pair tile, and kMaxTailItems
-    const int64_t tiles = (M + 255) / 256 * ((N + 255) / 256);
-    const int64_t items = tiles < kMaxTailItems ? tiles : kMaxTailItems;
+    // split tail tiles: at most 4 K ranges per pair tile (256 rows by at least
+    // 192 weight rows, the narrowest pair tile), and kMaxTailItems
+    const int64_t tiles = (M + 255) / 256 * ((N + 191) / 192);
+    const int64_t items = 4 * tiles < kMaxTailItems ? 4 * tiles : kMaxTailItems;
     off += up(static_cast<size_t>(items * kTailItemBytes));
   }
   L.q = off;

@@ -58,11 +58,13 @@ def test_workspace_bytes():
     assert lin >= dec + 64 * 6144 + 48 * 64 * 4
     assert fb.fp8bq_workspace_bytes(99, 1, 1, 1) == 256
     # block GEMM and linear above 64 rows: room for the split tail tiles'
-    # partials (at most 80 splits of 256 KB, and no more splits than pair tiles)
+    # partials (at most 4 K ranges of 256 KB per pair tile of 256 x 192 or
+    # wider, 80 in all)
     big = fb.fp8bq_workspace_bytes(fb.OP_GEMM, 4096, 6144, 6144)
     assert big >= 80 * 256 * 1024
-    assert fb.fp8bq_workspace_bytes(fb.OP_GEMM, 256, 512, 2048) >= 2 * 256 * 1024
-    assert fb.fp8bq_workspace_bytes(fb.OP_GEMM, 256, 512, 2048) < 3 * 256 * 1024
+    assert fb.fp8bq_workspace_bytes(fb.OP_GEMM, 256, 512, 2048) >= 12 * 256 * 1024
+    assert fb.fp8bq_workspace_bytes(fb.OP_GEMM, 256, 512, 2048) < 13 * 256 * 1024
+    assert fb.fp8bq_workspace_bytes(fb.OP_GEMM, 300, 1000, 6016) >= 48 * 256 * 1024
     assert fb.fp8bq_workspace_bytes(fb.OP_LINEAR, 4096, 6144, 6144) >= big + 4096 * 6144
     # other GEMMs keep no such partials
     assert fb.fp8bq_workspace_bytes(fb.OP_CHANNEL_GEMM, 4096, 6144, 6144) < 1024 * 1024

@@ -129,8 +129,19 @@ def test_gemm_split_tail_tiles(M, N, K, layout):
     bias = si.f32_to_bf16_bits(np.linspace(-3, 3, N).astype(np.float32))
     ws = fb.new_workspace(fb.OP_GEMM, M, N, K)
     ys = [_gemm(qa, sa, qw, sw, bias=bias, layout=layout, ws=ws) for _ in range(3)]
-    check_close(ys[0], oracle.gemm_block(qa, sa, qw, sw, bias=bias), f"split tail {M}x{N}x{K}")
+    ref = oracle.gemm_block(qa, sa, qw, sw, bias=bias)
+    check_close(ys[0], ref, f"split tail {M}x{N}x{K}")
     assert np.array_equal(ys[0], ys[1]) and np.array_equal(ys[1], ys[2])
+    # the no-allocation entry point has no room for the partials and runs the
+    # tiles whole: the same result within the tolerance, a different FP32
+    # summation order (so the split path did run)
+    if layout == fb.SCALE_ROW_MAJOR:
+        y1 = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+        fb.fp8bq_gemm_noalloc(dev(qa), dev(sa), dev(qw), dev(sw), y1, bias=dev(bias))
+        torch.cuda.synchronize()
+        y_whole = host(y1)
+        check_close(y_whole, ref, f"whole tiles {M}x{N}x{K}")
+        assert not np.array_equal(y_whole, ys[0])
 
 
 @pytest.mark.parametrize("M,N,K", [(16, 384, 256), (1, 6144, 6144), (64, 6144, 6144),
