@@ -450,7 +450,7 @@ def gemm_block_ue8m0_sampled(qa, ua, qw, uw, rows, cols, bias=None,
 def row_expert_contiguous(offsets, T: int) -> np.ndarray:
     """Expert of each row when rows are sorted by expert: rows offsets[e] ..
     offsets[e+1]-1 belong to expert e; rows outside every range get -1."""
-    off = np.asarray(offsets, np.int64)
+    off = np.clip(np.asarray(offsets, np.int64), 0, T)   # bounds outside [0, T] clamp
     r = np.full(T, -1, np.int32)
     for e in range(off.size - 1):
         r[off[e]:off[e + 1]] = e
@@ -460,10 +460,10 @@ def row_expert_contiguous(offsets, T: int) -> np.ndarray:
 def row_expert_masked(masked_m, max_m: int) -> np.ndarray:
     """Expert of each row of the masked layout [E, max_m, K]: the first
     masked_m[e] rows of slot e belong to expert e, the rest to none (-1)."""
-    m = np.asarray(masked_m, np.int64)
+    m = np.clip(np.asarray(masked_m, np.int64), 0, max_m)  # counts clamp to [0, max_m]
     r = np.full(m.size * max_m, -1, np.int32)
     for e in range(m.size):
-        r[e * max_m:e * max_m + min(int(m[e]), max_m)] = e
+        r[e * max_m:e * max_m + int(m[e])] = e
     return r
 
 

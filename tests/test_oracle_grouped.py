@@ -84,3 +84,12 @@ def test_masked_layout_rows_and_sampled():
     cols = np.array([0, 127, 5, 64, 64], np.int64)
     np.testing.assert_array_equal(oracle.gemm_grouped_sampled(qa, sa, qw, sw, re, rows, cols),
                                   y[rows, cols])
+
+
+def test_row_expert_helpers_clamp_out_of_range_bounds():
+    """Segment bounds outside [0, T] and masked counts outside [0, max_m] are
+    clamped, the reading the C interface documents for both layouts."""
+    assert list(oracle.row_expert_contiguous([3, 5, 9], 7)) == [-1, -1, -1, 0, 0, 1, 1]
+    assert list(oracle.row_expert_contiguous([-4, 2, 2], 4)) == [0, 0, -1, -1]
+    assert list(oracle.row_expert_masked([-2, 9], 3)) == [-1, -1, -1, 1, 1, 1]
+    assert list(oracle.row_expert_masked([0, 1], 2)) == [-1, -1, 1, -1]
