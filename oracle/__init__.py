@@ -113,6 +113,15 @@ def _c(a, dtype):
     return np.ascontiguousarray(a, dtype=dtype)
 
 
+def _check_samples(rows, cols, M: int, N: int) -> None:
+    """The C routines index with the sample coordinates unchecked, so reject
+    any outside the [M, N] output before they reach it."""
+    if rows.shape != cols.shape:
+        raise ValueError(f"rows {rows.shape} and cols {cols.shape} differ")
+    if rows.size and (rows.min() < 0 or rows.max() >= M or cols.min() < 0 or cols.max() >= N):
+        raise ValueError(f"sample coordinates outside the {M} x {N} output")
+
+
 # --------------------------------------------------------------------------
 # number formats
 # --------------------------------------------------------------------------
@@ -294,6 +303,7 @@ def gemm_block_sampled(qa, sa, qw, sw, rows, cols, bias=None, bn: int = 128,
     M, K = qa.shape
     N = qw.shape[0]
     b = _bias(bias)
+    _check_samples(rows, cols, M, N)
     y = np.empty(rows.size, np.float64)
     lib().orc_gemm_block_sampled(_p(qa), _p(sa), _p(qw), _p(sw), _p(b), M, N, K, bn,
                                  bk, _p(rows), _p(cols), rows.size, _p(y),
@@ -321,6 +331,7 @@ def gemm_mx_sampled(qa, ua, qw, uw, rows, cols, bias=None,
     M, K = qa.shape
     N = qw.shape[0]
     b = _bias(bias)
+    _check_samples(rows, cols, M, N)
     y = np.empty(rows.size, np.float64)
     lib().orc_gemm_mx_sampled(_p(qa), _p(ua), _p(qw), _p(uw), _p(b), M, N, K,
                               _p(rows), _p(cols), rows.size, _p(y),
@@ -352,6 +363,7 @@ def gemm_static_sampled(qa, s_x, qw, s_part, part_sizes, rows, cols, bias=None,
     M, K = qa.shape
     N = qw.shape[0]
     b = _bias(bias)
+    _check_samples(rows, cols, M, N)
     y = np.empty(rows.size, np.float64)
     lib().orc_gemm_static_sampled(_p(qa), float(np.float32(s_x)), _p(qw), _p(s_part),
                                   _p(parts), parts.size, _p(b), M, N, K, _p(rows),
@@ -393,6 +405,7 @@ def gemm_channel_sampled(qa, sa, qw, sw, rows, cols, bias=None,
     M, K = qa.shape
     N = qw.shape[0]
     b = _bias(bias)
+    _check_samples(rows, cols, M, N)
     y = np.empty(rows.size, np.float64)
     lib().orc_gemm_channel_sampled(_p(qa), _p(sa), _p(qw), _p(sw), _p(b), M, N, K, _p(rows),
                                    _p(cols), rows.size, _p(y), threads or default_threads())
@@ -491,6 +504,7 @@ def gemm_grouped_sampled(qa, sa, qw, sw, row_expert, rows, cols,
     rows, cols = _c(rows, np.int64), _c(cols, np.int64)
     M, K = qa.shape
     E, N, _ = qw.shape
+    _check_samples(rows, cols, M, N)
     y = np.empty(rows.size, np.float64)
     lib().orc_gemm_grouped_sampled(_p(qa), _p(sa), _p(qw), _p(sw), _p(re), M, N, K, _p(rows),
                                    _p(cols), rows.size, _p(y), threads or default_threads())

@@ -190,3 +190,11 @@ def test_static_gemm_is_channelwise_scaled_matmul():
     cols = rng.integers(0, 128, 50)
     assert np.array_equal(oracle.gemm_static_sampled(qa, s_x, qw, sp, parts, rows, cols),
                           y[rows, cols])
+
+
+def test_sampled_rejects_coordinates_outside_the_output():
+    qa, sa = oracle.quant_group(si.activations(3, 128))
+    qw, sw = oracle.quant_weight_block(si.weights(130, 128))
+    for rows, cols in (([3], [0]), ([0], [130]), ([-1], [0]), ([0, 1], [0])):
+        with pytest.raises(ValueError):
+            oracle.gemm_block_sampled(qa, sa, qw, sw, np.array(rows), np.array(cols))
