@@ -192,6 +192,30 @@ def test_static_gemm_is_channelwise_scaled_matmul():
                           y[rows, cols])
 
 
+
+def test_mx_and_static_bias_adds_the_decoded_bf16_per_column():
+    """A BF16 bias adds its decoded value to every row of its output column, in
+    the MX and static GEMMs alike; the sampled forms carry it too."""
+    M, N, K = 4, 96, 128
+    bias = si.f32_to_bf16_bits(np.linspace(-3, 3, N).astype(np.float32))
+    b = si.bf16_bits_to_f32(bias).astype(np.float64)[None, :]
+    rows, cols = np.array([0, 3, 1, 2]), np.array([0, 95, 47, 10])
+    qa, ua = oracle.quant_mx(si.activations(M, K))
+    qw, uw = oracle.quant_mx(si.weights(N, K))
+    y0, y1 = oracle.gemm_mx(qa, ua, qw, uw), oracle.gemm_mx(qa, ua, qw, uw, bias=bias)
+    np.testing.assert_allclose(y1 - y0, np.broadcast_to(b, (M, N)), rtol=0, atol=1e-12)
+    assert np.array_equal(oracle.gemm_mx_sampled(qa, ua, qw, uw, rows, cols, bias=bias),
+                          y1[rows, cols])
+    s_x = oracle.absmax_scale(si.calibration(32, K))
+    qs = oracle.quant_static(si.activations(M, K, outliers=False), s_x)
+    parts = [64, 32]
+    qws, sp = oracle.quant_weight_static(si.weights(N, K), parts)
+    z0 = oracle.gemm_static(qs, s_x, qws, sp, parts)
+    z1 = oracle.gemm_static(qs, s_x, qws, sp, parts, bias=bias)
+    np.testing.assert_allclose(z1 - z0, np.broadcast_to(b, (M, N)), rtol=0, atol=1e-12)
+    assert np.array_equal(oracle.gemm_static_sampled(qs, s_x, qws, sp, parts, rows, cols,
+                                                     bias=bias), z1[rows, cols])
+
 def test_sampled_rejects_coordinates_outside_the_output():
     qa, sa = oracle.quant_group(si.activations(3, 128))
     qw, sw = oracle.quant_weight_block(si.weights(130, 128))
