@@ -44,9 +44,62 @@ def check_close(y, ref, what=""):
     assert np.all(np.isfinite(y))
 
 
-def sample_indices(M, N, n, seed=0):
-    """n (row, col) pairs covering the first/last rows and columns and random ones."""
+def sample_indices(M, N, seed=0, per_block=4, block=128):
+    """Output coordinates that cover every block x block tile of an M x N
+    output: each tile's four corners (clipped to the matrix) and `per_block`
+    random elements inside it.  Every 128 x 128 promotion block -- and so every
+    tile of every kernel form, whose tiles are unions of such blocks -- has
+    checked elements, including the ragged last row and column of tiles."""
     rng = np.random.default_rng(seed)
-    rows = np.concatenate([[0, M - 1, 0, M - 1], rng.integers(0, M, n - 4)])
-    cols = np.concatenate([[0, 0, N - 1, N - 1], rng.integers(0, N, n - 4)])
-    return rows.astype(np.int64), cols.astype(np.int64)
+    rows, cols = [], []
+    for r0 in range(0, M, block):
+        r1 = min(M, r0 + block) - 1
+        for c0 in range(0, N, block):
+            c1 = min(N, c0 + block) - 1
+            rows += [r0, r0, r1, r1]
+            cols += [c0, c1, c0, c1]
+            rows += list(rng.integers(r0, r1 + 1, per_block))
+            cols += list(rng.integers(c0, c1 + 1, per_block))
+    return np.asarray(rows, np.int64), np.asarray(cols, np.int64)
+
+
+def assert_covers_every_block(rows, cols, M, N, block=128):
+    """Every block x block tile of the output holds at least one sample."""
+    hit = np.zeros((-(-M // block), -(-N // block)), bool)
+    hit[rows // block, cols // block] = True
+    assert hit.all(), f"{(~hit).sum()} output blocks without a checked element"
+
+
+# ------------------------------------------------------------ guard bands
+#
+# compute-sanitizer is not available on the GPU pool, so writes past the end of
+# an output are caught with canaries: the output is a view into the middle of a
+# larger buffer whose bytes before and after it hold a known pattern, checked
+# after the call.  The view starts on a 256-byte boundary, like an allocation.
+
+GUARD_BYTES = 4096
+CANARY = 0xA5
+
+
+class Guarded:
+    """An output tensor of `shape` and `dtype` with canary bands on both sides."""
+
+    def __init__(self, shape, dtype, fill=None, device="cuda"):
+        elem = torch.empty((), dtype=dtype).element_size()
+        n = int(np.prod(shape)) if len(shape) else 1
+        body = -(-n * elem // 256) * 256
+        self.buf = torch.full((GUARD_BYTES + body + GUARD_BYTES,), CANARY, dtype=torch.uint8,
+                              device=device)
+        self.lo, self.hi = GUARD_BYTES, GUARD_BYTES + n * elem
+        self.t = self.buf[self.lo:self.hi].view(dtype).view(shape)
+        if fill is not None:
+            self.t.fill_(fill)
+
+    def check(self, what=""):
+        b = self.buf.cpu().numpy()
+        before, after = b[:self.lo], b[self.hi:]
+        bad_b = np.flatnonzero(before != CANARY)
+        bad_a = np.flatnonzero(after != CANARY)
+        assert bad_b.size == 0, f"{what}: {bad_b.size} bytes written before the output"
+        assert bad_a.size == 0, (f"{what}: {bad_a.size} bytes written past the end of the "
+                                 f"output, first at +{bad_a[0]}")

@@ -8,18 +8,20 @@ import torch
 import block_wise_fp8_gb300 as fb
 import oracle
 import synthetic_inputs as si
-from gpu_util import check_close, dev, host, sample_indices
+from gpu_util import Guarded, assert_covers_every_block, check_close, dev, host, sample_indices
 
 pytestmark = pytest.mark.gpu
 
 
 def _quant(x):
     M, K = x.shape
-    q = torch.empty(M, K, dtype=torch.uint8, device="cuda")
-    s = torch.empty(M, dtype=torch.float32, device="cuda")
-    fb.fp8bq_channel_quant_act(dev(x), q, s)
+    q = Guarded((M, K), torch.uint8)
+    s = Guarded((M,), torch.float32)
+    fb.fp8bq_channel_quant_act(dev(x), q.t, s.t)
     torch.cuda.synchronize()
-    return q.cpu().numpy(), s.cpu().numpy()
+    q.check("per-token codes")
+    s.check("per-token scales")
+    return q.t.cpu().numpy(), s.t.cpu().numpy()
 
 
 @pytest.mark.parametrize("M,K", [(1, 6144), (5, 208), (130, 4096), (3, 16), (2, 20480),
@@ -44,12 +46,15 @@ def test_channel_quant_zero_rows():
 def _gemm(qa, sa, qw, sw, bias=None):
     M, K = qa.shape
     N = qw.shape[0]
-    y = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
-    ws = fb.new_workspace(fb.OP_CHANNEL_GEMM, M, N, K)
-    fb.fp8bq_channel_gemm(dev(qa), dev(sa), dev(qw), dev(sw), y, ws,
+    y = Guarded((M, N), torch.bfloat16, fill=float("nan"))
+    ws = Guarded((fb.fp8bq_workspace_bytes(fb.OP_CHANNEL_GEMM, M, N, K),), torch.uint8)
+    fb.fp8bq_workspace_init(ws.t)
+    fb.fp8bq_channel_gemm(dev(qa), dev(sa), dev(qw), dev(sw), y.t, ws.t,
                           bias=None if bias is None else dev(bias))
-    assert fb.fp8bq_poll_status(ws) == 0
-    return host(y)
+    assert fb.fp8bq_poll_status(ws.t) == 0
+    y.check(f"channel y {M}x{N}x{K}")
+    ws.check(f"channel workspace {M}x{N}x{K}")
+    return host(y.t)
 
 
 def _operands(M, N, K, seed=0):
@@ -81,18 +86,20 @@ def test_channel_gemm_decode_sampled(M):
     K = N = si.DECODE["K"]
     qa, sa, qw, sw = _operands(M, N, K, seed=7)
     y = _gemm(qa, sa, qw, sw)
-    rows, cols = sample_indices(M, N, 3000)
+    rows, cols = sample_indices(M, N, per_block=32)
+    assert_covers_every_block(rows, cols, M, N)
     check_close(y[rows, cols], oracle.gemm_channel_sampled(qa, sa, qw, sw, rows, cols),
                 f"channel decode M={M}")
     assert np.all(np.isfinite(y))
 
 
-def test_channel_gemm_prefill_sampled():
+@pytest.mark.parametrize("N", si.PREFILL["N_list"])
+def test_channel_gemm_prefill_sampled(N):
     M, K = si.PREFILL["M"], si.PREFILL["K"]
-    N = si.PREFILL["N_list"][0]
     qa, sa, qw, sw = _operands(M, N, K, seed=9)
     y = _gemm(qa, sa, qw, sw)
-    rows, cols = sample_indices(M, N, 4000)
+    rows, cols = sample_indices(M, N)
+    assert_covers_every_block(rows, cols, M, N)
     check_close(y[rows, cols], oracle.gemm_channel_sampled(qa, sa, qw, sw, rows, cols),
                 "channel prefill")
     assert np.all(np.isfinite(y))
@@ -104,9 +111,12 @@ def test_channel_linear_with_bias(M):
     x = si.activations(M, K)
     qw, sw = oracle.quant_channel(si.weights(N, K))
     bias = si.f32_to_bf16_bits(np.linspace(-2, 2, N).astype(np.float32))
-    y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
-    ws = fb.new_workspace(fb.OP_CHANNEL_LINEAR, M, N, K)
-    fb.fp8bq_channel_linear(dev(x), dev(qw), dev(sw), y, ws, bias=dev(bias))
-    assert fb.fp8bq_poll_status(ws) == 0
+    y = Guarded((M, N), torch.bfloat16)
+    ws = Guarded((fb.fp8bq_workspace_bytes(fb.OP_CHANNEL_LINEAR, M, N, K),), torch.uint8)
+    fb.fp8bq_workspace_init(ws.t)
+    fb.fp8bq_channel_linear(dev(x), dev(qw), dev(sw), y.t, ws.t, bias=dev(bias))
+    assert fb.fp8bq_poll_status(ws.t) == 0
+    y.check("channel linear y")
+    ws.check("channel linear workspace")
     qa, sa = oracle.quant_channel(x)
-    check_close(host(y), oracle.gemm_channel(qa, sa, qw, sw, bias=bias), f"channel linear M={M}")
+    check_close(host(y.t), oracle.gemm_channel(qa, sa, qw, sw, bias=bias), f"channel linear M={M}")

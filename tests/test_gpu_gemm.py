@@ -13,7 +13,7 @@ import torch
 import block_wise_fp8_gb300 as fb
 import oracle
 import synthetic_inputs as si
-from gpu_util import check_close, dev, host, sample_indices
+from gpu_util import Guarded, assert_covers_every_block, check_close, dev, host, sample_indices
 
 pytestmark = pytest.mark.gpu
 
@@ -31,13 +31,21 @@ def _gemm(qa, sa, qw, sw, bias=None, layout=fb.SCALE_ROW_MAJOR, ws=None):
         sa_dev[:, :M] = sa.T
     else:
         sa_dev = sa
-    y = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    # the output and a fresh workspace sit between canary bands: a write past
+    # either end fails the call
+    y = Guarded((M, N), torch.bfloat16, fill=float("nan"))
+    g_ws = None
     if ws is None:
-        ws = fb.new_workspace(fb.OP_GEMM, M, N, K)
-    fb.fp8bq_gemm(dev(qa), dev(sa_dev), dev(qw), dev(sw), y, ws,
+        g_ws = Guarded((fb.fp8bq_workspace_bytes(fb.OP_GEMM, M, N, K),), torch.uint8)
+        ws = g_ws.t
+        fb.fp8bq_workspace_init(ws)
+    fb.fp8bq_gemm(dev(qa), dev(sa_dev), dev(qw), dev(sw), y.t, ws,
                   bias=None if bias is None else dev(bias), s_layout=layout)
     assert fb.fp8bq_poll_status(ws) == 0
-    return host(y)
+    y.check(f"y {M}x{N}x{K}")
+    if g_ws is not None:
+        g_ws.check(f"workspace {M}x{N}x{K}")
+    return host(y.t)
 
 
 @pytest.mark.parametrize("M,N,K", [(16, 384, 256), (5, 200, 208), (1, 128, 128),
@@ -68,12 +76,12 @@ def test_gemm_prefill_sampled(N):
     qa, sa = oracle.quant_group(si.activations(M, K))
     qw, sw = _weights(N, K)
     y = _gemm(qa, sa, qw, sw)
-    rows, cols = sample_indices(M, N, 3000)
+    # every 128 x 128 output block: its corners and 4 random elements
+    rows, cols = sample_indices(M, N)
+    assert_covers_every_block(rows, cols, M, N)
     ref = oracle.gemm_block_sampled(qa, sa, qw, sw, rows, cols)
     check_close(y[rows, cols], ref, f"prefill N={N}")
-    # whole-output properties: finite everywhere, and the RMS matches the sample
     assert np.all(np.isfinite(y))
-    assert abs(np.sqrt(np.mean(y ** 2)) / np.sqrt(np.mean(ref ** 2)) - 1) < 0.1
 
 
 def test_gemm_bias():
@@ -151,15 +159,18 @@ def test_linear_matches_oracle(M, N, K):
     qw, sw = _weights(N, K)
     qa, sa = oracle.quant_group(x)
     xd = dev(x)
-    y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
-    ws = fb.new_workspace(fb.OP_LINEAR, M, N, K)
-    fb.fp8bq_linear(xd, dev(qw), dev(sw), y, ws)
-    assert fb.fp8bq_poll_status(ws) == 0
-    yh = host(y)
+    y = Guarded((M, N), torch.bfloat16)
+    g_ws = Guarded((fb.fp8bq_workspace_bytes(fb.OP_LINEAR, M, N, K),), torch.uint8)
+    fb.fp8bq_workspace_init(g_ws.t)
+    fb.fp8bq_linear(xd, dev(qw), dev(sw), y.t, g_ws.t)
+    assert fb.fp8bq_poll_status(g_ws.t) == 0
+    y.check("linear y")
+    g_ws.check("linear workspace")
+    yh = host(y.t)
     if M * N * K <= 64 * 6144 * 6144:
         check_close(yh, oracle.gemm_block(qa, sa, qw, sw), f"linear {M}x{N}x{K}")
     else:
-        rows, cols = sample_indices(M, N, 2000)
+        rows, cols = sample_indices(M, N)
         check_close(yh[rows, cols], oracle.gemm_block_sampled(qa, sa, qw, sw, rows, cols),
                     f"linear {M}x{N}x{K}")
 

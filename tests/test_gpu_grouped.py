@@ -10,7 +10,7 @@ import torch
 import block_wise_fp8_gb300 as fb
 import oracle
 import synthetic_inputs as si
-from gpu_util import check_close, dev, host, sample_indices
+from gpu_util import Guarded, assert_covers_every_block, check_close, dev, host, sample_indices
 
 pytestmark = pytest.mark.gpu
 
@@ -42,13 +42,16 @@ def _acts(T, K, seed=0, layout=fb.SCALE_ROW_MAJOR):
 def _run_contiguous(qa, sa_dev_layout, qw, sw, offsets, layout=fb.SCALE_ROW_MAJOR):
     T, K = qa.shape
     E, N, _ = qw.shape
-    y = torch.full((T, N), float("nan"), dtype=torch.bfloat16, device="cuda")
-    ws = fb.new_workspace(fb.OP_GROUPED_GEMM, T, N, K)
+    y = Guarded((T, N), torch.bfloat16, fill=float("nan"))
+    ws = Guarded((fb.fp8bq_workspace_bytes(fb.OP_GROUPED_GEMM, T, N, K),), torch.uint8)
+    fb.fp8bq_workspace_init(ws.t)
     off = torch.tensor(np.asarray(offsets, np.int32), device="cuda")
-    fb.fp8bq_grouped_gemm(dev(qa), dev(sa_dev_layout), dev(qw), dev(sw), off, y, ws,
+    fb.fp8bq_grouped_gemm(dev(qa), dev(sa_dev_layout), dev(qw), dev(sw), off, y.t, ws.t,
                           s_layout=layout)
-    assert fb.fp8bq_poll_status(ws) == 0
-    return host(y)
+    assert fb.fp8bq_poll_status(ws.t) == 0
+    y.check(f"grouped y {T}x{N}x{K}")
+    ws.check(f"grouped workspace {T}x{N}x{K}")
+    return host(y.t)
 
 
 def _check_rows(y, ref, row_expert, what):
@@ -119,13 +122,16 @@ def test_grouped_masked():
     T = E * max_m
     qa, _, sa = _acts(T, K, seed=4)
     qw, sw = _experts(E, N, K, seed=5)
-    y = torch.full((E, max_m, N), float("nan"), dtype=torch.bfloat16, device="cuda")
-    ws = fb.new_workspace(fb.OP_GROUPED_GEMM, T, N, K)
+    y = Guarded((E, max_m, N), torch.bfloat16, fill=float("nan"))
+    ws = Guarded((fb.fp8bq_workspace_bytes(fb.OP_GROUPED_GEMM, T, N, K),), torch.uint8)
+    fb.fp8bq_workspace_init(ws.t)
     fb.fp8bq_grouped_gemm_masked(dev(qa).view(E, max_m, K), dev(sa), dev(qw), dev(sw),
-                                 torch.tensor(masked, device="cuda"), y, ws)
-    assert fb.fp8bq_poll_status(ws) == 0
+                                 torch.tensor(masked, device="cuda"), y.t, ws.t)
+    assert fb.fp8bq_poll_status(ws.t) == 0
+    y.check("grouped masked y")
+    ws.check("grouped masked workspace")
     re = oracle.row_expert_masked(masked, max_m)
-    _check_rows(host(y).reshape(T, N), oracle.gemm_grouped(qa, sa, qw, sw, re), re,
+    _check_rows(host(y.t).reshape(T, N), oracle.gemm_grouped(qa, sa, qw, sw, re), re,
                 "grouped masked")
 
 
@@ -165,7 +171,8 @@ def test_grouped_moe_workload_sampled(which):
     y = _run_contiguous(qa, sa, qw, sw, off)
     assert np.all(np.isfinite(y))
     re = oracle.row_expert_contiguous(off, T)
-    rows, cols = sample_indices(T, N, 3000)
+    rows, cols = sample_indices(T, N)
+    assert_covers_every_block(rows, cols, T, N)
     # also the first and last row of every expert
     rows = np.concatenate([rows, off[:-1][counts > 0], off[1:][counts > 0] - 1]).astype(np.int64)
     cols = np.concatenate([cols, np.arange(2 * int((counts > 0).sum())) * 97 % N]).astype(np.int64)

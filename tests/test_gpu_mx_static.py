@@ -7,7 +7,7 @@ import torch
 import block_wise_fp8_gb300 as fb
 import oracle
 import synthetic_inputs as si
-from gpu_util import check_close, dev, host, sample_indices
+from gpu_util import Guarded, assert_covers_every_block, check_close, dev, host, sample_indices
 
 pytestmark = pytest.mark.gpu
 
@@ -17,12 +17,15 @@ pytestmark = pytest.mark.gpu
 def _mx_gemm(qa, ua, qw, uw, bias=None):
     M, K = qa.shape
     N = qw.shape[0]
-    y = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
-    ws = fb.new_workspace(fb.OP_MX_GEMM, M, N, K)
-    fb.fp8bq_mx_gemm(dev(qa), dev(ua), dev(qw), dev(uw), y, ws,
+    y = Guarded((M, N), torch.bfloat16, fill=float("nan"))
+    ws = Guarded((fb.fp8bq_workspace_bytes(fb.OP_MX_GEMM, M, N, K),), torch.uint8)
+    fb.fp8bq_workspace_init(ws.t)
+    fb.fp8bq_mx_gemm(dev(qa), dev(ua), dev(qw), dev(uw), y.t, ws.t,
                      bias=None if bias is None else dev(bias))
-    assert fb.fp8bq_poll_status(ws) == 0
-    return host(y)
+    assert fb.fp8bq_poll_status(ws.t) == 0
+    y.check(f"mx y {M}x{N}x{K}")
+    ws.check(f"mx workspace {M}x{N}x{K}")
+    return host(y.t)
 
 
 def test_mx_gemm_unit_scales():
@@ -61,7 +64,8 @@ def test_mx_gemm_workload_sampled():
     qa, ua = oracle.quant_mx(si.activations(M, K))
     qw, uw = oracle.quant_mx(si.weights(N, K))
     y = _mx_gemm(qa, ua, qw, uw)
-    rows, cols = sample_indices(M, N, 3000)
+    rows, cols = sample_indices(M, N)
+    assert_covers_every_block(rows, cols, M, N)
     check_close(y[rows, cols], oracle.gemm_mx_sampled(qa, ua, qw, uw, rows, cols),
                 "mx 2048x4096x7168")
     assert np.all(np.isfinite(y))
@@ -72,12 +76,15 @@ def test_mx_linear_and_bias():
     x = si.activations(M, K)
     qw, uw = oracle.quant_mx(si.weights(N, K))
     bias = si.f32_to_bf16_bits(np.linspace(-2, 2, N).astype(np.float32))
-    y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
-    ws = fb.new_workspace(fb.OP_MX_LINEAR, M, N, K)
-    fb.fp8bq_mx_linear(dev(x), dev(qw), dev(uw), y, ws, bias=dev(bias))
-    assert fb.fp8bq_poll_status(ws) == 0
+    y = Guarded((M, N), torch.bfloat16)
+    ws = Guarded((fb.fp8bq_workspace_bytes(fb.OP_MX_LINEAR, M, N, K),), torch.uint8)
+    fb.fp8bq_workspace_init(ws.t)
+    fb.fp8bq_mx_linear(dev(x), dev(qw), dev(uw), y.t, ws.t, bias=dev(bias))
+    assert fb.fp8bq_poll_status(ws.t) == 0
+    y.check("mx linear y")
+    ws.check("mx linear workspace")
     qa, ua = oracle.quant_mx(x)
-    check_close(host(y), oracle.gemm_mx(qa, ua, qw, uw, bias=bias), "mx linear")
+    check_close(host(y.t), oracle.gemm_mx(qa, ua, qw, uw, bias=bias), "mx linear")
 
 
 # ------------------------------------------------------------------ static per-tensor
@@ -96,13 +103,16 @@ def static_weights():
 def _static_gemm(qa, s_x, qw, sp, parts, bias=None):
     M, K = qa.shape
     N = qw.shape[0]
-    y = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
-    ws = fb.new_workspace(fb.OP_STATIC_GEMM, M, N, K)
+    y = Guarded((M, N), torch.bfloat16, fill=float("nan"))
+    ws = Guarded((fb.fp8bq_workspace_bytes(fb.OP_STATIC_GEMM, M, N, K),), torch.uint8)
+    fb.fp8bq_workspace_init(ws.t)
     sxd = torch.tensor([s_x], dtype=torch.float32, device="cuda")
-    fb.fp8bq_static_gemm(dev(qa), sxd, dev(qw), dev(sp), parts, y, ws,
+    fb.fp8bq_static_gemm(dev(qa), sxd, dev(qw), dev(sp), parts, y.t, ws.t,
                          bias=None if bias is None else dev(bias))
-    assert fb.fp8bq_poll_status(ws) == 0
-    return host(y)
+    assert fb.fp8bq_poll_status(ws.t) == 0
+    y.check(f"static y {M}x{N}x{K}")
+    ws.check(f"static workspace {M}x{N}x{K}")
+    return host(y.t)
 
 
 @pytest.mark.parametrize("M", [1, 512, 4096])
@@ -114,7 +124,8 @@ def test_static_gemm_workload(static_weights, M):
     if M == 1:
         check_close(y, oracle.gemm_static(qa, s_x, qw, sp, PARTS), "static M=1")
     else:
-        rows, cols = sample_indices(M, N, 2000)
+        rows, cols = sample_indices(M, N)
+        assert_covers_every_block(rows, cols, M, N)
         # columns on both sides of each partition boundary
         edge = np.array([4095, 4096, 8191, 8192, 14335], np.int64)
         rows = np.concatenate([rows, np.zeros(5, np.int64), np.full(5, M - 1)])
@@ -138,10 +149,13 @@ def test_static_linear(static_weights):
     qw, sp, s_x = static_weights
     M, K, N = 33, si.STATIC["K"], si.STATIC["N"]
     x = si.activations(M, K)
-    y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
-    ws = fb.new_workspace(fb.OP_STATIC_LINEAR, M, N, K)
+    y = Guarded((M, N), torch.bfloat16)
+    ws = Guarded((fb.fp8bq_workspace_bytes(fb.OP_STATIC_LINEAR, M, N, K),), torch.uint8)
+    fb.fp8bq_workspace_init(ws.t)
     sxd = torch.tensor([s_x], dtype=torch.float32, device="cuda")
-    fb.fp8bq_static_linear(dev(x), sxd, dev(qw), dev(sp), PARTS, y, ws)
-    assert fb.fp8bq_poll_status(ws) == 0
+    fb.fp8bq_static_linear(dev(x), sxd, dev(qw), dev(sp), PARTS, y.t, ws.t)
+    assert fb.fp8bq_poll_status(ws.t) == 0
+    y.check("static linear y")
+    ws.check("static linear workspace")
     qa = oracle.quant_static(x, s_x)
-    check_close(host(y), oracle.gemm_static(qa, s_x, qw, sp, PARTS), "static linear")
+    check_close(host(y.t), oracle.gemm_static(qa, s_x, qw, sp, PARTS), "static linear")

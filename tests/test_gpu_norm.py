@@ -8,7 +8,7 @@ import torch
 import block_wise_fp8_gb300 as fb
 import oracle
 import synthetic_inputs as si
-from gpu_util import dev
+from gpu_util import Guarded, dev
 
 pytestmark = pytest.mark.gpu
 
@@ -34,15 +34,21 @@ def _run_group(x, g, res=None, s_layout=fb.SCALE_ROW_MAJOR, in_place=False):
     M, K = x.shape
     dx = dev(x)
     dres = None if res is None else dev(res)
-    r_out = dres if in_place else torch.empty(M, K, dtype=torch.bfloat16, device="cuda")
-    y = torch.empty(M, K, dtype=torch.bfloat16, device="cuda")
-    q = torch.empty(M, K, dtype=torch.uint8, device="cuda")
+    # every output between canary bands
+    g_r = None if in_place else Guarded((M, K), torch.bfloat16)
+    r_out = dres if in_place else g_r.t
+    g_y = Guarded((M, K), torch.bfloat16)
+    g_q = Guarded((M, K), torch.uint8)
     G = (K + 127) // 128
-    s = torch.empty((M, G) if s_layout == fb.SCALE_ROW_MAJOR else (G, (M + 3) // 4 * 4),
-                    dtype=torch.float32, device="cuda")
+    g_s = Guarded((M, G) if s_layout == fb.SCALE_ROW_MAJOR else (G, (M + 3) // 4 * 4),
+                  torch.float32)
+    y, q, s = g_y.t, g_q.t, g_s.t
     fb.fp8bq_add_rmsnorm_quant_act(dx, dev(g), EPS, residual=dres, residual_out=r_out, y=y,
                                    q=q, s=s, s_layout=s_layout)
     torch.cuda.synchronize()
+    for name, gb in (("residual_out", g_r), ("y", g_y), ("q", g_q), ("s", g_s)):
+        if gb is not None:
+            gb.check(f"norm {name} {M}x{K}")
     s_h = s.cpu().numpy()
     if s_layout != fb.SCALE_ROW_MAJOR:
         s_h = s_h[:, :M].T
@@ -143,12 +149,15 @@ def test_static_quant(M, s_val):
         _, yc = oracle.add_rmsnorm(*_inputs(64, K, seed=12)[:1], g, EPS)
         s_val = float(oracle.absmax_scale(yc))
     s_x = torch.tensor([s_val], dtype=torch.float32, device="cuda")
-    q = torch.empty(M, K, dtype=torch.uint8, device="cuda")
-    y = torch.empty(M, K, dtype=torch.bfloat16, device="cuda")
-    r_out = torch.empty_like(y)
+    gq = Guarded((M, K), torch.uint8)
+    gy = Guarded((M, K), torch.bfloat16)
+    gr = Guarded((M, K), torch.bfloat16)
+    q, y, r_out = gq.t, gy.t, gr.t
     fb.fp8bq_add_rmsnorm_static_quant_act(dev(x), dev(g), EPS, s_x, q, residual=dev(res),
                                           residual_out=r_out, y=y)
     torch.cuda.synchronize()
+    for name, gb in (("q", gq), ("y", gy), ("residual_out", gr)):
+        gb.check(f"static norm {name} M={M}")
     r_ref, y_ref = oracle.add_rmsnorm(x, g, EPS, residual=res)
     np.testing.assert_array_equal(_bits(r_out), r_ref)
     np.testing.assert_array_equal(_bits(y), y_ref)
@@ -156,17 +165,17 @@ def test_static_quant(M, s_val):
 
 
 @pytest.mark.parametrize("M,K", [(4096, 6144), (4096, 4096)])
-def test_full_size_sampled_rows(M, K):
-    """Full-size launch; rows are independent, so the oracle runs on a sample."""
+def test_full_size_every_row(M, K):
+    """The full-size launch (persistent CTAs over all rows), every output row
+    checked bit for bit against the oracle."""
     x, res, g = _inputs(M, K, seed=21)
     r, y, q, s = _run_group(x, g, res)
-    rows = np.unique(np.concatenate([[0, M - 1], np.random.default_rng(5).integers(0, M, 60)]))
-    r_ref, y_ref = oracle.add_rmsnorm(x[rows], g, EPS, residual=res[rows])
+    r_ref, y_ref = oracle.add_rmsnorm(x, g, EPS, residual=res)
     q_ref, s_ref = oracle.quant_group(y_ref)
-    np.testing.assert_array_equal(r[rows], r_ref)
-    np.testing.assert_array_equal(y[rows], y_ref)
-    np.testing.assert_array_equal(q[rows], q_ref)
-    np.testing.assert_array_equal(s[rows], s_ref)
+    np.testing.assert_array_equal(r, r_ref)
+    np.testing.assert_array_equal(y, y_ref)
+    np.testing.assert_array_equal(q, q_ref)
+    np.testing.assert_array_equal(s, s_ref)
 
 
 def test_validation():
@@ -176,9 +185,12 @@ def test_validation():
     with pytest.raises(fb.Fp8bqError) as e:
         fb.fp8bq_add_rmsnorm_quant_act(x, g, -1.0, q=q, s=torch.empty(4, 1, device="cuda"))
     assert e.value.name == "FP8BQ_ERR_UNSUPPORTED"
-    with pytest.raises(fb.Fp8bqError) as e:
-        fb.fp8bq_add_rmsnorm_quant_act(x, g, 1e-5, q=q)             # s missing
-    assert e.value.name == "FP8BQ_ERR_NULL"
+    with pytest.raises(ValueError):
+        fb.fp8bq_add_rmsnorm_quant_act(x, g, 1e-5, q=q)             # s missing (binding)
+    st = fb._lib.fp8bq_add_rmsnorm_quant_act(                       # s missing (C ABI)
+        fb._ptr(x), 64, None, 0, None, fb._ptr(g), 1e-5, 4, 64, None, fb._ptr(q), None, 0,
+        fb._stream(None))
+    assert st == 1                                                  # FP8BQ_ERR_NULL
     x2 = torch.zeros(4, 40, dtype=torch.bfloat16, device="cuda")    # K % 16 != 0
     with pytest.raises(fb.Fp8bqError) as e:
         fb.fp8bq_add_rmsnorm_quant_act(x2, torch.ones(40, dtype=torch.bfloat16, device="cuda"),

@@ -8,7 +8,7 @@ import torch
 import block_wise_fp8_gb300 as fb
 import oracle
 import synthetic_inputs as si
-from gpu_util import dev, host
+from gpu_util import Guarded, dev, host
 
 pytestmark = pytest.mark.gpu
 
@@ -21,14 +21,14 @@ def _gpu_quant_group(x, layout=fb.SCALE_ROW_MAJOR, ldx_pad=0):
         wide[:, :K] = xd
         xd = wide[:, :K]
     G = -(-K // 128)
-    q = torch.empty(M, K, dtype=torch.uint8, device="cuda")
-    if layout == fb.SCALE_ROW_MAJOR:
-        s = torch.full((M, G), -1.0, dtype=torch.float32, device="cuda")
-    else:
-        s = torch.full((G, -(-M // 4) * 4), -1.0, dtype=torch.float32, device="cuda")
-    fb.fp8bq_quant_act(xd, q, s, layout)
+    q = Guarded((M, K), torch.uint8)
+    shape = (M, G) if layout == fb.SCALE_ROW_MAJOR else (G, -(-M // 4) * 4)
+    s = Guarded(shape, torch.float32, fill=-1.0)
+    fb.fp8bq_quant_act(xd, q.t, s.t, layout)
     torch.cuda.synchronize()
-    return host(q), host(s)
+    q.check(f"codes {M}x{K}")
+    s.check(f"scales {M}x{K} layout {layout}")
+    return host(q.t), host(s.t)
 
 
 @pytest.mark.parametrize("M,K", [(16, 256), (5, 208), (1, 6144), (8, 6144), (32, 6144),
@@ -102,22 +102,25 @@ def test_static_quant_every_finite_bf16_value(scale):
     pats = np.concatenate([pats, np.zeros((-len(pats)) % 16, np.uint16)])
     x = pats.reshape(-1, 16 * 64) if len(pats) % (16 * 64) == 0 else pats.reshape(-1, 16)
     sx = torch.full((1,), scale, dtype=torch.float32, device="cuda")
-    q = torch.empty(x.shape, dtype=torch.uint8, device="cuda")
-    fb.fp8bq_static_quant_act(dev(x), sx, q)
+    q = Guarded(x.shape, torch.uint8)
+    fb.fp8bq_static_quant_act(dev(x), sx, q.t)
     torch.cuda.synchronize()
-    assert np.array_equal(host(q), oracle.quant_static(x, np.float32(scale)))
+    q.check("static codes")
+    assert np.array_equal(host(q.t), oracle.quant_static(x, np.float32(scale)))
 
 
 @pytest.mark.parametrize("M,K", [(2048, 7168), (5, 96), (64, 7168), (1, 32)])
 def test_quant_mx_bit_exact(M, K):
     x = si.activations(M, K)
-    q = torch.empty(M, K, dtype=torch.uint8, device="cuda")
-    s = torch.empty(M, K // 32, dtype=torch.uint8, device="cuda")
-    fb.fp8bq_mx_quant_act(dev(x), q, s)
+    q = Guarded((M, K), torch.uint8)
+    s = Guarded((M, K // 32), torch.uint8)
+    fb.fp8bq_mx_quant_act(dev(x), q.t, s.t)
     torch.cuda.synchronize()
+    q.check("mx codes")
+    s.check("mx scale codes")
     qr, ur = oracle.quant_mx(x)
-    assert np.array_equal(host(s), ur)
-    assert np.array_equal(host(q), qr)
+    assert np.array_equal(host(s.t), ur)
+    assert np.array_equal(host(q.t), qr)
 
 
 def test_quant_mx_special_groups():
@@ -156,13 +159,15 @@ def test_static_scale_and_quant_bit_exact(M):
 @pytest.mark.parametrize("N,K", [(384, 256), (200, 208), (6144, 6144), (130, 16)])
 def test_weight_block_quant_bit_exact(N, K):
     w = si.weights(N, K)
-    q = torch.empty(N, K, dtype=torch.uint8, device="cuda")
-    s = torch.empty(-(-N // 128), -(-K // 128), dtype=torch.float32, device="cuda")
-    fb.fp8bq_quant_weight_block(dev(w), q, s)
+    q = Guarded((N, K), torch.uint8)
+    s = Guarded((-(-N // 128), -(-K // 128)), torch.float32)
+    fb.fp8bq_quant_weight_block(dev(w), q.t, s.t)
     torch.cuda.synchronize()
+    q.check("weight codes")
+    s.check("weight block scales")
     qr, sr = oracle.quant_weight_block(w)
-    assert np.array_equal(host(s).view(np.uint32), sr.view(np.uint32))
-    assert np.array_equal(host(q), qr)
+    assert np.array_equal(host(s.t).view(np.uint32), sr.view(np.uint32))
+    assert np.array_equal(host(q.t), qr)
 
 
 def test_weight_partition_scales_bit_exact():

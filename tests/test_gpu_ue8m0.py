@@ -9,7 +9,7 @@ import torch
 import block_wise_fp8_gb300 as fb
 import oracle
 import synthetic_inputs as si
-from gpu_util import check_close, dev, host, sample_indices
+from gpu_util import Guarded, assert_covers_every_block, check_close, dev, host, sample_indices
 
 pytestmark = pytest.mark.gpu
 
@@ -17,23 +17,29 @@ pytestmark = pytest.mark.gpu
 @pytest.mark.parametrize("M,K", [(1, 6144), (5, 208), (130, 4096), (3, 16), (4096, 6144)])
 def test_quant_ue8m0_bit_exact(M, K):
     x = si.activations(M, K)
-    q = torch.empty(M, K, dtype=torch.uint8, device="cuda")
-    u = torch.empty(M, (K + 127) // 128, dtype=torch.uint8, device="cuda")
-    fb.fp8bq_quant_act_ue8m0(dev(x), q, u)
+    q = Guarded((M, K), torch.uint8)
+    u = Guarded((M, (K + 127) // 128), torch.uint8)
+    fb.fp8bq_quant_act_ue8m0(dev(x), q.t, u.t)
     torch.cuda.synchronize()
+    q.check("ue8m0 codes")
+    u.check("ue8m0 scale codes")
     q_ref, u_ref = oracle.quant_ue8m0(x, group=128)
-    np.testing.assert_array_equal(u.cpu().numpy(), u_ref)
-    np.testing.assert_array_equal(q.cpu().numpy(), q_ref)
+    np.testing.assert_array_equal(u.t.cpu().numpy(), u_ref)
+    np.testing.assert_array_equal(q.t.cpu().numpy(), q_ref)
 
 
 def _requant(qw, sw, in_place=False):
     N, K = qw.shape
     dq = dev(qw)
-    out = dq if in_place else torch.empty_like(dq)
-    u = torch.empty(sw.shape, dtype=torch.uint8, device="cuda")
-    fb.fp8bq_requant_weight_ue8m0(dq, dev(sw), out, u)
+    g_out = None if in_place else Guarded(tuple(dq.shape), torch.uint8)
+    out = dq if in_place else g_out.t
+    u = Guarded(tuple(sw.shape), torch.uint8)
+    fb.fp8bq_requant_weight_ue8m0(dq, dev(sw), out, u.t)
     torch.cuda.synchronize()
-    return out.cpu().numpy(), u.cpu().numpy()
+    u.check("requant scale codes")
+    if g_out is not None:
+        g_out.check("requant codes")
+    return out.cpu().numpy(), u.t.cpu().numpy()
 
 
 @pytest.mark.parametrize("N,K", [(300, 520), (128, 128), (6144, 6144)])
@@ -63,12 +69,15 @@ def _operands(M, N, K, seed=0):
 def _gemm(qa, ua, qw, uw, bias=None):
     M, K = qa.shape
     N = qw.shape[0]
-    y = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
-    ws = fb.new_workspace(fb.OP_UE8M0_GEMM, M, N, K)
-    fb.fp8bq_ue8m0_gemm(dev(qa), dev(ua), dev(qw), dev(uw), y, ws,
+    y = Guarded((M, N), torch.bfloat16, fill=float("nan"))
+    ws = Guarded((fb.fp8bq_workspace_bytes(fb.OP_UE8M0_GEMM, M, N, K),), torch.uint8)
+    fb.fp8bq_workspace_init(ws.t)
+    fb.fp8bq_ue8m0_gemm(dev(qa), dev(ua), dev(qw), dev(uw), y.t, ws.t,
                         bias=None if bias is None else dev(bias))
-    assert fb.fp8bq_poll_status(ws) == 0
-    return host(y)
+    assert fb.fp8bq_poll_status(ws.t) == 0
+    y.check(f"ue8m0 y {M}x{N}x{K}")
+    ws.check(f"ue8m0 workspace {M}x{N}x{K}")
+    return host(y.t)
 
 
 @pytest.mark.parametrize("M,N,K", [(16, 384, 256), (5, 200, 96), (130, 136, 224),
@@ -90,12 +99,13 @@ def test_ue8m0_gemm_scale_layout():
     check_close(_gemm(qa, ua, qw, uw), oracle.gemm_block_ue8m0(qa, ua, qw, uw), "ue8m0 layout")
 
 
-def test_ue8m0_gemm_prefill_sampled():
+@pytest.mark.parametrize("N", si.PREFILL["N_list"])
+def test_ue8m0_gemm_prefill_sampled(N):
     M, K = si.PREFILL["M"], si.PREFILL["K"]
-    N = si.PREFILL["N_list"][0]
     qa, ua, qw, uw = _operands(M, N, K, seed=5)
     y = _gemm(qa, ua, qw, uw)
-    rows, cols = sample_indices(M, N, 3000)
+    rows, cols = sample_indices(M, N)
+    assert_covers_every_block(rows, cols, M, N)
     check_close(y[rows, cols], oracle.gemm_block_ue8m0_sampled(qa, ua, qw, uw, rows, cols),
                 "ue8m0 prefill")
     assert np.all(np.isfinite(y))
@@ -107,9 +117,12 @@ def test_ue8m0_linear_with_bias():
     qw, sw = oracle.quant_weight_block(si.weights(N, K))
     qw2, uw = oracle.requant_weight_ue8m0(qw, sw)
     bias = si.f32_to_bf16_bits(np.linspace(-2, 2, N).astype(np.float32))
-    y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
-    ws = fb.new_workspace(fb.OP_UE8M0_LINEAR, M, N, K)
-    fb.fp8bq_ue8m0_linear(dev(x), dev(qw2), dev(uw), y, ws, bias=dev(bias))
-    assert fb.fp8bq_poll_status(ws) == 0
+    y = Guarded((M, N), torch.bfloat16)
+    ws = Guarded((fb.fp8bq_workspace_bytes(fb.OP_UE8M0_LINEAR, M, N, K),), torch.uint8)
+    fb.fp8bq_workspace_init(ws.t)
+    fb.fp8bq_ue8m0_linear(dev(x), dev(qw2), dev(uw), y.t, ws.t, bias=dev(bias))
+    assert fb.fp8bq_poll_status(ws.t) == 0
+    y.check("ue8m0 linear y")
+    ws.check("ue8m0 linear workspace")
     qa, ua = oracle.quant_ue8m0(x, group=128)
-    check_close(host(y), oracle.gemm_block_ue8m0(qa, ua, qw2, uw, bias=bias), "ue8m0 linear")
+    check_close(host(y.t), oracle.gemm_block_ue8m0(qa, ua, qw2, uw, bias=bias), "ue8m0 linear")
