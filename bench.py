@@ -59,6 +59,7 @@ PREFILL_NS = si.PREFILL["N_list"]
 FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FP8_PER_BF16 = 2.0   # nominal dense FP8 / BF16 tensor rate
+ORACLE_ROWS = 8      # token rows of a large output that the CPU baseline recomputes
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one prefill
 # block-GEMM launch from an ncu capture, valid only for the kernel sources whose
@@ -199,8 +200,19 @@ def run_ours(args):
 
     stream = torch.cuda.current_stream(dev)
     peaks, peak_src = load_peaks()
-    fp8_peak = peaks["bf16_tflops"] * FP8_PER_BF16
     hbm_peak = peaks["hbm_gbs"]
+    # FP8 dense peak: the larger of 2 x the measured BF16 burst rate (the
+    # nominal FP8 / BF16 ratio) and the vendor's plain FP8 GEMM measured here at
+    # 8192^3 -- the larger denominator keeps every fraction conservative
+    nominal = peaks["bf16_tflops"] * FP8_PER_BF16
+    vendor = vendor_fp8_reference(torch, dev, stream)
+    v8192 = vendor.get("square_8192", {}).get("tflops")
+    fp8_peak = max(nominal, v8192 or 0.0)
+    fp8_src = (f"same-run cuBLASLt FP8 GEMM 8192^3 ({v8192} TFLOP/s)" if v8192 and v8192 > nominal
+               else f"{peak_src}: 2 x bf16 burst {peaks['bf16_tflops']} TFLOP/s")
+    for k in ("prefill_4096x24576x6144", "square_8192"):
+        if k in vendor:
+            vendor[k]["frac_fp8"] = round(vendor[k]["tflops"] / fp8_peak, 4)
 
     def to_dev(bits):
         return torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
@@ -224,15 +236,21 @@ def run_ours(args):
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     flops_step = sum(2.0 * M * K * L["N"] for L in layers)
 
+    nv = torch.cuda.nvtx
+
     def step(ev=None):
         # A1: group-128 activation quantisation (row-major scales)
+        nv.range_push("quant_act 4096x6144")
         fb.fp8bq_quant_act(x, q, sx, fb.SCALE_ROW_MAJOR)
+        nv.range_pop()
         for i, L in enumerate(layers):
             if ev is not None:
                 ev[i][0].record(stream)
             # A2: block-scaled GEMM
+            nv.range_push(f"block GEMM {M}x{L['N']}x{K}")
             fb.fp8bq_gemm(q, sx, L["qw"], L["sw"], L["y"], L["ws"],
                           s_layout=fb.SCALE_ROW_MAJOR)
+            nv.range_pop()
             if ev is not None:
                 ev[i][1].record(stream)
 
@@ -283,16 +301,23 @@ def run_ours(args):
     roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(fp8_peak, 1),
                 "unit": "TFLOP/s", "frac": round(achieved / fp8_peak, 4), "traffic": traffic,
                 "kernel": f"block-scaled GEMM {M}x{layers[j]['N']}x{K}",
-                "peak_source": f"{peak_src}: 2 x bf16 burst {peaks['bf16_tflops']} TFLOP/s",
+                "peak_source": fp8_src,
+                "peak_candidates": {"2x_bf16_burst": round(nominal, 1),
+                                    "vendor_fp8_8192_cubed": v8192},
+                "frac_of_2x_bf16_burst": round(achieved / nominal, 4),
                 "gemm_ms": {str(L["N"]): round(t, 4) for L, t in zip(layers, gemm_ms)},
                 "gemm_ms_p10_p50_p90": {str(L["N"]): pcts(g) for L, g in zip(layers, gemm_lists)}}
 
     # ---- e2e through fp8bq_linear with host buffers
     e2e = run_e2e(fb, torch, dev, stream, layers, x, args, world, rank)
 
-    extra = run_extra(fb, torch, dev, stream, hbm_peak, fp8_peak) if (rank == 0 and
-                                                                     not args.no_extra) else {}
-    cpu = cpu_baseline(args) if (rank == 0 and not args.no_cpu) else None
+    keep = {"prefill": {L["N"]: L["y"][:ORACLE_ROWS].cpu() for L in layers}}
+    extra = run_extra(fb, torch, dev, stream, hbm_peak, fp8_peak, keep) if (
+        rank == 0 and not args.no_extra) else {}
+    extra["vendor_fp8_gemm"] = vendor
+    cpu = cpu_baseline(args, keep) if (rank == 0 and not args.no_cpu) else None
+    records = build_records(M, K, layers, gemm_lists, step_list, flops_step, extra, cpu,
+                            hbm_peak, fp8_peak, achieved) if rank == 0 else []
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOPS", "n_gpus": world,
@@ -311,6 +336,7 @@ def run_ours(args):
         "step_ms_p10_p50_p90": pcts(step_list),
         "gpu_launches": 3 * args.steps,
         "clocks": clk.summary(),
+        "records": records,
         "extra": extra,
         "cpu_baseline": cpu,
     }
@@ -390,10 +416,26 @@ def run_e2e(fb, torch, dev, stream, layers, x, args, world, rank):
                        "the neighbouring steps' kernels"}
 
 
+class Timing(float):
+    """Mean ms per launch (the float value) with the 10th / 50th / 90th
+    percentiles of the per-launch times beside it."""
+
+    def __new__(cls, mean_ms, samples_ms):
+        t = super().__new__(cls, mean_ms)
+        t.pct = pcts(samples_ms) if len(samples_ms) else [mean_ms] * 3
+        return t
+
+    def us_pct(self):
+        return [round(v * 1e3, 2) for v in self.pct]
+
+
 def _time_back_to_back(torch, stream, fns, reps):
     """Mean ms per launch of `reps` launches issued back to back, cycling through
     `fns` (one per independent copy of the inputs, so that together they exceed
-    L2 and every launch streams its operands from HBM)."""
+    L2 and every launch streams its operands from HBM).  A second pass with an
+    event pair around every launch gives the per-launch percentiles (events
+    between launches stop dependent launches from overlapping, so the mean
+    comes from the first pass)."""
     for f in fns:
         f()
     for _ in range(3):
@@ -406,13 +448,21 @@ def _time_back_to_back(torch, stream, fns, reps):
         fns[i % len(fns)]()
     e.record(stream)
     e.synchronize()
-    return s.elapsed_time(e) / reps
+    mean = s.elapsed_time(e) / reps
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+    ev[0].record(stream)
+    for i in range(reps):
+        fns[i % len(fns)]()
+        ev[i + 1].record(stream)
+    ev[-1].synchronize()
+    return Timing(mean, [ev[i].elapsed_time(ev[i + 1]) for i in range(reps)])
 
 
 def _time_graph(torch, fns, per_graph, reps=20):
     """Mean ms per launch of `per_graph` launches (cycling through `fns`) captured
     back to back in one CUDA graph and replayed `reps` times: launches follow
-    each other with no host in between, as in a captured decode step."""
+    each other with no host in between, as in a captured decode step.  The
+    percentiles are over the replays (each replay's time / per_graph)."""
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(side):
@@ -426,21 +476,21 @@ def _time_graph(torch, fns, per_graph, reps=20):
             fns[i % len(fns)]()
     g.replay()
     torch.cuda.synchronize()
-    s = torch.cuda.Event(enable_timing=True)
-    e = torch.cuda.Event(enable_timing=True)
-    s.record()
-    for _ in range(reps):
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+    ev[0].record()
+    for i in range(reps):
         g.replay()
-    e.record()
-    e.synchronize()
-    return s.elapsed_time(e) / (reps * per_graph)
+        ev[i + 1].record()
+    ev[-1].synchronize()
+    per = [ev[i].elapsed_time(ev[i + 1]) / per_graph for i in range(reps)]
+    return Timing(ev[0].elapsed_time(ev[-1]) / (reps * per_graph), per)
 
 
 def _copies(t, n):
     return [t] + [t.clone() for _ in range(n - 1)]
 
 
-def vendor_fp8_reference(torch, dev, stream, fp8_peak):
+def vendor_fp8_reference(torch, dev, stream):
     res = {"what": "torch._scaled_mm (cuBLASLt), E4M3 x E4M3, per-tensor FP32 scales, BF16 out"}
     try:
         for name, (M, N, K) in (("prefill_4096x24576x6144", (PREFILL_M, PREFILL_NS[1], PREFILL_K)),
@@ -451,23 +501,25 @@ def vendor_fp8_reference(torch, dev, stream, fp8_peak):
             f = lambda: torch._scaled_mm(a, b.t(), scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
             t = _time_back_to_back(torch, stream, [f], 20)
             tf = 2.0 * M * N * K / (t * 1e-3) / 1e12
-            res[name] = {"us": round(t * 1e3, 2), "tflops": round(tf, 1),
-                         "frac_fp8": round(tf / fp8_peak, 4)}
+            res[name] = {"us": round(t * 1e3, 2), "tflops": round(tf, 1)}
             del a, b
     except Exception as e:  # noqa: BLE001 - context figure only
         res["unavailable"] = f"{type(e).__name__}: {str(e)[:160]}"
     return res
 
 
-def run_extra(fb, torch, dev, stream, hbm_peak, fp8_peak):
+def run_extra(fb, torch, dev, stream, hbm_peak, fp8_peak, keep):
     """Decode, quantiser and fused residual-add + RMSNorm + quantisation GB/s,
     MXFP8 and static TFLOPS (informational).  Each
     figure is the mean over back-to-back launches rotating through enough input
     copies to exceed 1.5x the L2 size.  Launches shorter than the host's own
     cost per call (about 11 us through the Python binding) are timed inside a
     CUDA graph (`*_us`, used for the fractions); the eager figures
-    (`*_eager_us`) are reported beside them."""
+    (`*_eager_us`) are reported beside them.  `keep` receives host copies of
+    the outputs of the workload configurations, for the oracle's check in the
+    CPU baseline leg."""
     out = {}
+    nv = torch.cuda.nvtx
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
 
     def to_dev(bits):
@@ -486,6 +538,8 @@ def run_extra(fb, torch, dev, stream, hbm_peak, fp8_peak):
     ns = n_sets(N * K)
     qws, sws = _copies(qw, ns), _copies(sw, ns)
     dec = {}
+    keep["decode"] = {}
+    nv.range_push("decode GEMM and linear 6144x6144")
     for M in si.DECODE["M_list"]:
         x = to_dev(si.activations(M, K))
         q = torch.empty(M, K, dtype=torch.uint8, device=dev)
@@ -499,9 +553,12 @@ def run_extra(fb, torch, dev, stream, hbm_peak, fp8_peak):
         tle = _time_back_to_back(torch, stream, l, 60)
         t = _time_graph(torch, g, 2 * ns)
         tl = _time_graph(torch, l, 2 * ns)
+        g[0]()
+        keep["decode"][M] = y.cpu()
         gemm_bytes = N * K + sw.numel() * 4 + M * (K + K // 128 * 4) + 2 * M * N
         lin_bytes = N * K + sw.numel() * 4 + 2 * M * K + 2 * M * N
-        dec[str(M)] = {"gemm_us": round(t * 1e3, 2),
+        dec[str(M)] = {"gemm_us": round(t * 1e3, 2), "gemm_us_p10_p50_p90": t.us_pct(),
+                       "linear_us_p10_p50_p90": tl.us_pct(),
                        "gemm_gbs": round(gemm_bytes / (t * 1e-3) / 1e9, 1),
                        "gemm_frac_hbm": round(gemm_bytes / (t * 1e-3) / 1e9 / hbm_peak, 4),
                        "gemm_eager_us": round(te * 1e3, 2),
@@ -510,10 +567,12 @@ def run_extra(fb, torch, dev, stream, hbm_peak, fp8_peak):
                        "linear_frac_hbm": round(lin_bytes / (tl * 1e-3) / 1e9 / hbm_peak, 4),
                        "linear_eager_us": round(tle * 1e3, 2)}
     out["decode_N6144_K6144"] = dec
+    nv.range_pop()
     del qw, sw, qws, sws
 
     # quantisers at the workload shapes
     quant = {}
+    nv.range_push("quantisers")
     M, K = 4096, 6144
     b = M * K * 2 + M * K + M * (K // 128) * 4
     ns = n_sets(b)
@@ -522,8 +581,10 @@ def run_extra(fb, torch, dev, stream, hbm_peak, fp8_peak):
     ss = [torch.empty(M, K // 128, dtype=torch.float32, device=dev) for _ in range(ns)]
     t = _time_graph(torch, [lambda i=i: fb.fp8bq_quant_act(xs[i], qs[i], ss[i])
                             for i in range(ns)], 2 * ns)
-    quant["group128_4096x6144"] = {"us": round(t * 1e3, 2), "gbs": round(b / (t * 1e-3) / 1e9, 1),
+    quant["group128_4096x6144"] = {"us": round(t * 1e3, 2), "us_p10_p50_p90": t.us_pct(),
+                                   "gbs": round(b / (t * 1e-3) / 1e9, 1),
                                    "frac_hbm": round(b / (t * 1e-3) / 1e9 / hbm_peak, 4)}
+    keep["quant_group"] = (qs[0].cpu(), ss[0].cpu())
     del xs, qs, ss
     M, K = si.MXFP8["M"], si.MXFP8["K"]
     b = M * K * 3 + M * K // 32
@@ -534,9 +595,12 @@ def run_extra(fb, torch, dev, stream, hbm_peak, fp8_peak):
     ums = [torch.empty(M, K // 32, dtype=torch.uint8, device=dev) for _ in range(ns)]
     t = _time_graph(torch, [lambda i=i: fb.fp8bq_mx_quant_act(xms[i], qms[i], ums[i])
                             for i in range(ns)], 2 * ns)
-    quant["mx_2048x7168"] = {"us": round(t * 1e3, 2), "gbs": round(b / (t * 1e-3) / 1e9, 1),
+    quant["mx_2048x7168"] = {"us": round(t * 1e3, 2), "us_p10_p50_p90": t.us_pct(),
+                             "gbs": round(b / (t * 1e-3) / 1e9, 1),
                              "frac_hbm": round(b / (t * 1e-3) / 1e9 / hbm_peak, 4)}
+    keep["quant_mx"] = (qms[0].cpu(), ums[0].cpu())
     out["quant"] = quant
+    nv.range_pop()
     qm, um = qms[0], ums[0]
     del xms
 
@@ -549,10 +613,13 @@ def run_extra(fb, torch, dev, stream, hbm_peak, fp8_peak):
     del wb
     ym = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
     wsm = fb.new_workspace(fb.OP_MX_GEMM, M, N, K, device=dev)
+    nv.range_push("MXFP8 GEMM 2048x4096x7168")
     t = _time_back_to_back(torch, stream, [lambda: fb.fp8bq_mx_gemm(qm, um, qwm, uwm, ym, wsm)], 30)
+    nv.range_pop()
+    keep["mx_gemm"] = ym[:ORACLE_ROWS].cpu()
     tf = 2.0 * M * N * K / (t * 1e-3) / 1e12
-    out["mx_gemm_2048x4096x7168"] = {"us": round(t * 1e3, 2), "tflops": round(tf, 1),
-                                     "frac_fp8": round(tf / fp8_peak, 4)}
+    out["mx_gemm_2048x4096x7168"] = {"us": round(t * 1e3, 2), "us_p10_p50_p90": t.us_pct(),
+                                     "tflops": round(tf, 1), "frac_fp8": round(tf / fp8_peak, 4)}
     del qwm, uwm
 
     # static per-tensor GEMM, N = 14336 (4096/4096/6144), K = 4096
@@ -571,6 +638,8 @@ def run_extra(fb, torch, dev, stream, hbm_peak, fp8_peak):
     s_x = torch.empty(1, dtype=torch.float32, device=dev)
     fb.fp8bq_absmax_scale(to_dev(si.calibration(si.STATIC["calib_rows"], K)), s_x)
     st = {}
+    keep["static"] = {}
+    nv.range_push("static per-tensor GEMM N=14336")
     for M in si.STATIC["M_list"]:
         xs = to_dev(si.activations(M, K, outliers=False))
         qs = torch.empty(M, K, dtype=torch.uint8, device=dev)
@@ -580,17 +649,20 @@ def run_extra(fb, torch, dev, stream, hbm_peak, fp8_peak):
         t = _time_graph(
             torch, [lambda i=i: fb.fp8bq_static_gemm(qs, s_x, qwss[i], sp, parts, ys, wss)
                     for i in range(ns)], 2 * ns)
+        keep["static"][M] = ys[:ORACLE_ROWS].cpu()
         tf = 2.0 * M * N * K / (t * 1e-3) / 1e12
         b = N * K + M * K + 2 * M * N
-        st[str(M)] = {"us": round(t * 1e3, 2), "tflops": round(tf, 2),
+        st[str(M)] = {"us": round(t * 1e3, 2), "us_p10_p50_p90": t.us_pct(), "tflops": round(tf, 2),
                       "frac_fp8": round(tf / fp8_peak, 4),
                       "gbs": round(b / (t * 1e-3) / 1e9, 1),
                       "frac_hbm": round(b / (t * 1e-3) / 1e9 / hbm_peak, 4)}
     out["static_N14336_K4096"] = st
+    nv.range_pop()
     del qwss, qws
 
     # channelwise W8A8: per-token quantiser, GEMM at the prefill and decode shapes
     ch = {}
+    nv.range_push("channelwise W8A8")
     M, K = si.PREFILL["M"], si.PREFILL["K"]
     b = M * K * 3 + M * 4
     ns = n_sets(b)
@@ -613,8 +685,8 @@ def run_extra(fb, torch, dev, stream, hbm_peak, fp8_peak):
         ws = fb.new_workspace(fb.OP_CHANNEL_GEMM, M, N, K, device=dev)
         t = _time_back_to_back(torch, stream, [lambda: fb.fp8bq_channel_gemm(qa, sa, qw, sw, y, ws)], 20)
         tf = 2.0 * M * N * K / (t * 1e-3) / 1e12
-        ch[f"gemm_{M}x{N}x{K}"] = {"us": round(t * 1e3, 2), "tflops": round(tf, 1),
-                                   "frac_fp8": round(tf / fp8_peak, 4)}
+        ch[f"gemm_{M}x{N}x{K}"] = {"us": round(t * 1e3, 2), "us_p10_p50_p90": t.us_pct(),
+                                   "tflops": round(tf, 1), "frac_fp8": round(tf / fp8_peak, 4)}
         del qw, sw, y
     K = N = si.DECODE["K"]
     wb = to_dev(si.weights(N, K))
@@ -633,14 +705,16 @@ def run_extra(fb, torch, dev, stream, hbm_peak, fp8_peak):
         t = _time_graph(torch, [lambda i=i: fb.fp8bq_channel_gemm(qd, sd, qws[i], sws[i], y, ws)
                                 for i in range(ns)], 2 * ns)
         bb = N * K + N * 4 + M * (K + 4) + 2 * M * N
-        ch[f"gemm_decode_{M}x{N}x{K}"] = {"us": round(t * 1e3, 2),
+        ch[f"gemm_decode_{M}x{N}x{K}"] = {"us": round(t * 1e3, 2), "us_p10_p50_p90": t.us_pct(),
                                           "gbs": round(bb / (t * 1e-3) / 1e9, 1),
                                           "frac_hbm": round(bb / (t * 1e-3) / 1e9 / hbm_peak, 4)}
     out["channel_w8a8"] = ch
+    nv.range_pop()
     del qw, sw, qws, sws
 
     # block FP8 with UE8M0 scales on the block-scaled MMA, at the prefill shapes
     ue = {}
+    nv.range_push("block FP8 with UE8M0 scales")
     M, K = si.PREFILL["M"], si.PREFILL["K"]
     KB = K // 128
     b = M * K * 3 + M * KB
@@ -666,10 +740,11 @@ def run_extra(fb, torch, dev, stream, hbm_peak, fp8_peak):
         ws = fb.new_workspace(fb.OP_UE8M0_GEMM, M, N, K, device=dev)
         t = _time_back_to_back(torch, stream, [lambda: fb.fp8bq_ue8m0_gemm(qa, ua, qw, uw, y, ws)], 20)
         tf = 2.0 * M * N * K / (t * 1e-3) / 1e12
-        ue[f"gemm_{M}x{N}x{K}"] = {"us": round(t * 1e3, 2), "tflops": round(tf, 1),
-                                   "frac_fp8": round(tf / fp8_peak, 4)}
+        ue[f"gemm_{M}x{N}x{K}"] = {"us": round(t * 1e3, 2), "us_p10_p50_p90": t.us_pct(),
+                                   "tflops": round(tf, 1), "frac_fp8": round(tf / fp8_peak, 4)}
         del qw, sw, uw, y
     out["block_ue8m0"] = ue
+    nv.range_pop()
     del qs, us
 
     # grouped (MoE) block GEMM: 32 local experts, 4096 routed rows with skewed
@@ -683,6 +758,7 @@ def run_extra(fb, torch, dev, stream, hbm_peak, fp8_peak):
     live = int((counts > 0).sum())
     gr = {"experts": E, "rows": T, "max_rows": int(counts.max()), "min_rows": int(counts.min()),
           "m_tiles_256": int(np.sum((counts + 255) // 256))}
+    nv.range_push("grouped (MoE) GEMM")
     for which, N, K in (("w13", 2 * mo["I"], mo["H"]), ("w2", mo["H"], mo["I"])):
         KB, NB = K // 128, N // 128
         qw = torch.empty(E, N, K, dtype=torch.uint8, device=dev)
@@ -707,7 +783,8 @@ def run_extra(fb, torch, dev, stream, hbm_peak, fp8_peak):
         gbs = bb / (t * 1e-3) / 1e9
         # the bound: the larger of the HBM time and the FP8 tensor time
         t_min = max(bb / (hbm_peak * 1e9), flops / (fp8_peak * 1e12))
-        gr[f"{which}_N{N}_K{K}"] = {"us": round(t * 1e3, 2), "tflops": round(tf, 1),
+        gr[f"{which}_N{N}_K{K}"] = {"us": round(t * 1e3, 2), "us_p10_p50_p90": t.us_pct(),
+                                    "tflops": round(tf, 1),
                                     "gbs": round(gbs, 1), "frac_fp8": round(tf / fp8_peak, 4),
                                     "frac_hbm": round(gbs / hbm_peak, 4),
                                     "frac_roofline": round(t_min / (t * 1e-3), 4)}
@@ -729,20 +806,22 @@ def run_extra(fb, torch, dev, stream, hbm_peak, fp8_peak):
             live_d = int((cd > 0).sum())
             bd = live_d * (N * K + NB * KB * 4) + int(cd.sum()) * (K + KB * 4 + 2 * N)
             gr[f"masked_decode_{which}_rows{int(cd.sum())}_slots{max_m}"] = {
-                "us": round(t * 1e3, 2), "gbs": round(bd / (t * 1e-3) / 1e9, 1),
+                "us": round(t * 1e3, 2), "us_p10_p50_p90": t.us_pct(),
+                "gbs": round(bd / (t * 1e-3) / 1e9, 1),
                 "frac_hbm": round(bd / (t * 1e-3) / 1e9 / hbm_peak, 4)}
             del qd, sd, yd
         del qw, sw
     out["grouped_moe"] = gr
+    nv.range_pop()
 
     # context only (not a denominator): the vendor's plain FP8 GEMM with
     # per-tensor scales (cuBLASLt through torch._scaled_mm) at the prefill shape
     # and at 8192^3; it has no per-block promotion to do
-    out["vendor_fp8_gemm"] = vendor_fp8_reference(torch, dev, stream, fp8_peak)
 
     # residual add + RMSNorm + quantisation (the step before the linear):
     # x, residual in; updated residual, E4M3 codes (and group scales) out
     norm = {}
+    nv.range_push("residual add + RMSNorm + quantisation")
     eps = si.NORM["eps"]
     cases = [("group", 4096, 6144), ("group", 64, 6144), ("group", 1, 6144),
              ("static", 4096, 4096), ("static", 512, 4096), ("static", 1, 4096)]
@@ -770,11 +849,27 @@ def run_extra(fb, torch, dev, stream, hbm_peak, fp8_peak):
                 xs[i], gn, eps, s_n, qs[i], residual=rs[i], residual_out=ros[i])
                 for i in range(ns)]
         t = _time_graph(torch, fns, 2 * ns)
-        norm[f"{mode}_{M}x{K}"] = {"us": round(t * 1e3, 2),
+        norm[f"{mode}_{M}x{K}"] = {"us": round(t * 1e3, 2), "us_p10_p50_p90": t.us_pct(),
                                    "gbs": round(b / (t * 1e-3) / 1e9, 1),
                                    "frac_hbm": round(b / (t * 1e-3) / 1e9 / hbm_peak, 4)}
         del xs, rs, ros, qs
     out["add_rmsnorm_quant"] = norm
+    nv.range_pop()
+
+    # the tiny linear (16 x 384 x 256): launch-bound, timed in a graph
+    nv.range_push("tiny linear 16x384x256")
+    M, K, N = si.TINY["M"], si.TINY["K"], si.TINY["N"]
+    xt = to_dev(si.activations(M, K, outliers=False))
+    wb = to_dev(si.weights(N, K))
+    qwt = torch.empty(N, K, dtype=torch.uint8, device=dev)
+    swt = torch.empty(-(-N // 128), -(-K // 128), dtype=torch.float32, device=dev)
+    fb.fp8bq_quant_weight_block(wb, qwt, swt)
+    yt = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+    wst = fb.new_workspace(fb.OP_LINEAR, M, N, K, device=dev)
+    t = _time_graph(torch, [lambda: fb.fp8bq_linear(xt, qwt, swt, yt, wst)], 20)
+    keep["tiny"] = yt.cpu()
+    out["tiny_linear_16x384x256"] = {"us": round(t * 1e3, 2), "us_p10_p50_p90": t.us_pct()}
+    nv.range_pop()
     return out
 
 
@@ -801,32 +896,250 @@ def oracle_step(x, ws, threads):
         oracle.gemm_block(qa, sa, qw, sw, threads=threads)
 
 
-def cpu_baseline(args):
-    """The oracle on the host cores: quantisation (single-threaded C) and the
-    FP64 block GEMMs (all cores) timed separately on the first rows of the
-    workload, and the quantiser alone on 512 rows for a steadier figure."""
+def _bf16_host(t):
+    """A host BF16 tensor (GPU output) as float64 numpy."""
+    return t.float().numpy().astype(np.float64)
+
+
+def _close(y, ref):
+    """The parity tests' GEMM tolerance: per element |y - ref| <= 1e-2 max(1, |ref|),
+    relative Frobenius error <= 4e-3."""
+    y = np.asarray(y, np.float64)
+    ref = np.asarray(ref, np.float64)
+    err = np.abs(y - ref)
+    ok = bool(np.all(err <= 1e-2 * np.maximum(1.0, np.abs(ref))) and np.all(np.isfinite(y)))
+    nref = np.linalg.norm(ref)
+    rel = float(np.linalg.norm(y - ref) / nref) if nref > 0 else 0.0
+    return {"ok": ok and rel <= 4e-3, "max_abs_err": float(err.max()) if err.size else 0.0,
+            "rel_frob": round(rel, 7)}
+
+
+def _exact(got, ref):
+    got, ref = np.asarray(got), np.asarray(ref)
+    bad = int(np.count_nonzero(got != ref)) if got.shape == ref.shape else -1
+    return {"ok": bad == 0, "mismatches": bad}
+
+
+def cpu_baseline(args, keep=None):
+    """The oracle on the host cores: one bounded sample of every workload
+    configuration, timed (its quantisers single-threaded C, its binary64 GEMMs
+    on all cores).  Where `keep` holds the GPU's outputs for the same seeded
+    inputs, each sample also checks them: codes and scales bit for bit, GEMM
+    outputs within the parity tests' tolerance.  The headline figure (value,
+    unit) is the prefill linear's; `configs` has one entry per configuration."""
     import oracle
+    keep = keep or {}
     threads = os.cpu_count() or 1
-    rows = args.cpu_rows
-    x, ws = oracle_sample(rows)
-    t0 = time.perf_counter()
+    cfg = {}
+    perf = time.perf_counter
+
+    # tiny linear 16 x 384 x 256: all of it
+    M, K, N = si.TINY["M"], si.TINY["K"], si.TINY["N"]
+    qw, sw = oracle.quant_weight_block(si.weights(N, K))
+    x = si.activations(M, K, outliers=False)
+    t0 = perf()
     qa, sa = oracle.quant_group(x)
-    t1 = time.perf_counter()
-    for qw, sw in ws:
-        oracle.gemm_block(qa, sa, qw, sw, threads=threads)
-    t2 = time.perf_counter()
-    xq = si.activations(512, PREFILL_K)
-    t3 = time.perf_counter()
-    oracle.quant_group(xq)
-    t4 = time.perf_counter()
+    y = oracle.gemm_block(qa, sa, qw, sw, threads=threads)
+    dt = perf() - t0
+    cfg["tiny_linear_16x384x256"] = {
+        "s": round(dt, 4), "tflops": 2.0 * M * N * K / dt / 1e12, "cores": threads,
+        "sample": "the whole linear",
+        "parity": _close(_bf16_host(keep["tiny"]), y) if "tiny" in keep else None}
+
+    # decode GEMMs K = N = 6144, M in {1, 8, 32, 64}: every output
+    K = N = si.DECODE["K"]
+    qw, sw = oracle.quant_weight_block(si.weights(N, K))
+    dec = {}
+    for M in si.DECODE["M_list"]:
+        x = si.activations(M, K)
+        t0 = perf()
+        qa, sa = oracle.quant_group(x)
+        y = oracle.gemm_block(qa, sa, qw, sw, threads=threads)
+        dt = perf() - t0
+        b = N * K + sw.size * 4 + M * (K + K // 128 * 4) + 2 * M * N
+        got = keep.get("decode", {}).get(M)
+        dec[str(M)] = {"s": round(dt, 4), "gbs": round(b / dt / 1e9, 4),
+                       "parity": _close(_bf16_host(got), y) if got is not None else None}
+    cfg["decode_6144x6144"] = {"cores": threads, "sample": "quant + GEMM, every output",
+                               "per_M": dec}
+
+    # prefill: the first rows of the 4096-token batch through quant + both GEMMs
+    rows = args.cpu_rows
+    K = PREFILL_K
+    x = si.activations(rows, K)
+    wts = {N: oracle.quant_weight_block(si.weights(N, K)) for N in PREFILL_NS}
+    t0 = perf()
+    qa, sa = oracle.quant_group(x)
+    t1 = perf()
+    ys = {N: oracle.gemm_block(qa, sa, qw, sw, threads=threads) for N, (qw, sw) in wts.items()}
+    t2 = perf()
     dt = t2 - t0
-    flops = sum(2.0 * rows * PREFILL_K * N for N in PREFILL_NS)
-    quant_bytes = 512 * (3 * PREFILL_K + 4 * (PREFILL_K // 128))
-    return {"value": flops / dt / 1e12, "unit": "TFLOPS", "cores": threads, "kind": "oracle",
-            "sample": f"first {rows} tokens of the prefill batch through quant + FP64 block "
-                      f"GEMM for N in {list(PREFILL_NS)} ({dt:.1f} s)",
-            "quant_s": round(t1 - t0, 4), "gemm_s": round(t2 - t1, 3),
-            "quant_1thread_gbs": round(quant_bytes / (t4 - t3) / 1e9, 3)}
+    flops = sum(2.0 * rows * K * N for N in PREFILL_NS)
+    par = {str(N): _close(_bf16_host(keep["prefill"][N][:rows]), ys[N])
+           for N in PREFILL_NS if N in keep.get("prefill", {})}
+    prefill_tf = flops / dt / 1e12
+    cfg["prefill_4096x6144"] = {
+        "s": round(dt, 3), "tflops": prefill_tf, "cores": threads,
+        "sample": f"first {rows} tokens through quant + FP64 block GEMM for N in "
+                  f"{list(PREFILL_NS)}",
+        "quant_s": round(t1 - t0, 4), "gemm_s": round(t2 - t1, 3), "parity": par or None}
+    del wts, ys
+
+    # MXFP8 2048 x 4096 x 7168: the first rows
+    M, K, N = si.MXFP8["M"], si.MXFP8["K"], si.MXFP8["N"]
+    r = min(ORACLE_ROWS, M)
+    qw, uw = oracle.quant_mx(si.weights(N, K))
+    x = si.activations(r, K)
+    t0 = perf()
+    qa, ua = oracle.quant_mx(x)
+    y = oracle.gemm_mx(qa, ua, qw, uw, threads=threads)
+    dt = perf() - t0
+    cfg["mxfp8_2048x4096x7168"] = {
+        "s": round(dt, 4), "tflops": 2.0 * r * N * K / dt / 1e12, "cores": threads,
+        "sample": f"first {r} tokens through MX quant + FP64 MX GEMM",
+        "parity": _close(_bf16_host(keep["mx_gemm"][:r]), y) if "mx_gemm" in keep else None}
+
+    # static per-tensor N = 14336 (4096 / 4096 / 6144), K = 4096
+    K, N, parts = si.STATIC["K"], si.STATIC["N"], list(si.STATIC["parts"])
+    s_x = oracle.absmax_scale(si.calibration(si.STATIC["calib_rows"], K))
+    qw, sp = oracle.quant_weight_static(si.weights(N, K), parts)
+    st = {}
+    for M in si.STATIC["M_list"]:
+        r = min(ORACLE_ROWS, M)
+        x = si.activations(r, K, outliers=False)
+        t0 = perf()
+        qa = oracle.quant_static(x, s_x)
+        y = oracle.gemm_static(qa, s_x, qw, sp, parts, threads=threads)
+        dt = perf() - t0
+        got = keep.get("static", {}).get(M)
+        st[str(M)] = {"s": round(dt, 4), "tflops": 2.0 * r * N * K / dt / 1e12,
+                      "rows": r, "parity": _close(_bf16_host(got[:r]), y)
+                      if got is not None else None}
+    cfg["static_14336x4096"] = {"cores": threads, "per_M": st,
+                                "sample": f"first min(M, {ORACLE_ROWS}) tokens per M"}
+    del qw
+
+    # quantisers (single-threaded C), whole workload inputs
+    M, K = 4096, 6144
+    x = si.activations(M, K)
+    t0 = perf()
+    q, s = oracle.quant_group(x)
+    dt = perf() - t0
+    par = None
+    if "quant_group" in keep:
+        gq, gs = keep["quant_group"]
+        a, b = _exact(gq.numpy(), q), _exact(gs.numpy().view(np.uint32), s.view(np.uint32))
+        par = {"ok": a["ok"] and b["ok"], "code_mismatches": a["mismatches"],
+               "scale_mismatches": b["mismatches"]}
+    cfg["quant_group128_4096x6144"] = {
+        "s": round(dt, 4), "gbs": round(M * (3 * K + 4 * (K // 128)) / dt / 1e9, 4),
+        "cores": 1, "sample": "the whole 4096 x 6144 input", "parity": par}
+    M, K = si.MXFP8["M"], si.MXFP8["K"]
+    x = si.activations(M, K)
+    t0 = perf()
+    q, u = oracle.quant_mx(x)
+    dt = perf() - t0
+    par = None
+    if "quant_mx" in keep:
+        gq, gu = keep["quant_mx"]
+        a, b = _exact(gq.numpy(), q), _exact(gu.numpy(), u)
+        par = {"ok": a["ok"] and b["ok"], "code_mismatches": a["mismatches"],
+               "scale_mismatches": b["mismatches"]}
+    cfg["quant_mx_2048x7168"] = {
+        "s": round(dt, 4), "gbs": round(M * (3 * K + K // 32) / dt / 1e9, 4), "cores": 1,
+        "sample": "the whole 2048 x 7168 input", "parity": par}
+
+    return {"value": prefill_tf, "unit": "TFLOPS", "cores": threads, "kind": "oracle",
+            "sample": cfg["prefill_4096x6144"]["sample"] + f" ({cfg['prefill_4096x6144']['s']} s)",
+            "configs": cfg}
+
+
+def build_records(M, K, layers, gemm_lists, step_list, flops_step, extra, cpu, hbm_peak,
+                  fp8_peak, achieved):
+    """One record per (workload configuration, op): time percentiles, the
+    roofline fraction, the oracle's parity check and its time with its cores."""
+    recs = []
+    cc = (cpu or {}).get("configs", {})
+
+    def rec(config, op, shape, us_pct, bound, value, unit, frac, parity=None, oracle=None):
+        recs.append({"config": config, "op": op, "shape": shape, "us_p10_p50_p90": us_pct,
+                     "bound": bound, "achieved": value, "unit": unit, "frac": frac,
+                     "parity": parity, "oracle": oracle})
+
+    def orc(entry, keys=("s", "cores", "sample")):
+        return None if entry is None else {k: entry.get(k) for k in keys if k in entry}
+
+    pre = cc.get("prefill_4096x6144")
+    for L, g in zip(layers, gemm_lists):
+        us = [round(v * 1e3, 2) for v in pcts(g)]
+        tf = 2.0 * M * K * L["N"] / (np.median(g) * 1e-3) / 1e12
+        rec("prefill", "block GEMM", f"{M}x{L['N']}x{K}", us, "tensor", round(tf, 1), "TFLOP/s",
+            round(tf / fp8_peak, 4), (pre or {}).get("parity", {}).get(str(L["N"])) if pre
+            else None, orc(pre))
+    st_us = [round(v * 1e3, 2) for v in pcts(step_list)]
+    rec("prefill", "quant + 2 GEMMs (bench step)", f"X[{M},{K}]", st_us, "tensor",
+        round(flops_step / (np.median(step_list) * 1e-3) / 1e12, 1), "TFLOP/s", None,
+        None, orc(pre))
+    if not extra:
+        return recs
+    tiny = extra.get("tiny_linear_16x384x256")
+    if tiny:
+        rec("tiny", "linear", "16x384x256", tiny["us_p10_p50_p90"], "launch", None, None, None,
+            (cc.get("tiny_linear_16x384x256") or {}).get("parity"),
+            orc(cc.get("tiny_linear_16x384x256")))
+    dec_o = (cc.get("decode_6144x6144") or {}).get("per_M", {})
+    for Ms, d in extra.get("decode_N6144_K6144", {}).items():
+        o = dec_o.get(Ms)
+        rec("decode", "block GEMM", f"{Ms}x6144x6144", d["gemm_us_p10_p50_p90"], "hbm",
+            d["gemm_gbs"], "GB/s", d["gemm_frac_hbm"], (o or {}).get("parity"),
+            None if o is None else {"s": o["s"], "cores": cc["decode_6144x6144"]["cores"],
+                                    "sample": "every output"})
+        rec("decode", "linear", f"{Ms}x6144x6144", d["linear_us_p10_p50_p90"], "hbm",
+            d["linear_gbs"], "GB/s", d["linear_frac_hbm"], None, None)
+    qd = extra.get("quant", {})
+    if "group128_4096x6144" in qd:
+        d, o = qd["group128_4096x6144"], cc.get("quant_group128_4096x6144")
+        rec("prefill", "group-128 quant", "4096x6144", d["us_p10_p50_p90"], "hbm", d["gbs"],
+            "GB/s", d["frac_hbm"], (o or {}).get("parity"), orc(o))
+    if "mx_2048x7168" in qd:
+        d, o = qd["mx_2048x7168"], cc.get("quant_mx_2048x7168")
+        rec("mxfp8", "MX quant", "2048x7168", d["us_p10_p50_p90"], "hbm", d["gbs"], "GB/s",
+            d["frac_hbm"], (o or {}).get("parity"), orc(o))
+    d = extra.get("mx_gemm_2048x4096x7168")
+    if d:
+        o = cc.get("mxfp8_2048x4096x7168")
+        rec("mxfp8", "MX GEMM", "2048x4096x7168", d["us_p10_p50_p90"], "tensor", d["tflops"],
+            "TFLOP/s", d["frac_fp8"], (o or {}).get("parity"), orc(o))
+    st_o = (cc.get("static_14336x4096") or {}).get("per_M", {})
+    for Ms, d in extra.get("static_N14336_K4096", {}).items():
+        o = st_o.get(Ms)
+        hbm = Ms == "1"
+        rec("static", "per-tensor GEMM", f"{Ms}x14336x4096", d["us_p10_p50_p90"],
+            "hbm" if hbm else "tensor", d["gbs"] if hbm else d["tflops"],
+            "GB/s" if hbm else "TFLOP/s", d["frac_hbm"] if hbm else d["frac_fp8"],
+            (o or {}).get("parity"),
+            None if o is None else {"s": o["s"], "rows": o["rows"],
+                                    "cores": cc["static_14336x4096"]["cores"]})
+    # rows past the five configurations: parity is in the -m gpu tests
+    gpu_tests = "tests -m gpu (not rechecked here)"
+    for k, d in extra.get("channel_w8a8", {}).items():
+        hbm = "gbs" in d and "tflops" not in d
+        rec("channelwise", k, k.split("_")[-1], d["us_p10_p50_p90"], "hbm" if hbm else "tensor",
+            d["gbs"] if hbm else d["tflops"], "GB/s" if hbm else "TFLOP/s",
+            d["frac_hbm"] if hbm else d["frac_fp8"], gpu_tests, None)
+    for k, d in extra.get("block_ue8m0", {}).items():
+        hbm = "tflops" not in d
+        rec("block UE8M0", k, k.split("_")[-1], d["us_p10_p50_p90"], "hbm" if hbm else "tensor",
+            d["gbs"] if hbm else d["tflops"], "GB/s" if hbm else "TFLOP/s",
+            d["frac_hbm"] if hbm else d["frac_fp8"], gpu_tests, None)
+    for k, d in extra.get("grouped_moe", {}).items():
+        if isinstance(d, dict):
+            rec("grouped MoE", k, k, d["us_p10_p50_p90"], "hbm", d["gbs"], "GB/s",
+                d["frac_hbm"], gpu_tests, None)
+    for k, d in extra.get("add_rmsnorm_quant", {}).items():
+        rec("add + RMSNorm + quant", k, k.split("_")[-1], d["us_p10_p50_p90"], "hbm", d["gbs"],
+            "GB/s", d["frac_hbm"], gpu_tests, None)
+    return recs
 
 
 def run_reference(args):

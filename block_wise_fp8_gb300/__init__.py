@@ -37,7 +37,7 @@ __all__ = [
     "fp8bq_mx_gemm", "fp8bq_mx_linear", "fp8bq_static_quant_act", "fp8bq_static_gemm",
     "fp8bq_add_rmsnorm_quant_act", "fp8bq_add_rmsnorm_static_quant_act",
     "fp8bq_static_linear", "fp8bq_quant_weight_block", "fp8bq_absmax_scale",
-    "new_workspace",
+    "new_workspace", "fp8bq_e4m3_from_bits",
 ]
 
 SCALE_ROW_MAJOR, SCALE_COL_MAJOR = 0, 1
@@ -108,6 +108,7 @@ def _load():
                                       P]),
         "fp8bq_quant_weight_block": (I32, [P, I64, I64, I64, P, P, P]),
         "fp8bq_absmax_scale": (I32, [P, I64, I64, I64, P, P]),
+        "fp8bq_e4m3_from_bits": (I32, [ctypes.c_uint32, I64, P, P]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)
@@ -650,3 +651,13 @@ def fp8bq_absmax_scale(x, s, stream=None):
         _Spec("s", s, _F32, numel=1)], stream)
     _check(_lib.fp8bq_absmax_scale(_ptr(x), rows, K, _ld(x), _ptr(s), _stream(stream)),
            "fp8bq_absmax_scale")
+
+
+def fp8bq_e4m3_from_bits(first: int, codes, stream=None):
+    """codes[i] = the quantisers' E4M3 conversion of the binary32 value with bit
+    pattern first + i, for every element of the uint8 tensor `codes`."""
+    _validate("fp8bq_e4m3_from_bits", [_Spec("codes", codes, _U8, numel=codes.numel()
+                                             if isinstance(codes, torch.Tensor) else None)],
+              stream)
+    _check(_lib.fp8bq_e4m3_from_bits(first, codes.numel(), _ptr(codes), _stream(stream)),
+           "fp8bq_e4m3_from_bits")

@@ -75,6 +75,9 @@ void launch_absmax_scale(const void *x, int64_t rows, int64_t K, int64_t ldx, fl
 // index when there is none).  `out` is device memory of 4 words.
 void launch_check_scales(const float *s, int64_t n, unsigned long long *out, int num_sms,
                          cudaStream_t st);
+// codes[i] = the quantisers' binary32 -> E4M3 conversion of bit pattern first + i
+// (i < n); `codes` 8-byte aligned.
+void launch_e4m3_bits(uint32_t first, int64_t n, uint8_t *codes, int num_sms, cudaStream_t st);
 
 // ---------------------------------------------------------------- GEMM
 

@@ -644,6 +644,19 @@ int fp8bq_check_scales(const float *s, int64_t n, void *scratch, int64_t *counts
   return FP8BQ_OK;
 }
 
+int fp8bq_e4m3_from_bits(uint32_t first, int64_t n, uint8_t *codes, void *stream) {
+  if (n < 0 || static_cast<uint64_t>(first) + static_cast<uint64_t>(n) > (1ull << 32))
+    return FP8BQ_ERR_SHAPE;
+  if (n == 0) return FP8BQ_OK;
+  if (!codes) return FP8BQ_ERR_NULL;
+  if (!aligned(codes, 8)) return FP8BQ_ERR_ALIGN;
+  DeviceInfo dev;
+  RETURN_IF(device_info(&dev));
+  launch_e4m3_bits(first, n, codes, dev.num_sms, static_cast<cudaStream_t>(stream));
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? FP8BQ_OK : cuda_fail(e);
+}
+
 // ------------------------------------------------------------------ no-allocation GEMM
 
 // fp8bq_gemm with the library's fixed scratch array in place of a caller

@@ -529,6 +529,48 @@ void launch_requant_ue8m0(const void *q, const float *s, int64_t N, int64_t K, v
              static_cast<int>(N), static_cast<int>(K), KB, static_cast<uint8_t *>(q2), u);
 }
 
+// The binary32 -> E4M3 conversion of every quantiser (the paired, saturating,
+// round-to-nearest-even conversion of quant_words and to_e4m3x16) applied to
+// consecutive bit patterns: codes[i] = E4M3(bits first + i).  Each thread
+// converts 8 patterns, two per conversion, and stores them as one 8-byte word.
+__global__ void __launch_bounds__(kThreads) e4m3_bits_kernel(uint32_t first, int64_t n,
+                                                             uint8_t *__restrict__ codes) {
+  griddep_launch_dependents();
+  griddep_wait();
+  const int64_t groups = (n + 7) / 8;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < groups;
+       g += stride) {
+    const int64_t i0 = g * 8;
+    uint32_t w[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t word = 0;
+#pragma unroll
+      for (int p = 0; p < 2; ++p) {
+        const uint32_t b = first + static_cast<uint32_t>(i0 + 4 * h + 2 * p);
+        const float2 v = make_float2(__uint_as_float(b), __uint_as_float(b + 1u));
+        const uint32_t c = __nv_cvt_float2_to_fp8x2(v, __NV_SATFINITE, __NV_E4M3);
+        word |= (c & 0xFFFFu) << (16 * p);
+      }
+      w[h] = word;
+    }
+    if (i0 + 8 <= n) {
+      *reinterpret_cast<uint2 *>(codes + i0) = make_uint2(w[0], w[1]);
+    } else {
+      for (int j = 0; i0 + j < n; ++j) codes[i0 + j] = static_cast<uint8_t>(w[j / 4] >> (8 * (j % 4)));
+    }
+  }
+}
+
+void launch_e4m3_bits(uint32_t first, int64_t n, uint8_t *codes, int num_sms, cudaStream_t st) {
+  unsigned grid = blocks_for((n + 7) / 8, kThreads);
+  const unsigned cap = static_cast<unsigned>(num_sms) * 8u;
+  if (grid > cap) grid = cap;
+  if (grid == 0) grid = 1;
+  launch_pdl(e4m3_bits_kernel, grid, kThreads, 0, st, first, n, codes);
+}
+
 void launch_check_scales(const float *s, int64_t n, unsigned long long *out, int num_sms,
                          cudaStream_t st) {
   // counts to 0, first index to 0x7f7f7f7f7f7f7f7f (above any index)

@@ -413,6 +413,16 @@ FP8BQ_API int fp8bq_check_scales(const float *s, int64_t n, void *scratch,
                                  int64_t *counts_host, int64_t *first_bad_host,
                                  void *stream);
 
+/* Test helper for the conversion every quantiser ends with: codes[i] = the
+ * E4M3 code of the binary32 value whose bit pattern is first + i (0 <= i < n,
+ * first + n <= 2^32), from the same saturating round-to-nearest-even hardware
+ * conversion the quantisers apply to their quotients ("SGLang 源码完全拆解(十九)",
+ * §从浮点到 FP8 的基本公式: q = clamp(round(x/s), -448, 448), RNE; |v| >= 448
+ * and infinities give +-448).  Lets a test compare the conversion with an
+ * independent encoder over all 2^32 inputs.  codes: device uint8 [n], 8-byte
+ * aligned.  FP8BQ_ERR_SHAPE for n < 0 or a range past 2^32 - 1. */
+FP8BQ_API int fp8bq_e4m3_from_bits(uint32_t first, int64_t n, uint8_t *codes, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -54,6 +54,7 @@ _SIGS = {
     "orc_bf16_to_f32": (ctypes.c_float, [ctypes.c_uint16]),
     "orc_e4m3_encode_f32_array": (None, [_P, _I64, _P]),
     "orc_e4m3_decode_array": (None, [_P, _I64, _P]),
+    "orc_e4m3_encode_bits_range": (None, [ctypes.c_uint32, _I64, _P, ctypes.c_int]),
     "orc_quant_group": (None, [_P, _I64, _I64, _I64, _I64, _P, _P]),
     "orc_quant_mx": (None, [_P, _I64, _I64, _I64, _P, _P]),
     "orc_quant_static": (None, [_P, _I64, _I64, _I64, ctypes.c_float, _P]),
@@ -131,6 +132,15 @@ def e4m3_encode(v) -> np.ndarray:
     v = _c(v, np.float32)
     out = np.empty(v.shape, np.uint8)
     lib().orc_e4m3_encode_f32_array(_p(v), v.size, _p(out))
+    return out
+
+
+def e4m3_encode_bits_range(first: int, n: int, threads: int | None = None) -> np.ndarray:
+    """Codes of the binary32 values whose bit patterns are first .. first + n - 1."""
+    if first < 0 or n < 0 or first + n > 1 << 32:
+        raise ValueError("bit patterns outside 0 .. 2^32 - 1")
+    out = np.empty(n, np.uint8)
+    lib().orc_e4m3_encode_bits_range(first, n, _p(out), threads or default_threads())
     return out
 
 

@@ -5,8 +5,7 @@
  * baseline of the benchmark, never by the library.  Shares no code with the
  * CUDA path.  Citations: see fp8bq_oracle.h.
  *
- * Readings taken where the pages leave a step open (each also listed in the
- * design notes):
+ * Readings taken where the pages leave a step open:
  *   - s = amax / 448 and q = x / s are IEEE binary32 divisions.
  *   - amax is floored at 1e-10 (the pages' E8M0 scale rule floors it; the FP32
  *     rule is silent, and an all-zero group would otherwise give 0/0).
@@ -103,6 +102,50 @@ void orc_e4m3_encode_f32_array(const float *v, int64_t n, uint8_t *out) {
 
 void orc_e4m3_decode_array(const uint8_t *c, int64_t n, double *out) {
   for (int64_t i = 0; i < n; ++i) out[i] = orc_e4m3_decode(c[i]);
+}
+
+/* The encoder over consecutive binary32 bit patterns: out[i] = the code of the
+ * binary32 value whose bits are first + i (i < n, first + n <= 2^32).  Every
+ * binary32 value is exact in binary64, so this is orc_e4m3_encode on each
+ * pattern; the threads take contiguous ranges. */
+typedef struct {
+  uint32_t first;
+  int64_t i0, i1;
+  uint8_t *out;
+} bits_job;
+
+static void *bits_worker(void *p) {
+  bits_job *j = (bits_job *)p;
+  for (int64_t i = j->i0; i < j->i1; ++i) {
+    union {
+      uint32_t u;
+      float f;
+    } c;
+    c.u = j->first + (uint32_t)i;
+    j->out[i] = orc_e4m3_encode((double)c.f);
+  }
+  return NULL;
+}
+
+void orc_e4m3_encode_bits_range(uint32_t first, int64_t n, uint8_t *out, int nthreads) {
+  enum { MAX_THREADS = 256 };
+  if (n <= 0) return;
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > MAX_THREADS) nthreads = MAX_THREADS;
+  pthread_t th[MAX_THREADS];
+  int joined[MAX_THREADS];
+  bits_job jobs[MAX_THREADS];
+  int64_t per = (n + nthreads - 1) / nthreads;
+  for (int t = 0; t < nthreads; ++t) {
+    jobs[t].first = first;
+    jobs[t].out = out;
+    jobs[t].i0 = (int64_t)t * per < n ? (int64_t)t * per : n;
+    jobs[t].i1 = jobs[t].i0 + per < n ? jobs[t].i0 + per : n;
+    joined[t] = pthread_create(&th[t], NULL, bits_worker, &jobs[t]) == 0;
+    if (!joined[t]) bits_worker(&jobs[t]); /* no thread available: run inline */
+  }
+  for (int t = 0; t < nthreads; ++t)
+    if (joined[t]) pthread_join(th[t], NULL);
 }
 
 /* binary32 amax floored at 1e-10, then the binary32 division amax / 448. */

@@ -36,6 +36,8 @@ float   orc_bf16_to_f32(uint16_t b);
 /* Array forms of the codecs (binary32 inputs, as a kernel converts them). */
 void    orc_e4m3_encode_f32_array(const float *v, int64_t n, uint8_t *out);
 void    orc_e4m3_decode_array(const uint8_t *c, int64_t n, double *out);
+/* codes of the binary32 values with bit patterns first .. first + n - 1 */
+void    orc_e4m3_encode_bits_range(uint32_t first, int64_t n, uint8_t *out, int nthreads);
 
 /* ---- quantisers (activation side) -------------------------------------- */
 /* Per-token group quantisation, FP32 scales, row-major s[M][ceil(K/group)]. */

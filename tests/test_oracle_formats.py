@@ -205,3 +205,18 @@ def test_generator_thread_invariance(threads):
     a = si.normal_bf16(300, 1000, 0.02, 1, chunk_elems=20000, threads=threads)
     b = si.normal_bf16(300, 1000, 0.02, 1, chunk_elems=1 << 22, threads=1)
     assert np.array_equal(a, b)
+
+
+def test_encode_bits_range_is_the_encoder_on_each_pattern():
+    """The range encoder used by the exhaustive GPU sweep is the pinned
+    encoder applied to consecutive binary32 bit patterns: around the subnormal
+    and normal boundaries, the saturation threshold, infinities and NaNs, and
+    at the ends of the 32-bit range; the thread count does not matter."""
+    for first, n in ((0, 4096), (0x3A7F_F000, 8192), (0x43DF_F000, 8192),
+                     (0x7F7F_FF00, 0x200), (0xFF7F_FF00, 0x100), ((1 << 32) - 300, 300)):
+        bits = (np.uint64(first) + np.arange(n, dtype=np.uint64)).astype(np.uint32)
+        ref = oracle.e4m3_encode(bits.view(np.float32))
+        for threads in (1, 3):
+            assert np.array_equal(oracle.e4m3_encode_bits_range(first, n, threads=threads), ref)
+    with pytest.raises(ValueError):
+        oracle.e4m3_encode_bits_range((1 << 32) - 2, 3)
