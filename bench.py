@@ -671,7 +671,8 @@ def run_extra(fb, torch, dev, stream, hbm_peak, fp8_peak, keep):
     ss = [torch.empty(M, dtype=torch.float32, device=dev) for _ in range(ns)]
     t = _time_graph(torch, [lambda i=i: fb.fp8bq_channel_quant_act(xs[i], qs[i], ss[i])
                             for i in range(ns)], 2 * ns)
-    ch["quant_4096x6144"] = {"us": round(t * 1e3, 2), "gbs": round(b / (t * 1e-3) / 1e9, 1),
+    ch["quant_4096x6144"] = {"us": round(t * 1e3, 2), "us_p10_p50_p90": t.us_pct(),
+                             "gbs": round(b / (t * 1e-3) / 1e9, 1),
                              "frac_hbm": round(b / (t * 1e-3) / 1e9 / hbm_peak, 4)}
     qa, sa = qs[0], ss[0]
     del xs
@@ -724,7 +725,8 @@ def run_extra(fb, torch, dev, stream, hbm_peak, fp8_peak, keep):
     us = [torch.empty(M, KB, dtype=torch.uint8, device=dev) for _ in range(ns)]
     t = _time_graph(torch, [lambda i=i: fb.fp8bq_quant_act_ue8m0(xs[i], qs[i], us[i])
                             for i in range(ns)], 2 * ns)
-    ue["quant_4096x6144"] = {"us": round(t * 1e3, 2), "gbs": round(b / (t * 1e-3) / 1e9, 1),
+    ue["quant_4096x6144"] = {"us": round(t * 1e3, 2), "us_p10_p50_p90": t.us_pct(),
+                             "gbs": round(b / (t * 1e-3) / 1e9, 1),
                              "frac_hbm": round(b / (t * 1e-3) / 1e9 / hbm_peak, 4)}
     qa, ua = qs[0], us[0]
     del xs
@@ -1090,31 +1092,31 @@ def build_records(M, K, layers, gemm_lists, step_list, flops_step, extra, cpu, h
     dec_o = (cc.get("decode_6144x6144") or {}).get("per_M", {})
     for Ms, d in extra.get("decode_N6144_K6144", {}).items():
         o = dec_o.get(Ms)
-        rec("decode", "block GEMM", f"{Ms}x6144x6144", d["gemm_us_p10_p50_p90"], "hbm",
+        rec("decode", "block GEMM", f"{Ms}x6144x6144", d.get("gemm_us_p10_p50_p90"), "hbm",
             d["gemm_gbs"], "GB/s", d["gemm_frac_hbm"], (o or {}).get("parity"),
             None if o is None else {"s": o["s"], "cores": cc["decode_6144x6144"]["cores"],
                                     "sample": "every output"})
-        rec("decode", "linear", f"{Ms}x6144x6144", d["linear_us_p10_p50_p90"], "hbm",
+        rec("decode", "linear", f"{Ms}x6144x6144", d.get("linear_us_p10_p50_p90"), "hbm",
             d["linear_gbs"], "GB/s", d["linear_frac_hbm"], None, None)
     qd = extra.get("quant", {})
     if "group128_4096x6144" in qd:
         d, o = qd["group128_4096x6144"], cc.get("quant_group128_4096x6144")
-        rec("prefill", "group-128 quant", "4096x6144", d["us_p10_p50_p90"], "hbm", d["gbs"],
+        rec("prefill", "group-128 quant", "4096x6144", d.get("us_p10_p50_p90"), "hbm", d["gbs"],
             "GB/s", d["frac_hbm"], (o or {}).get("parity"), orc(o))
     if "mx_2048x7168" in qd:
         d, o = qd["mx_2048x7168"], cc.get("quant_mx_2048x7168")
-        rec("mxfp8", "MX quant", "2048x7168", d["us_p10_p50_p90"], "hbm", d["gbs"], "GB/s",
+        rec("mxfp8", "MX quant", "2048x7168", d.get("us_p10_p50_p90"), "hbm", d["gbs"], "GB/s",
             d["frac_hbm"], (o or {}).get("parity"), orc(o))
     d = extra.get("mx_gemm_2048x4096x7168")
     if d:
         o = cc.get("mxfp8_2048x4096x7168")
-        rec("mxfp8", "MX GEMM", "2048x4096x7168", d["us_p10_p50_p90"], "tensor", d["tflops"],
+        rec("mxfp8", "MX GEMM", "2048x4096x7168", d.get("us_p10_p50_p90"), "tensor", d["tflops"],
             "TFLOP/s", d["frac_fp8"], (o or {}).get("parity"), orc(o))
     st_o = (cc.get("static_14336x4096") or {}).get("per_M", {})
     for Ms, d in extra.get("static_N14336_K4096", {}).items():
         o = st_o.get(Ms)
         hbm = Ms == "1"
-        rec("static", "per-tensor GEMM", f"{Ms}x14336x4096", d["us_p10_p50_p90"],
+        rec("static", "per-tensor GEMM", f"{Ms}x14336x4096", d.get("us_p10_p50_p90"),
             "hbm" if hbm else "tensor", d["gbs"] if hbm else d["tflops"],
             "GB/s" if hbm else "TFLOP/s", d["frac_hbm"] if hbm else d["frac_fp8"],
             (o or {}).get("parity"),
@@ -1124,20 +1126,20 @@ def build_records(M, K, layers, gemm_lists, step_list, flops_step, extra, cpu, h
     gpu_tests = "tests -m gpu (not rechecked here)"
     for k, d in extra.get("channel_w8a8", {}).items():
         hbm = "gbs" in d and "tflops" not in d
-        rec("channelwise", k, k.split("_")[-1], d["us_p10_p50_p90"], "hbm" if hbm else "tensor",
+        rec("channelwise", k, k.split("_")[-1], d.get("us_p10_p50_p90"), "hbm" if hbm else "tensor",
             d["gbs"] if hbm else d["tflops"], "GB/s" if hbm else "TFLOP/s",
             d["frac_hbm"] if hbm else d["frac_fp8"], gpu_tests, None)
     for k, d in extra.get("block_ue8m0", {}).items():
         hbm = "tflops" not in d
-        rec("block UE8M0", k, k.split("_")[-1], d["us_p10_p50_p90"], "hbm" if hbm else "tensor",
+        rec("block UE8M0", k, k.split("_")[-1], d.get("us_p10_p50_p90"), "hbm" if hbm else "tensor",
             d["gbs"] if hbm else d["tflops"], "GB/s" if hbm else "TFLOP/s",
             d["frac_hbm"] if hbm else d["frac_fp8"], gpu_tests, None)
     for k, d in extra.get("grouped_moe", {}).items():
         if isinstance(d, dict):
-            rec("grouped MoE", k, k, d["us_p10_p50_p90"], "hbm", d["gbs"], "GB/s",
+            rec("grouped MoE", k, k, d.get("us_p10_p50_p90"), "hbm", d["gbs"], "GB/s",
                 d["frac_hbm"], gpu_tests, None)
     for k, d in extra.get("add_rmsnorm_quant", {}).items():
-        rec("add + RMSNorm + quant", k, k.split("_")[-1], d["us_p10_p50_p90"], "hbm", d["gbs"],
+        rec("add + RMSNorm + quant", k, k.split("_")[-1], d.get("us_p10_p50_p90"), "hbm", d["gbs"],
             "GB/s", d["frac_hbm"], gpu_tests, None)
     return recs
 

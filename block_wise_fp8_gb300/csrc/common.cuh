@@ -226,5 +226,8 @@ cudaError_t run_mx_pair(const GemmArgs &a, const void *q, const void *w, const L
 // fp8bq status; a CUDA error is returned through `cuda_err`.
 int launch_gemm(const GemmArgs &a, const void *q_act, const void *w, const DeviceInfo &dev,
                 cudaStream_t st, cudaError_t *cuda_err);
+// K split of the decode tiles (M <= 64): the number of splits (0 if K is too
+// large for them) and, in *kps, the K blocks per split
+int decode_splits(int64_t N, int64_t K, int num_sms, int *kps);
 
 }  // namespace fp8bq

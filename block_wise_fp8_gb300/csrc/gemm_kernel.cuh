@@ -41,8 +41,9 @@
 //           range order (split_tail_tiles).
 //   normal  the same with one CTA: UMMA M = 128 tokens, UMMA N = BN weight rows.
 //   swap    UMMA M = 128 weight rows, UMMA N = BN tokens (decode, M <= 64), with
-//           split-K across CTAs and a deterministic last-CTA reduction in
-//           ascending split order.
+//           split-K across CTAs: split 0 of each weight tile polls the other
+//           splits' partials (no counter, no election) and sums them in
+//           ascending split order (deterministic).
 //   grouped (GROUPED instances, block pair or normal) the MoE form: A and Y rows
 //           are split into per-expert segments whose bounds the kernel reads
 //           from the device; every CTA builds the m-tile table in shared
@@ -91,8 +92,12 @@ struct Cfg {
   static constexpr int kSfBBytes = 128 * kSfColsBPad;
   static constexpr int kSfStageBytes = (MODE == kModeMx) ? 512 + kSfBBytes : 0;
   // block tiles: two MMA-issuing warps take alternate K blocks (disjoint TMEM
-  // partial buffers), so one issues while the other waits on its barriers
-  static constexpr int kIssuers = (MODE == kModeBlock) ? 2 : 1;
+  // partial buffers), so one issues while the other waits on its barriers.
+  // The decode tiles with 16 or 32 tokens issue from four warps: their MMAs
+  // are so short that one MMA instruction's issue latency, not its work, sets
+  // the pace (measured 10.4 -> 9.1 us at 1 x 6144 x 6144; the 64-token tile
+  // measured slower with four)
+  static constexpr int kIssuers = (MODE == kModeBlock) ? ((SWAP && BN <= 32) ? 4 : 2) : 1;
   // block pair and normal tiles keep the promoted FP32 accumulators in the
   // epilogue warps' registers: warpgroup 0 (producer, the two issuers and one
   // idle warp) hands registers to the epilogue warpgroups with setmaxnreg
@@ -324,6 +329,36 @@ __device__ __forceinline__ Unit decode_unit(int u, int num_a_tiles, int splits, 
   r.kb0 = r.split * kps;
   r.kb1 = min(KB, r.kb0 + kps);
   return r;
+}
+
+// Split-K partials of one split for one weight row: v[j] = the slot of token j
+// (j < M, rows `stride` apart) once every one of them is non-zero, i.e. written
+// (slots j >= M read as 1, the encoding of 0.0).  Polls with a short sleep;
+// gives up, setting `abort`, after `limit_ns` or when another wait of the CTA
+// has given up.
+template <int CNT>
+__device__ __forceinline__ bool poll_partials(const uint32_t *src, int64_t stride, int M,
+                                              uint32_t (&v)[CNT], volatile uint32_t *abort,
+                                              uint64_t limit_ns) {
+  uint64_t t0 = 0;
+  while (true) {
+    bool all = true;
+#pragma unroll
+    for (int j = 0; j < CNT; ++j) {
+      v[j] = j < M ? ld_relaxed_gpu(src + static_cast<int64_t>(j) * stride) : 1u;
+      all = all && v[j] != 0u;
+    }
+    if (all) return true;
+    if (*abort) return false;
+    const uint64_t now = global_timer_ns();
+    if (t0 == 0) {
+      t0 = now;
+    } else if (now - t0 > limit_ns) {
+      *abort = 1u;
+      return false;
+    }
+    __nanosleep(64);
+  }
 }
 
 // Store `n` (multiple of 8 unless ragged) BF16 values of row m starting at column c0.
@@ -1046,54 +1081,60 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
               }
           }
         } else {
-          // split-K: publish FP32 partials, the last CTA of the tile reduces them
-          float *part = args.partials;
-          if (n_ok) {
-#pragma unroll
-            for (int j = 0; j < C::kCPT; ++j)
-              if (j < args.M)
-                __stcg(part + (static_cast<int64_t>(w.split) * args.M + j) * args.N + n, acc[j]);
-          }
-          // the barrier orders every epilogue thread's partial stores before the
-          // counter update, whose release (GPU scope) publishes them; the last
-          // CTA's acquire on the same update makes all splits' partials visible
-          // to its epilogue threads after the next barrier
-          named_bar_sync(2, C::kEpiThreads);
-          if (et == 0) {
-            const uint32_t prev = atom_add_acq_rel_gpu(args.counters + w.tile, 1u);
-            bars->is_last = (prev == static_cast<uint32_t>(shape.splits - 1)) ? 1u : 0u;
-          }
-          named_bar_sync(2, C::kEpiThreads);
-          if (bars->is_last) {
+          // split-K: the K range of weight tile w.tile is split over
+          // shape.splits CTAs.  Splits 1.. publish their FP32 partials and
+          // leave; split 0 sums them into its own in ascending split order and
+          // writes Y.  A partial travels as its bits + 1 in a relaxed GPU-scope
+          // store, so a slot holding 0 has not been written yet (FP32
+          // arithmetic never yields the bits 0xFFFFFFFF, the one value that
+          // would wrap to 0): split 0 polls the elements themselves -- no
+          // counter, no fence, no election on the path -- and writes 0 back to
+          // every slot it consumed, which leaves the workspace ready for the
+          // next call.  The polling ends because every CTA of the grid is
+          // resident at once (one CTA per SM, tiles x splits <= SMs, and no
+          // CTA waits on anything that a later kernel produces); it is bounded
+          // all the same.
+          uint32_t *part = reinterpret_cast<uint32_t *>(args.partials);
+          if (w.split != 0) {
             if (n_ok) {
-              // ascending split order; all of one split's loads are in flight at once
-              float sum[C::kCPT];
+              uint32_t *dst = part + static_cast<int64_t>(w.split) * args.M * args.N + n;
 #pragma unroll
-              for (int j = 0; j < C::kCPT; ++j) sum[j] = 0.0f;
-              for (int sp = 0; sp < shape.splits; ++sp) {
-                if (sp == w.split) {
+              for (int j = 0; j < C::kCPT; ++j)
+                if (j < args.M)
+                  st_relaxed_gpu(dst + static_cast<int64_t>(j) * args.N, __float_as_uint(acc[j]) + 1u);
+            }
+          } else if (n_ok) {
+            float sum[C::kCPT];
 #pragma unroll
-                  for (int j = 0; j < C::kCPT; ++j) sum[j] += acc[j];
-                } else {
-                  const float *src = part + static_cast<int64_t>(sp) * args.M * args.N + n;
-                  float v[C::kCPT];
+            for (int j = 0; j < C::kCPT; ++j) sum[j] = acc[j];
+            bool got = true;
+            for (int sp = 1; sp < shape.splits && got; ++sp) {
+              uint32_t *src = part + static_cast<int64_t>(sp) * args.M * args.N + n;
+              uint32_t v[C::kCPT];
+              got = poll_partials<C::kCPT>(src, args.N, args.M, v, abort_flag, limit);
+              if (got) {
 #pragma unroll
-                  for (int j = 0; j < C::kCPT; ++j)
-                    v[j] = (j < args.M) ? __ldcg(src + static_cast<int64_t>(j) * args.N) : 0.0f;
-#pragma unroll
-                  for (int j = 0; j < C::kCPT; ++j) sum[j] += v[j];
-                }
+                for (int j = 0; j < C::kCPT; ++j) sum[j] += __uint_as_float(v[j] - 1u);
               }
+            }
+            if (got) {
 #pragma unroll
               for (int j = 0; j < C::kCPT; ++j)
                 if (j < args.M) {
                   __nv_bfloat16 h = __float2bfloat16_rn(sum[j] + bv);
                   y[static_cast<int64_t>(j) * args.N + n] = *reinterpret_cast<uint16_t *>(&h);
                 }
+              // consumed: back to "not written" for the next call
+              for (int sp = 1; sp < shape.splits; ++sp) {
+                uint32_t *src = part + static_cast<int64_t>(sp) * args.M * args.N + n;
+#pragma unroll
+                for (int j = 0; j < C::kCPT; ++j)
+                  if (j < args.M) src[static_cast<int64_t>(j) * args.N] = 0u;
+              }
+            } else {
+              record_timeout(args);
             }
-            if (et == 0) args.counters[w.tile] = 0u;  // ready for the next call
           }
-          named_bar_sync(2, C::kEpiThreads);
         }
       }
     }

@@ -27,6 +27,27 @@ constexpr int kMaxSplits = 8;
 
 }  // namespace
 
+// Decode (M <= 64) tiles: 128 weight rows each, the K blocks split over
+// splits CTAs so that tiles x splits fills the SMs (at most kMaxSplits, each
+// split at most 64 K blocks, no empty split).  Returns the split count and
+// the K blocks per split, or 0 when K needs more than kMaxSplits x 64 blocks.
+int decode_splits(int64_t N, int64_t K, int num_sms, int *kps_out) {
+  const int KB = static_cast<int>((K + 127) / 128);
+  const int tiles = static_cast<int>((N + 127) / 128);
+  int splits = num_sms / tiles;
+  if (splits < 1) splits = 1;
+  if (splits > kMaxSplits) splits = kMaxSplits;
+  if (splits > KB) splits = KB;
+  int kps = (KB + splits - 1) / splits;
+  while (kps > 64 && splits < kMaxSplits) {  // bounds the s_x staging buffer
+    ++splits;
+    kps = (KB + splits - 1) / splits;
+  }
+  if (kps > 64) return 0;
+  *kps_out = kps;
+  return (KB + kps - 1) / kps;  // no empty split
+}
+
 bool make_kmajor_map(CUtensorMap *m, const void *base, int64_t rows, int64_t K, int box_rows) {
   auto enc = get_encoder();
   if (!enc) return false;
@@ -245,19 +266,11 @@ int launch_gemm(const GemmArgs &a, const void *q_act, const void *w, const Devic
   const bool swap = (a.mode != kModeMx) && a.M <= 64;
   if (swap) {
     // decode: weight rows on the MMA's M side, tokens on its N side, K split so
-    // that tiles x splits fills the SMs; partials reduced by the last CTA
+    // that tiles x splits fills the SMs; split 0 of each tile sums the partials
     const int tiles = (a.N + 127) / 128;
-    int splits = dev.num_sms / tiles;
-    if (splits < 1) splits = 1;
-    if (splits > kMaxSplits) splits = kMaxSplits;
-    if (splits > sh.KB) splits = sh.KB;
-    int kps = (sh.KB + splits - 1) / splits;
-    while (kps > 64 && splits < kMaxSplits) {  // bounds the s_x staging buffer
-      ++splits;
-      kps = (sh.KB + splits - 1) / splits;
-    }
-    if (kps > 64) return 4;  // FP8BQ_ERR_UNSUPPORTED: K too large for the decode tile
-    splits = (sh.KB + kps - 1) / kps;  // no empty split
+    int kps = 0;
+    const int splits = decode_splits(a.N, a.K, dev.num_sms, &kps);
+    if (splits == 0) return 4;  // FP8BQ_ERR_UNSUPPORTED: K too large for the decode tile
     sh.splits = splits;
     sh.kps = kps;
     sh.num_a_tiles = tiles;

@@ -49,8 +49,9 @@
  *  - GEMM and linear entry points take a workspace `ws` of at least
  *    fp8bq_workspace_bytes(op, M, N, K) bytes, 256-byte aligned, zeroed once
  *    with fp8bq_workspace_init before its first use.  The library keeps it in a
- *    valid state between calls.  Besides a status word and tile counters it
- *    holds FP32 partial sums: the split-K decode tiles' (M <= 64) and, for the
+ *    valid state between calls (every partial-sum slot a call fills is read
+ *    and cleared again within the same call).  Besides a status word and tile
+ *    counters it holds FP32 partial sums: the split-K decode tiles' (M <= 64) and, for the
  *    block GEMM and linear above 64 rows, those of the last wave's tiles,
  *    which run split into K ranges on otherwise idle SMs (256 KB per split,
  *    at most 80 splits: up to 20 MB).  Calls that share a workspace must not overlap
