@@ -126,6 +126,10 @@ struct GemmArgs {
   // fault injection for the timeout tests (0 in normal use): CTA 0 issues no
   // copy for its first K block, so the waits on that stage run out
   int fault_skip_first_load;
+  // fused decode linear: the BF16 activations [M, K] (pitch ldxq elements)
+  // that the GEMM quantises itself; nullptr otherwise
+  const void *xq;
+  int64_t ldxq;
 };
 
 struct DeviceInfo {
@@ -196,6 +200,10 @@ bool cached_f32_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols
 // through a small cache like the one above.
 bool cached_bf16_rows_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols,
                           int box_cols, int box_rows);
+// BF16 [rows, cols] with a row pitch of `pitch` elements, unswizzled boxes of
+// [box_rows x box_cols] (the fused decode linear's activations)
+bool cached_bf16_pitched_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols,
+                             int64_t pitch, int box_cols, int box_rows);
 
 // Kernel variants, one translation unit each (instantiated from gemm_kernel.cuh).
 // Pair (prefill) forms: `bn` is the weight-row tile, 192 or 256, and `grid` the
@@ -207,6 +215,8 @@ cudaError_t run_block_pair(int bn, const GemmArgs &a, const void *q, const void 
 // 128 x 256 tiles (`grid` CTAs).
 cudaError_t run_block_grouped(bool pair, const GemmArgs &a, const void *q, const void *w,
                               const LaunchShape &sh, int grid, cudaStream_t st, int *status);
+cudaError_t run_block_swap_fused(int bn, const GemmArgs &a, const void *w, const LaunchShape &sh,
+                                 int grid, cudaStream_t st, int *status);
 cudaError_t run_block_swap(int bn, const GemmArgs &a, const void *q, const void *w,
                            const LaunchShape &sh, int grid, cudaStream_t st, int *status);
 cudaError_t run_tensor_pair(int bn, const GemmArgs &a, const void *q, const void *w,

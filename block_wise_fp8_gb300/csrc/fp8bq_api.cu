@@ -388,6 +388,14 @@ int fp8bq_gemm(const void *q, const float *s_x, int s_layout, const void *w, con
                          static_cast<cudaStream_t>(stream), dev);
 }
 
+// Up to this many tokens the decode linear quantises inside the GEMM (every
+// weight tile's CTAs quantise the same activations again, which pays only while
+// the token rows are few); above, the quantiser kernel runs first.
+#ifndef FP8BQ_FUSED_LINEAR_MAX_M
+#define FP8BQ_FUSED_LINEAR_MAX_M 16
+#endif
+constexpr int64_t kFusedLinearMaxM = FP8BQ_FUSED_LINEAR_MAX_M;
+
 int fp8bq_linear(const void *x, int64_t ldx, const void *w, const float *s_w, const void *bias,
                  void *y, int64_t M, int64_t N, int64_t K, void *ws, size_t ws_bytes,
                  void *stream) {
@@ -402,6 +410,19 @@ int fp8bq_linear(const void *x, int64_t ldx, const void *w, const float *s_w, co
   DeviceInfo dev;
   RETURN_IF(device_info(&dev));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (M <= kFusedLinearMaxM) {
+    // decode: one launch -- the GEMM's CTAs quantise the activations of
+    // their own K range as the stages arrive (same codes and scales as
+    // fp8bq_quant_act), with no second kernel and no round trip through the
+    // workspace
+    GemmArgs a = base_args(kModeBlock, M, N, K, bias, y, ws, FP8BQ_OP_LINEAR);
+    a.sw = s_w;
+    a.xq = x;
+    a.ldxq = ldx;
+    cudaError_t e;
+    const int r = launch_gemm(a, nullptr, w, dev, st, &e);
+    return finish_launch(r, e);
+  }
   const WorkspaceLayout L = workspace_layout(FP8BQ_OP_LINEAR, M, N, K);
   uint8_t *q = static_cast<uint8_t *>(ws) + L.q;
   float *s = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + L.s);

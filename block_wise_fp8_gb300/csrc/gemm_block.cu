@@ -20,6 +20,18 @@ cudaError_t run_block_grouped(bool pair, const GemmArgs &a, const void *q, const
   return run<kModeBlock, false, 256, 3, 8, 2, false, true>(a, q, w, sh, grid, st, status);
 }
 
+// the decode linear with the activation quantisation fused in: each stage also
+// holds the BF16 activation slice (256 B per token), so the deeper tiles keep
+// fewer stages
+cudaError_t run_block_swap_fused(int bn, const GemmArgs &a, const void *w, const LaunchShape &sh,
+                                 int grid, cudaStream_t st, int *status) {
+  switch (bn) {
+    case 16: return run<kModeBlock, true, 16, 8, 4, 8, false, false, true>(a, nullptr, w, sh, grid, st, status);
+    case 32: return run<kModeBlock, true, 32, 7, 4, 8, false, false, true>(a, nullptr, w, sh, grid, st, status);
+    default: return run<kModeBlock, true, 64, 5, 4, 8, false, false, true>(a, nullptr, w, sh, grid, st, status);
+  }
+}
+
 cudaError_t run_block_swap(int bn, const GemmArgs &a, const void *q, const void *w,
                            const LaunchShape &sh, int grid, cudaStream_t st, int *status) {
   switch (bn) {

@@ -62,6 +62,7 @@
 
 #include "common.cuh"
 #include "ptx.cuh"
+#include "quant_math.cuh"
 
 namespace fp8bq {
 namespace {
@@ -76,7 +77,7 @@ constexpr uint32_t pow2_at_least(uint32_t v) {
 }
 
 template <int MODE, bool SWAP, int BN, int STAGES, int EPI_WARPS, int ACCB, bool PAIR,
-          bool GROUPED = false>
+          bool GROUPED = false, bool FUSEQ = false>
 struct Cfg {
   static constexpr int kMmaM = PAIR ? 256 : 128;     // rows of the MMA (both CTAs)
   static constexpr int kBrows = PAIR ? BN / 2 : BN;  // weight rows loaded by this CTA
@@ -103,7 +104,12 @@ struct Cfg {
   // idle warp) hands registers to the epilogue warpgroups with setmaxnreg
   static constexpr bool kRegSplit = (MODE == kModeBlock) && !SWAP;
   static constexpr int kEpiBase = kRegSplit ? 4 : 1 + kIssuers;  // first epilogue warp
-  static constexpr int kThreads = 32 * (kEpiBase + EPI_WARPS);
+  // fused decode linear (FUSEQ): four more warps quantise each stage's BF16
+  // activation slice into the stage's E4M3 operand
+  static constexpr bool kFuseQ = FUSEQ;
+  static constexpr int kQWarps = FUSEQ ? 4 : 0;
+  static constexpr int kQBase = kEpiBase + EPI_WARPS;          // first quantiser warp
+  static constexpr int kThreads = 32 * (kEpiBase + EPI_WARPS + kQWarps);
   // register budget: warps are dealt round-robin to the SM's four schedulers,
   // each with a quarter of the register file, so the bound counts whole
   // groups of four warps
@@ -133,8 +139,14 @@ struct Cfg {
   // one box per epilogue warp; a thread's columns beyond one box go out in
   // further rounds through the same box
   static constexpr int kYStageBytes = kTmaStoreY ? EPI_WARPS * kYBoxBytes : 0;
-  static constexpr int kBbytes = kBrows * 128;
+  // B slot of a stage: the E4M3 operand (kBrows x 128 B, 128-byte swizzled);
+  // fused: followed by the BF16 activation slice it is quantised from
+  // (kBrows x 128 values, 256 B per row, unswizzled)
+  static constexpr int kXbytes = FUSEQ ? kBrows * 256 : 0;
+  static constexpr int kBbytes = kBrows * 128 + kXbytes;
   static constexpr int kStageBytes = kAbytes + kBbytes;
+  // bytes that land on a stage's full barrier
+  static constexpr int kTxBytes = FUSEQ ? kAbytes + kXbytes : kStageBytes;
   // block pair and normal tiles: promotion factors come through a shared-memory
   // ring filled by the TMA producer, kScQuad K blocks per slot: s_x of this
   // CTA's 128 rows and s_w of the tile's (at most two) 128-row weight blocks
@@ -168,6 +180,9 @@ struct Cfg {
                 "block tiles: each thread's columns lie in one 128-row weight block");
   static_assert(!SWAP || (kCPT <= 64 && EPI_WARPS == 4),
                 "swapped tiles keep all token columns of a weight row in one thread");
+  static_assert(!FUSEQ || (SWAP && MODE == kModeBlock && !PAIR && !GROUPED &&
+                           (kBrows * 128) % 1024 == 0 && kBbytes % 1024 == 0),
+                "fused quantisation: decode block tiles, swizzle atoms aligned");
   static_assert(!kRegSplit || (kThreads % 128 == 0 && kHighRegs >= kLowRegs &&
                                128 * kLowRegs + (kThreads - 128) * kHighRegs <=
                                    kLaunchRegs * kThreads),
@@ -181,6 +196,7 @@ struct SmemBarriers {
   uint64_t full[8], empty[8];
   uint64_t tfull[8], tempty[8];
   uint64_t sc_full[4], sc_empty[4];
+  uint64_t qfull[8];  // fused quantisation: a stage's E4M3 operand is written
   uint64_t drain;
   uint32_t tmem_base;
   uint32_t abort;
@@ -390,15 +406,16 @@ __device__ __forceinline__ void store_row(uint16_t *y, const float *v, int m, in
 
 // One CTA per SM.  Registers are split over the SM's four schedulers, so the
 // per-thread budget is set by the scheduler holding the most warps.
-template <int MODE, bool SWAP, int BN, int STAGES, int EPI_WARPS, int ACCB, bool PAIR, bool GROUPED>
-__global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, PAIR, GROUPED>::kBoundThreads, 1)
+template <int MODE, bool SWAP, int BN, int STAGES, int EPI_WARPS, int ACCB, bool PAIR, bool GROUPED,
+          bool FUSEQ>
+__global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, PAIR, GROUPED, FUSEQ>::kBoundThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmY,
                     const __grid_constant__ CUtensorMap tmSx,
                     const __grid_constant__ CUtensorMap tmSw,
                     const __grid_constant__ GemmArgs args, const LaunchShape shape) {
-  using C = Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, PAIR, GROUPED>;
+  using C = Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, PAIR, GROUPED, FUSEQ>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -433,6 +450,7 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
       mbar_init(&bars->sc_full[s], 1);
       mbar_init(&bars->sc_empty[s], EPI_WARPS);
     }
+    for (int s = 0; s < (C::kFuseQ ? STAGES : 0); ++s) mbar_init(&bars->qfull[s], C::kQWarps);
     mbar_init(&bars->drain, C::kIssuers);
     bars->abort = 0;
     bars->is_last = 0;
@@ -592,6 +610,12 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
                 tma_load_2d_pair(sf, &tmSx, bar0, 0, sfa_row);
                 tma_load_2d_pair(sf + 512, &tmSw, bar0, 0, sfb_row);
               }
+            } else if (C::kFuseQ) {
+              // the weight tile and the BF16 activations of K block kb (all
+              // tokens; rows >= M and columns >= K read as zero)
+              mbar_arrive_expect_tx(&bars->full[s], C::kTxBytes);
+              tma_load_2d(sA + s * kAbytes, &tmA, &bars->full[s], kb * 128, w.a_row0);
+              tma_load_2d(sB + s * C::kBbytes + C::kBrows * 128, &tmB, &bars->full[s], kb * 128, 0);
             } else {
               mbar_arrive_expect_tx(&bars->full[s], C::kStageBytes + C::kSfStageBytes);
               tma_load_2d(sA + s * kAbytes, &tmA, &bars->full[s], kb * 128, w.a_row0);
@@ -655,7 +679,8 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
               d_tmem = tmem_base + (uit % ACCB) * BN;
             }
             const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
-            if (!mbar_wait(&bars->full[s], ph, abort_flag, limit)) {
+            // fused: the quantiser warps have seen the stage land and written its operand
+            if (!mbar_wait(C::kFuseQ ? &bars->qfull[s] : &bars->full[s], ph, abort_flag, limit)) {
               ok = false;
               break;
             }
@@ -718,7 +743,7 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
       }
       __syncwarp();
     }
-  } else {
+  } else if (warp < C::kQBase) {
     // ------------------------------------------------------------ epilogue
     const int ew = warp - C::kEpiBase;
     const int quarter = warp & 3;
@@ -990,7 +1015,8 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
         for (int j = 0; j < C::kCPT; ++j) acc[j] = 0.0f;
         if (MODE == kModeBlock) {
           // stage s_x[token][kb] for this unit's K range: sx_stage[(kb-kb0)*BN + token]
-          const int nkb = w.kb1 - w.kb0;
+          // (fused: the quantiser warps write it as they quantise each K block)
+          const int nkb = C::kFuseQ ? 0 : w.kb1 - w.kb0;
           for (int e = et; e < nkb * BN; e += C::kEpiThreads) {
             const int kb = w.kb0 + e / BN, t = e % BN;
             float v = 0.0f;
@@ -1141,6 +1167,68 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
     // the staging boxes stay in use until this warp's TMA stores complete
     if (C::kTmaStoreY && lane == 0) bulk_wait_group0();
     if (!ok && et == 0) record_timeout(args);
+  } else if (C::kFuseQ) {
+    // ------------------------------------------------------------ fused activation quantiser
+    // Per K block: the group-128 quantisation of every token's 128 BF16 values
+    // in the stage (one group per token: s = amax / 448 from the scale table,
+    // codes = RNE_sat(x / s) from the FMA-corrected quotient -- the arithmetic
+    // of the activation quantiser kernel, so the codes and scales are the
+    // same bits), codes into the stage's E4M3 operand in the 128-byte swizzled
+    // layout the MMA reads, scales into sx_stage for the promotion.  Eight
+    // threads per token, 16 values each.
+    const int qt = threadIdx.x - 32 * C::kQBase;  // 0 .. 127
+    ScaleTable &table = *reinterpret_cast<ScaleTable *>(sx_stage + shape.sx_stage);
+    for (int m = qt; m <= 128; m += 32 * C::kQWarps) {
+      const float a = m < 128 ? 1.0f + static_cast<float>(m) * 0.0078125f : kFloor;
+      const float sv = __fdiv_rn(a, 448.0f);
+      const float2 v = make_float2(sv, __frcp_rn(sv));
+      if (m < 128) table.e[m] = v;
+      else table.floor_entry = v;
+    }
+    named_bar_sync(3, 32 * C::kQWarps);
+    uint32_t it = 0;
+    bool ok = true;
+    for (int u = cl_id; ok && u < units; u += cl_num) {
+      const Unit w = decode_unit<SWAP, PAIR, GROUPED>(u, num_a, shape.splits, shape.kps, KB, BN, rank, args.M, args.N, gt, shape);
+      for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
+        const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+        if (!warp_wait(&bars->full[s], ph, abort_flag, limit)) {
+          ok = false;
+          break;
+        }
+        uint8_t *codes = sB + s * C::kBbytes;
+        const uint8_t *xs = codes + C::kBrows * 128;
+        // Token rows >= M only feed output columns that are never stored, so
+        // whole warps past them skip the work.  The bound is rounded up to
+        // whole warps: every lane of a warp that enters runs the shuffles
+        // (rows below BN, inside the stage), only rows < M store.
+        const int lim = min(BN * 8, (args.M * 8 + 31) / 32 * 32);
+        for (int task = qt; task < lim; task += 32 * C::kQWarps) {
+          const int t = task >> 3, sub = task & 7;
+          uint4 v[2];
+          v[0] = *reinterpret_cast<const uint4 *>(xs + t * 256 + sub * 32);
+          v[1] = *reinterpret_cast<const uint4 *>(xs + t * 256 + sub * 32 + 16);
+          float f[16];
+          unpack16(v, f);
+          float amax = amax16(f);
+          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+          const float2 sc = scale_of(table, amax);
+          // 16-byte chunk c of row t sits at chunk position c ^ (t % 8)
+          const uint4 out = quant16<1>(v, f, sc.x, sc.y);
+          if (t < args.M) {
+            *reinterpret_cast<uint4 *>(codes + t * 128 + ((sub ^ (t & 7)) << 4)) = out;
+            if (sub == 0) sx_stage[(kb - w.kb0) * BN + t] = sc.x;
+          }
+        }
+        // the operand is read by the tensor cores (async proxy)
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->qfull[s]);
+      }
+    }
+    if (!ok && qt == 0) record_timeout(args);
   }
 
   // ------------------------------------------------------------ teardown
@@ -1183,10 +1271,10 @@ inline void split_tail_tiles(LaunchShape &sh, int clusters, int64_t partials_byt
 // for pair tiles; for pair tiles it is clamped to the clusters the device can
 // hold at once, so the persistent grid is a single wave.
 template <int MODE, bool SWAP, int BN, int STAGES, int EPI_WARPS, int ACCB, bool PAIR,
-          bool GROUPED = false>
+          bool GROUPED = false, bool FUSEQ = false>
 cudaError_t run(const GemmArgs &a, const void *q_act, const void *w, const LaunchShape &sh,
                 int grid, cudaStream_t st, int *status) {
-  using C = Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, PAIR, GROUPED>;
+  using C = Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, PAIR, GROUPED, FUSEQ>;
   static_assert(!GROUPED || (MODE == kModeBlock && !SWAP), "grouped: block tiles");
   if (GROUPED != (a.g_experts > 0)) {
     *status = 4;  // FP8BQ_ERR_UNSUPPORTED: grouped arguments to a plain variant or back
@@ -1236,19 +1324,24 @@ cudaError_t run(const GemmArgs &a, const void *q_act, const void *w, const Launc
   const int64_t a_rows = SWAP ? a.N : a.M;
   // grouped form: all experts' weights as one [E * N, K] operand
   const int64_t b_rows = SWAP ? a.M : static_cast<int64_t>(a.N) * (a.g_experts > 0 ? a.g_experts : 1);
-  if (!cached_kmajor_map(&ta, a_ptr, a_rows, a.K, kBM) ||
-      !cached_kmajor_map(&tb, b_ptr, b_rows, a.K, C::kBrows)) {
+  // fused quantisation: B is the BF16 activation matrix [M, K] (pitch ldxq),
+  // loaded unswizzled in [kBrows tokens x 128 values] boxes
+  const bool b_ok = FUSEQ ? (a.xq != nullptr && al16(a.xq) &&
+                             cached_bf16_pitched_map(&tb, a.xq, a.M, a.K, a.ldxq, 128, C::kBrows))
+                          : cached_kmajor_map(&tb, b_ptr, b_rows, a.K, C::kBrows);
+  if (!cached_kmajor_map(&ta, a_ptr, a_rows, a.K, kBM) || !b_ok) {
     *status = 4;  // FP8BQ_ERR_UNSUPPORTED: tensor map rejected
     return cudaSuccess;
   }
-  const size_t smem = C::kFixedSmem + static_cast<size_t>(sh.sx_stage) * sizeof(float);
-  auto kern = fp8_gemm_kernel<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, PAIR, GROUPED>;
+  const size_t smem = C::kFixedSmem + static_cast<size_t>(sh.sx_stage) * sizeof(float) +
+                      (FUSEQ ? sizeof(ScaleTable) : 0);
+  auto kern = fp8_gemm_kernel<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, PAIR, GROUPED, FUSEQ>;
   // the opt-in shared-memory limit is raised once per variant to the largest
   // request it can see: the fixed part plus the biggest s_x staging buffer
   // (swapped tiles) or, where it fits in 227 KB, the grouped form's tile table
   // (pair tiles)
   constexpr size_t kSmemCap = 227 * 1024;
-  constexpr size_t kTail = SWAP ? size_t(BN) * 64 * sizeof(float)
+  constexpr size_t kTail = SWAP ? size_t(BN) * 64 * sizeof(float) + (FUSEQ ? sizeof(ScaleTable) : 0)
                            : GROUPED ? kGroupTableBytes
                                                                                      : 0;
   static_assert(C::kFixedSmem + kTail <= kSmemCap, "shared memory");

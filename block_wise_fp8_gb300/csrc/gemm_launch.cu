@@ -186,6 +186,51 @@ bool cached_bf16_rows_map(CUtensorMap *m, const void *base, int64_t rows, int64_
   return true;
 }
 
+bool cached_bf16_pitched_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols,
+                             int64_t pitch, int box_cols, int box_rows) {
+  struct Entry {
+    const void *base;
+    int64_t rows, cols, pitch;
+    int bc, br;
+    CUtensorMap map;
+  };
+  constexpr int kEntries = 16;
+  static Entry cache[kEntries];
+  static int used = 0, next = 0;
+  static std::mutex mu;
+  {
+    std::lock_guard<std::mutex> g(mu);
+    for (int i = 0; i < used; ++i)
+      if (cache[i].base == base && cache[i].rows == rows && cache[i].cols == cols &&
+          cache[i].pitch == pitch && cache[i].bc == box_cols && cache[i].br == box_rows) {
+        *m = cache[i].map;
+        return true;
+      }
+  }
+  auto enc = get_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(pitch) * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return false;
+  std::lock_guard<std::mutex> g(mu);
+  Entry &e = cache[next];
+  e.base = base;
+  e.rows = rows;
+  e.cols = cols;
+  e.pitch = pitch;
+  e.bc = box_cols;
+  e.br = box_rows;
+  e.map = *m;
+  next = (next + 1) % kEntries;
+  if (used < kEntries) ++used;
+  return true;
+}
+
 // [status word | split-K tile counters | split-K FP32 partials | fused: Q | fused: scales |
 //  MX: activation and weight scale-factor chunks]
 WorkspaceLayout workspace_layout(int op, int64_t M, int64_t N, int64_t K, bool tail) {
@@ -277,6 +322,12 @@ int launch_gemm(const GemmArgs &a, const void *q_act, const void *w, const Devic
     sh.units = tiles * splits;
     const int bn = a.M <= 16 ? 16 : a.M <= 32 ? 32 : 64;
     sh.sx_stage = (a.mode == kModeBlock) ? bn * kps : 0;
+    if (a.xq) {
+      // fused decode linear: the GEMM quantises the activations itself
+      if (a.mode != kModeBlock) return 4;
+      *cuda_err = run_block_swap_fused(bn, a, w, sh, sh.units, st, &status);
+      return status;
+    }
     *cuda_err = (a.mode == kModeBlock)     ? run_block_swap(bn, a, q_act, w, sh, sh.units, st, &status)
                 : (a.mode == kModeChannel) ? run_channel_swap(bn, a, q_act, w, sh, sh.units, st, &status)
                                            : run_tensor_swap(bn, a, q_act, w, sh, sh.units, st, &status);

@@ -199,3 +199,39 @@ def test_empty_batch():
     sw = torch.ones(2, 2, dtype=torch.float32, device="cuda")
     fb.fp8bq_gemm(q, s, w, sw, y, ws)
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 6144, 6144), (5, 200, 208), (16, 384, 256), (17, 640, 1040),
+                                   (33, 1000, 2048), (64, 6144, 6144), (8, 24576, 6144)])
+def test_decode_linear_fuses_quantisation_bit_exactly(M, N, K):
+    """Up to 64 tokens fp8bq_linear is one launch: the GEMM's CTAs quantise their
+    own K range of X as the stages arrive.  Its output must be bit for bit that
+    of the quantiser followed by the GEMM (the same codes, scales, MMAs and
+    promotion order), with the bias and a row pitch wider than K, and within the
+    GEMM tolerance of the oracle."""
+    x = si.activations(M, K, base_seed=M + K)
+    qw, sw = _weights(N, K)
+    bias = si.f32_to_bf16_bits(np.linspace(-2, 2, N).astype(np.float32))
+    wide = torch.zeros(M, K + 64, dtype=torch.bfloat16, device="cuda")
+    wide[:, :K] = dev(x)
+    xd = wide[:, :K]
+    y = Guarded((M, N), torch.bfloat16, fill=float("nan"))
+    g_ws = Guarded((fb.fp8bq_workspace_bytes(fb.OP_LINEAR, M, N, K),), torch.uint8)
+    fb.fp8bq_workspace_init(g_ws.t)
+    fb.fp8bq_linear(xd, dev(qw), dev(sw), y.t, g_ws.t, bias=dev(bias))
+    assert fb.fp8bq_poll_status(g_ws.t) == 0
+    y.check("fused linear y")
+    g_ws.check("fused linear workspace")
+    q = torch.empty(M, K, dtype=torch.uint8, device="cuda")
+    s = torch.empty(M, -(-K // 128), dtype=torch.float32, device="cuda")
+    fb.fp8bq_quant_act(xd, q, s)
+    y2 = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    ws2 = fb.new_workspace(fb.OP_GEMM, M, N, K)
+    fb.fp8bq_gemm(q, s, dev(qw), dev(sw), y2, ws2, bias=dev(bias))
+    assert fb.fp8bq_poll_status(ws2) == 0
+    assert torch.equal(y.t.view(torch.int16), y2.view(torch.int16))
+    qa, sa = oracle.quant_group(x)
+    rows, cols = sample_indices(M, N, per_block=16)
+    check_close(host(y.t)[rows, cols],
+                oracle.gemm_block_sampled(qa, sa, qw, sw, rows, cols, bias=bias),
+                f"fused linear {M}x{N}x{K}")
