@@ -33,6 +33,7 @@ __all__ = [
     "fp8bq_version", "fp8bq_status_string", "fp8bq_last_cuda_error",
     "fp8bq_workspace_bytes", "fp8bq_workspace_init", "fp8bq_poll_status",
     "fp8bq_quant_act", "fp8bq_gemm", "fp8bq_linear", "fp8bq_gemm_noalloc",
+    "fp8bq_noalloc_poll_status",
     "NOALLOC_SCRATCH_BYTES", "fp8bq_mx_quant_act",
     "fp8bq_mx_gemm", "fp8bq_mx_linear", "fp8bq_static_quant_act", "fp8bq_static_gemm",
     "fp8bq_add_rmsnorm_quant_act", "fp8bq_add_rmsnorm_static_quant_act",
@@ -84,6 +85,7 @@ def _load():
         "fp8bq_gemm": (I32, [P, P, I32, P, P, P, P, I64, I64, I64, P, SZ, P]),
         "fp8bq_linear": (I32, [P, I64, P, P, P, P, I64, I64, I64, P, SZ, P]),
         "fp8bq_gemm_noalloc": (I32, [P, P, I32, P, P, P, P, I64, I64, I64, P]),
+        "fp8bq_noalloc_poll_status": (I32, [P]),
         "fp8bq_mx_quant_act": (I32, [P, I64, I64, I64, P, P, P]),
         "fp8bq_mx_gemm": (I32, [P, P, P, P, P, P, I64, I64, I64, P, SZ, P]),
         "fp8bq_mx_linear": (I32, [P, I64, P, P, P, P, I64, I64, I64, P, SZ, P]),
@@ -354,6 +356,12 @@ def _linear_specs(x, w, y, bias):
         _Spec("w", w, _E4M3, (N, K)),
         _Spec("y", y, _BF16, (M, N)),
         _bias(bias, N)]
+
+
+def fp8bq_noalloc_poll_status(stream=None) -> int:
+    """Synchronises the stream; 0, or 8 (FP8BQ_ERR_TIMEOUT) if a wait of an
+    fp8bq_gemm_noalloc call on this device ran out."""
+    return _lib.fp8bq_noalloc_poll_status(_stream(stream))
 
 
 def fp8bq_linear(x, w, s_w, y, ws, bias=None, stream=None):

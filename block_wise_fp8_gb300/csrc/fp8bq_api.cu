@@ -723,6 +723,19 @@ int fp8bq_gemm_noalloc(const void *q, const float *s_x, int s_layout, const void
 }
 
 
+// The status word of the scratch array on the current device: read after the
+// stream's work has finished, then cleared (like fp8bq_poll_status).
+int fp8bq_noalloc_poll_status(void *stream) {
+  DeviceInfo dev;
+  RETURN_IF(device_info(&dev));
+  int d = 0;
+  cudaError_t e = cudaGetDevice(&d);
+  if (e != cudaSuccess) return cuda_fail(e);
+  void *scratch = nullptr;
+  RETURN_IF(noalloc_scratch(d, &scratch));
+  return fp8bq_poll_status(scratch, stream);
+}
+
 // ------------------------------------------------------------------ channelwise path
 
 int fp8bq_channel_quant_act(const void *x, int64_t M, int64_t K, int64_t ldx, void *q, float *s,

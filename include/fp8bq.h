@@ -107,7 +107,10 @@ enum {
   FP8BQ_OP_GROUPED_GEMM = 10 /* both grouped forms; M = rows of A and Y in all */
 };
 
-/* ---------------------------------------------------------------- utility */
+/* ---------------------------------------------------------------- utility
+ * Library plumbing with no counterpart on the pages (there, the framework
+ * owns memory and streams): version, status strings, workspace sizing and
+ * the status word that the bounded device waits report through. */
 
 /* Library version, major*10000 + minor*100 + patch. */
 FP8BQ_API int fp8bq_version(void);
@@ -130,21 +133,41 @@ FP8BQ_API int fp8bq_poll_status(void *ws, void *stream);
 
 /* ------------------------------------------------ block path (group/block 128) */
 
-/* Per-token group-128 activation quantisation (per_token_group_quant_fp8).
+/* Per-token group-128 activation quantisation (per_token_group_quant_fp8):
+ * "GLM-5.3 推理全链路(十七)", §第1站 (s_g = max|x| / 448 per group of 128
+ * channels, q = round(x / s_g)) and "SGLang 源码完全拆解(十九)", §从浮点到 FP8
+ * 的基本公式 (clamp to +-448, round to nearest even).
  * x: BF16 [M, K] pitch ldx.  q: E4M3 [M, K].  s: FP32 scales in `s_layout`.
  * Bit-exact rule: amax = max|x| over the group (floored at 1e-10),
- * s = amax / 448 and q = RNE_sat(x / s), both IEEE binary32 divisions. */
+ * s = amax / 448 and q = RNE_sat(x / s), both IEEE binary32 divisions.
+ * Errors: ERR_NULL (q or s NULL), ERR_SHAPE, ERR_ALIGN (x, q not 16-byte
+ * aligned, ldx % 8, K % 16), ERR_UNSUPPORTED (layout value). */
 FP8BQ_API int fp8bq_quant_act(const void *x, int64_t M, int64_t K, int64_t ldx,
                               void *q, float *s, int s_layout, void *stream);
 
 /* Block-scaled FP8 GEMM: y = BF16(sum_b P_b * s_x[:, b] * s_w[n/128, b] + bias),
- * P_b the FP32 tensor-core sum over K block b. */
+ * P_b the FP32 tensor-core sum over K block b -- "SGLang 源码完全拆解(十九)",
+ * §一条 GEMM 的三种缩放组合 (the block-wise equation) and §Triton 分块内核在
+ * 做什么 (one scale read per K block and tile, dequantisation in the
+ * epilogue); "GLM-5.3 推理全链路(十七)", §先把 GLM-5.3 的数值常量摆出来 (FP32
+ * promotion of every 128-wide K slice, the DeepSeek-V3 Fig. 7 scheme).
+ * q: E4M3 [M, K]; s_x in `s_layout`; w: E4M3 [N, K]; s_w: FP32
+ * [ceil(N/128)][ceil(K/128)]; bias: BF16 [N] or NULL; y: BF16 [M, N].
+ * Errors: ERR_NULL, ERR_SHAPE, ERR_ALIGN, ERR_UNSUPPORTED (layout value, or
+ * K > 65536 when M <= 64), ERR_WORKSPACE, ERR_CUDA; a
+ * timed-out device wait is reported later by fp8bq_poll_status. */
 FP8BQ_API int fp8bq_gemm(const void *q, const float *s_x, int s_layout,
                          const void *w, const float *s_w, const void *bias,
                          void *y, int64_t M, int64_t N, int64_t K, void *ws,
                          size_t ws_bytes, void *stream);
 
-/* Fused linear: fp8bq_quant_act into the workspace, then fp8bq_gemm. */
+/* Fused linear, BF16 in and BF16 out ("SGLang 源码完全拆解(十九)", §一次前向的
+ * 完整时序: quantise the activations, block-scaled GEMM, bias, output dtype):
+ * the result of fp8bq_quant_act (row-major scales) followed by fp8bq_gemm,
+ * bit for bit.  Up to 16 tokens it is one launch: the GEMM quantises the
+ * activations of each K block itself as they arrive; above, the quantiser
+ * writes codes and scales into the workspace first.  Arguments and errors as
+ * fp8bq_quant_act and fp8bq_gemm; workspace fp8bq_workspace_bytes(FP8BQ_OP_LINEAR, ...). */
 FP8BQ_API int fp8bq_linear(const void *x, int64_t ldx, const void *w,
                            const float *s_w, const void *bias, void *y,
                            int64_t M, int64_t N, int64_t K, void *ws,
@@ -183,31 +206,46 @@ FP8BQ_API int fp8bq_linear(const void *x, int64_t ldx, const void *w,
  *    array, which keeps what the last call left there: calls that may overlap
  *    on the GPU (different streams without ordering between them) race on it
  *    and give undefined results.  Calls on one stream are ordered and safe.
- *  - A device-side wait that runs out leaves the outputs undefined and is not
- *    reported to the host (there is no workspace to poll); the next call
- *    clears the status word. */
+ *  - A device-side wait that runs out leaves the outputs undefined and sets
+ *    the array's status word; fp8bq_noalloc_poll_status reports it (the next
+ *    call clears it in any case). */
 FP8BQ_API int fp8bq_gemm_noalloc(const void *q, const float *s_x, int s_layout,
                                  const void *w, const float *s_w,
                                  const void *bias, void *y, int64_t M,
                                  int64_t N, int64_t K, void *stream);
 
+/* The status of the fp8bq_gemm_noalloc calls on the current device: synchronises
+ * `stream`, then returns and clears the scratch array's status word -- FP8BQ_OK,
+ * or FP8BQ_ERR_TIMEOUT if a bounded device wait of one of those calls ran out
+ * (its output is then undefined).  No counterpart on the pages; it allocates
+ * nothing.  Like fp8bq_gemm_noalloc, the first call on a device looks up the
+ * array's address. */
+FP8BQ_API int fp8bq_noalloc_poll_status(void *stream);
+
 /* ------------------------------------------------ MXFP8 path ([1,32], UE8M0) */
 
-/* MXFP8 activation quantisation: per 32-channel group, e = ceil(log2(max(amax,
- * 1e-10) / 448)) (binary32 division), s = e + 127 (UE8M0), q = RNE_sat(x * 2^-e).
- * s: uint8 [M][K/32].  Also quantises weights (rows = N). */
+/* MXFP8 activation quantisation ("SGLang 源码完全拆解(十九)", §checkpoint 里的
+ * 量化元数据 and "[SGLang] FP8" §1: blocks of [1, 32]; "GLM-5.3 推理全链路(十七)",
+ * §第4站: the E8M0 exponent rounded up, amax floored at 1e-10): per 32-channel
+ * group, e = ceil(log2(max(amax, 1e-10) / 448)) (binary32 division),
+ * s = e + 127 (UE8M0), q = RNE_sat(x * 2^-e).  s: uint8 [M][K/32].  Also
+ * quantises weights (rows = N).  K % 32 == 0 (ERR_ALIGN otherwise). */
 FP8BQ_API int fp8bq_mx_quant_act(const void *x, int64_t M, int64_t K,
                                  int64_t ldx, void *q, uint8_t *s,
                                  void *stream);
 
-/* MXFP8 GEMM on the tensor cores' block-scaled MMA: s_x uint8 [M][K/32],
- * s_w uint8 [N][K/32]; y = BF16(sum_g P_g * 2^(s_x-127) * 2^(s_w-127) + bias). */
+/* MXFP8 GEMM on the tensor cores' block-scaled MMA ("GLM-5.3 推理全链路(十七)",
+ * §第7站: the UE8M0 scales are consumed by the MMA itself): s_x uint8
+ * [M][K/32], s_w uint8 [N][K/32]; y = BF16(sum_g P_g * 2^(s_x-127) *
+ * 2^(s_w-127) + bias).  Workspace fp8bq_workspace_bytes(FP8BQ_OP_MX_GEMM, ...)
+ * (it holds the scale codes rearranged for the MMA).  Errors as fp8bq_gemm. */
 FP8BQ_API int fp8bq_mx_gemm(const void *q, const uint8_t *s_x, const void *w,
                             const uint8_t *s_w, const void *bias, void *y,
                             int64_t M, int64_t N, int64_t K, void *ws,
                             size_t ws_bytes, void *stream);
 
-/* Fused MXFP8 linear: fp8bq_mx_quant_act into the workspace, then fp8bq_mx_gemm. */
+/* Fused MXFP8 linear (the same page sequence as fp8bq_linear with the MXFP8
+ * formats): fp8bq_mx_quant_act into the workspace, then fp8bq_mx_gemm. */
 FP8BQ_API int fp8bq_mx_linear(const void *x, int64_t ldx, const void *w,
                               const uint8_t *s_w, const void *bias, void *y,
                               int64_t M, int64_t N, int64_t K, void *ws,
@@ -249,15 +287,20 @@ FP8BQ_API int fp8bq_add_rmsnorm_static_quant_act(const void *x, int64_t ldx,
 
 /* ------------------------------------------------ static per-tensor path */
 
-/* Static quantisation with one device-resident FP32 scale s_x[0]:
- * q = RNE_sat(x / s_x), binary32 division. */
+/* Static per-tensor quantisation ("SGLang 源码完全拆解(十九)", §激活量化的三种选择:
+ * one calibrated scale for the whole tensor; "[SGLang] FP8" §5) with one
+ * device-resident FP32 scale s_x[0]: q = RNE_sat(x / s_x), binary32 division;
+ * values beyond 448 s_x saturate.  Errors: ERR_NULL, ERR_SHAPE, ERR_ALIGN. */
 FP8BQ_API int fp8bq_static_quant_act(const void *x, int64_t M, int64_t K,
                                      int64_t ldx, const float *s_x, void *q,
                                      void *stream);
 
-/* Per-tensor FP8 GEMM: y = BF16((sum_k q w) * s_x[0] * s_w_part[p(j)] + bias),
- * p(j) the output partition of row j.  part_sizes_host[n_parts] (host memory,
- * 1 <= n_parts <= 64) must sum to N; s_w_part is a device FP32 [n_parts]. */
+/* Per-tensor FP8 GEMM ("SGLang 源码完全拆解(十九)", §一条 GEMM 的三种缩放组合: the
+ * per-tensor scales come out of the sum; "[SGLang] FP8" §5: one weight scale
+ * per output partition of a fused weight): y = BF16((sum_k q w) * s_x[0] *
+ * s_w_part[p(j)] + bias), p(j) the output partition of row j.
+ * part_sizes_host[n_parts] (host memory, 1 <= n_parts <= 64) must sum to N
+ * (ERR_SHAPE otherwise); s_w_part is a device FP32 [n_parts]. */
 FP8BQ_API int fp8bq_static_gemm(const void *q, const float *s_x, const void *w,
                                 const float *s_w_part,
                                 const int64_t *part_sizes_host, int n_parts,
@@ -265,7 +308,9 @@ FP8BQ_API int fp8bq_static_gemm(const void *q, const float *s_x, const void *w,
                                 int64_t K, void *ws, size_t ws_bytes,
                                 void *stream);
 
-/* Fused static linear: fp8bq_static_quant_act into the workspace, then fp8bq_static_gemm. */
+/* Fused static linear ("GLM-5.3 推理全链路(十七)", §第1站: the static per-tensor
+ * path multiplies by the fixed FP8 scale): fp8bq_static_quant_act into the
+ * workspace, then fp8bq_static_gemm. */
 FP8BQ_API int fp8bq_static_linear(const void *x, int64_t ldx, const float *s_x,
                                   const void *w, const float *s_w_part,
                                   const int64_t *part_sizes_host, int n_parts,
