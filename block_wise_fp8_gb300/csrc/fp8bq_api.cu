@@ -706,16 +706,16 @@ int fp8bq_gemm_noalloc(const void *q, const float *s_x, int s_layout, const void
   RETURN_IF(noalloc_scratch(d, &scratch));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // The status word, the tile counters and the decode tiles' partial slots
-  // (split 1 on) must start at zero; a previous call whose bounded wait ran
-  // out may have left them set.
+  // must start at zero; a previous call whose bounded wait ran out may have
+  // left them set.
   e = cudaMemsetAsync(scratch, 0, L.partials, st);
   if (e != cudaSuccess) return cuda_fail(e);
   int kps = 0;
   const int splits = M <= 64 ? decode_splits(N, K, dev.num_sms, &kps) : 1;
   if (splits > 1) {
-    const size_t slot = static_cast<size_t>(M) * static_cast<size_t>(N) * 4;
-    e = cudaMemsetAsync(static_cast<uint8_t *>(scratch) + L.partials + slot, 0,
-                        static_cast<size_t>(splits - 1) * slot, st);
+    const size_t slot = static_cast<size_t>((M + 3) / 4 * 4) * static_cast<size_t>(N) * 4;
+    e = cudaMemsetAsync(static_cast<uint8_t *>(scratch) + L.partials, 0,
+                        static_cast<size_t>(splits) * slot, st);
     if (e != cudaSuccess) return cuda_fail(e);
   }
   return gemm_block_impl(q, s_x, s_layout, w, s_w, bias, y, M, N, K, scratch, FP8BQ_OP_GEMM, st,

@@ -248,7 +248,9 @@ WorkspaceLayout workspace_layout(int op, int64_t M, int64_t N, int64_t K, bool t
   const bool grouped = (op == 10);  // pair tiles at every M: no split-K partials
   const bool block = (op == 0 || op == 1);
   if (M <= 64 && !mx && !grouped) {
-    off += up(static_cast<size_t>(kMaxSplits) * M * N * 4);
+    // decode split-K partials, one FP32 slot per split, token and weight row
+    // (room for the token count rounded up to 4)
+    off += up(static_cast<size_t>(kMaxSplits) * ((M + 3) / 4 * 4) * N * 4);
   } else if (block && tail) {
     // split tail tiles: at most 4 K ranges per pair tile (256 rows by at least
     // 192 weight rows, the narrowest pair tile), and kMaxTailItems

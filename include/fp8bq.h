@@ -192,9 +192,9 @@ FP8BQ_API int fp8bq_linear(const void *x, int64_t ldx, const void *w,
  *    than FP8BQ_NOALLOC_SCRATCH_BYTES are rejected with FP8BQ_ERR_WORKSPACE
  *    before anything is launched.  For M > 64 that is a status word and one
  *    counter per 128 output columns (at least 160), so every N up to about
- *    5 * 10^8 fits; for M <= 64 it adds FP32 split-K partials (32 * M * N
- *    bytes), so M * N must stay below about 524,000: every M <= 64 at
- *    N = 6144, M <= 16 at N = 24576.  Without the partials, the last wave's
+ *    5 * 10^8 fits; for M <= 64 it adds FP32 split-K partials (32 *
+ *    round_up(M, 4) * N bytes), so round_up(M, 4) * N must stay below about
+ *    524,000: every M <= 64 at N = 6144, M <= 16 at N = 24576.  Without the partials, the last wave's
  *    tiles run whole: results agree with fp8bq_gemm's within the GEMM
  *    tolerance, not bit for bit.
  *  - Set-up: the first call on a device, with that device current, looks up
