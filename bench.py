@@ -66,8 +66,8 @@ ORACLE_ROWS = 8      # token rows of a large output that the CPU baseline recomp
 # digest is recorded; anything else reports null.
 NCU_TRAFFIC = {
     # profiles/block_gemm_prefill_4096x24576x6144.md (N = 24576 launch)
-    "source_sha256": "f563fb4d3ff93d95ce8bc40722abd36acee0104de5653dd5258ee7d6774f8309",
-    "bytes_per_launch": 188697856 + 184808960,
+    "source_sha256": "bfcb2cb2dfae42890cf3f56ae0fa52d38e9c3aa7844af138669b2c9df496ca05",
+    "bytes_per_launch": 188278016 + 183880448,
 }
 
 
