@@ -6,9 +6,10 @@ The failure is made on purpose in a child process: FP8BQ_FAULT_INJECT makes CTA
 0 of the next few GEMM launches skip the copy of its first K block, so the MMA
 issuer's wait on that stage (and every wait behind it) runs out after
 FP8BQ_WAIT_LIMIT_MS = 50 ms.  Each kernel form is hit once -- split-K decode
-tiles, 2-CTA prefill tiles (with split tail tiles), per-tensor pair tiles,
-MXFP8 tiles, grouped single-CTA and pair tiles -- and each must report
-FP8BQ_ERR_TIMEOUT.  After that the same process must still be able to
+tiles (16 and 64 tokens), the one-launch decode linear (its quantiser warps
+wait on the stage too), 2-CTA prefill tiles (with split tail tiles),
+per-tensor pair tiles, MXFP8 tiles, grouped single-CTA and pair tiles -- and
+each must report FP8BQ_ERR_TIMEOUT.  After that the same process must still be able to
 use the GPU: the next GEMMs, on freshly zeroed workspaces, match the oracle."""
 import json
 import os
@@ -61,6 +62,15 @@ def mx(M, N, K):
     fb.fp8bq_mx_gemm(q, ux, w, uw, y, ws)
     return fb.fp8bq_poll_status(ws)
 
+def linear(M, N, K):
+    x = torch.randn(M, K, device="cuda").to(torch.bfloat16)
+    w = codes(N, K)
+    sw = torch.rand(-(-N // 128), K // 128, device="cuda") + 0.5
+    y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    ws = fb.new_workspace(fb.OP_LINEAR, M, N, K)
+    fb.fp8bq_linear(x, w, sw, y, ws)
+    return fb.fp8bq_poll_status(ws)
+
 def grouped(N, K, counts):
     E, T = len(counts), sum(counts)
     q, w = codes(T, K), codes(E * N, K).view(E, N, K)
@@ -72,8 +82,10 @@ def grouped(N, K, counts):
     fb.fp8bq_grouped_gemm(q, sx, w, sw, off, y, ws)
     return fb.fp8bq_poll_status(ws)
 
-# six injected launches, one per kernel form
+# eight injected launches, one per kernel form
 res["decode_block"] = block(8, 1024, 2048)
+res["decode_block_64"] = block(64, 1024, 2048)
+res["decode_linear_fused"] = linear(4, 1024, 2048)
 res["prefill_block_pair"] = block(512, 768, 2048)
 res["static_pair"] = static(512, 1024, 1024)
 res["mx"] = mx(256, 512, 1024)
@@ -97,7 +109,7 @@ print("RESULT " + json.dumps(res))
 
 def test_bounded_waits_report_timeout_and_leave_the_context_usable():
     env = dict(os.environ)
-    env["FP8BQ_FAULT_INJECT"] = "skip_first_load:6"
+    env["FP8BQ_FAULT_INJECT"] = "skip_first_load:8"
     env["FP8BQ_WAIT_LIMIT_MS"] = "50"
     env["PYTHONPATH"] = os.pathsep.join([ROOT, os.path.join(ROOT, "tests"),
                                          env.get("PYTHONPATH", "")])
@@ -107,7 +119,7 @@ def test_bounded_waits_report_timeout_and_leave_the_context_usable():
     line = [l for l in p.stdout.splitlines() if l.startswith("RESULT ")][-1]
     res = json.loads(line[len("RESULT "):])
     timeout = 8  # FP8BQ_ERR_TIMEOUT
-    for k in ("decode_block", "prefill_block_pair", "static_pair", "mx", "grouped_normal",
-              "grouped_pair"):
+    for k in ("decode_block", "decode_block_64", "decode_linear_fused", "prefill_block_pair",
+              "static_pair", "mx", "grouped_normal", "grouped_pair"):
         assert res[k] == timeout, res
     assert res["after_8x1024x2048"] == 0 and res["after_300x704x1040"] == 0, res
