@@ -49,7 +49,8 @@ NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024      # FP8BQ_NOALLOC_SCRATCH_BYTES
 
 STATUS_NAMES = {0: "FP8BQ_OK", 1: "FP8BQ_ERR_NULL", 2: "FP8BQ_ERR_SHAPE",
                 3: "FP8BQ_ERR_ALIGN", 4: "FP8BQ_ERR_UNSUPPORTED", 5: "FP8BQ_ERR_ARCH",
-                6: "FP8BQ_ERR_WORKSPACE", 7: "FP8BQ_ERR_CUDA", 8: "FP8BQ_ERR_TIMEOUT"}
+                6: "FP8BQ_ERR_WORKSPACE", 7: "FP8BQ_ERR_CUDA", 8: "FP8BQ_ERR_TIMEOUT",
+                9: "FP8BQ_ERR_BOUNDS"}
 
 
 class Fp8bqError(RuntimeError):
@@ -62,16 +63,21 @@ class Fp8bqError(RuntimeError):
         super().__init__(msg)
 
 
+# FP8BQ_LIBRARY selects another build of the same library, e.g. the debug
+# build with device-side bounds checks (_build.build(debug=True))
+_LIB_PATH = os.environ.get("FP8BQ_LIBRARY") or _build.LIB
+
+
 def library_path() -> str:
-    return _build.LIB
+    return _LIB_PATH
 
 
 def _load():
-    if not os.path.exists(_build.LIB):
+    if not os.path.exists(_LIB_PATH):
         raise ImportError(
-            f"CUDA library {_build.LIB} is not built; run __graft_entry__.build() "
+            f"CUDA library {_LIB_PATH} is not built; run __graft_entry__.build() "
             "(there is no CPU fallback)")
-    lib = ctypes.CDLL(_build.LIB)
+    lib = ctypes.CDLL(_LIB_PATH)
     P, I64, I32, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
     F32 = ctypes.c_float
     sigs = {
@@ -288,7 +294,8 @@ def fp8bq_workspace_init(ws, stream=None):
 
 
 def fp8bq_poll_status(ws, stream=None) -> int:
-    """Synchronises the stream; returns 0, or 8 (FP8BQ_ERR_TIMEOUT)."""
+    """Synchronises the stream; returns 0, 8 (FP8BQ_ERR_TIMEOUT) or, from a
+    debug build, 9 (FP8BQ_ERR_BOUNDS)."""
     _validate("fp8bq_poll_status", [_ws(ws)], stream)
     return _lib.fp8bq_poll_status(_ptr(ws), _stream(stream))
 

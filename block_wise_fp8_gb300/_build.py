@@ -14,6 +14,10 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 OUT = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT, "libfp8bq.so")
+# the debug build: the same sources with FP8BQ_DEBUG_CHECKS (device-side bounds
+# checks on the GEMM epilogues' writes, reported as FP8BQ_ERR_BOUNDS)
+OUT_DEBUG = os.path.join(PKG, "_build_debug")
+LIB_DEBUG = os.path.join(OUT_DEBUG, "libfp8bq.so")
 INCLUDE = os.path.join(os.path.dirname(PKG), "include")
 
 SOURCES = ["fp8bq_api.cu", "quant.cu", "gemm_launch.cu", "gemm_block.cu",
@@ -38,24 +42,26 @@ def _deps() -> list[str]:
     return files
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(f) <= t for f in _deps())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(OUT, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, debug: bool = False) -> str:
+    out, lib = (OUT_DEBUG, LIB_DEBUG) if debug else (OUT, LIB)
+    if not force and up_to_date(lib):
+        return lib
+    os.makedirs(out, exist_ok=True)
     nvcc = _nvcc()
     procs = []
     objs = []
+    extra = ["-DFP8BQ_DEBUG_CHECKS"] if debug else []
     for src in SOURCES:
-        obj = os.path.join(OUT, src.replace(".cu", ".o"))
+        obj = os.path.join(out, src.replace(".cu", ".o"))
         objs.append(obj)
-        cmd = [nvcc, *NVCC_FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+        cmd = [nvcc, *NVCC_FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
         procs.append((src, subprocess.Popen(cmd, stdout=subprocess.PIPE,
@@ -69,13 +75,14 @@ def build(force: bool = False, verbose: bool = False) -> str:
             failed.append(src)
     if failed:
         raise RuntimeError(f"nvcc failed for {failed}")
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     link = [nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-lpthread", "-ldl", "-lrt"]
     subprocess.run(link, check=True)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
     import sys
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv,
+                debug="--debug" in sys.argv))

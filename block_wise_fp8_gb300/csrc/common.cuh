@@ -21,6 +21,7 @@ constexpr int kGroupTableBytes = (3 * kMaxExperts + 1) * 4;
 
 // Status values stored in the workspace status word (same numbers as fp8bq_status).
 constexpr uint32_t kStatusTimeout = 8;
+constexpr uint32_t kStatusBounds = 9;  // a debug build's bounds check caught a write
 
 // Every kernel of the library is launched with programmatic stream
 // serialization: it may start while the preceding kernel of the stream is

@@ -316,6 +316,7 @@ const char *fp8bq_status_string(int s) {
     case FP8BQ_ERR_WORKSPACE: return "workspace missing or too small";
     case FP8BQ_ERR_CUDA: return "CUDA runtime error";
     case FP8BQ_ERR_TIMEOUT: return "a device-side wait timed out";
+    case FP8BQ_ERR_BOUNDS: return "a device-side bounds check skipped a write (debug build)";
     default: return "unknown status";
   }
 }
@@ -346,7 +347,7 @@ int fp8bq_poll_status(void *ws, void *stream) {
   if (word != 0) {
     e = cudaMemset(ws, 0, sizeof word);
     if (e != cudaSuccess) return cuda_fail(e);
-    return FP8BQ_ERR_TIMEOUT;
+    return word == kStatusBounds ? FP8BQ_ERR_BOUNDS : FP8BQ_ERR_TIMEOUT;
   }
   return FP8BQ_OK;
 }

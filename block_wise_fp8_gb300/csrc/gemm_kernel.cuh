@@ -240,6 +240,22 @@ __device__ __forceinline__ void record_timeout(const GemmArgs &a) {
   if (a.status) atomicExch(a.status, kStatusTimeout);
 }
 
+// Debug builds (FP8BQ_DEBUG_CHECKS defined): every global write of the
+// epilogues is checked against the buffer it belongs to (Y rows and columns,
+// the workspace's partial region); a write outside is skipped and recorded as
+// FP8BQ_ERR_BOUNDS in the workspace status word.  Release builds compile the
+// checks away.
+#ifdef FP8BQ_DEBUG_CHECKS
+constexpr bool kDebugChecks = true;
+#else
+constexpr bool kDebugChecks = false;
+#endif
+__device__ __forceinline__ bool write_ok(const GemmArgs &a, bool in_bounds) {
+  if (!kDebugChecks || in_bounds) return true;
+  if (a.status) atomicExch(a.status, kStatusBounds);
+  return false;
+}
+
 // every lane waits; the warp proceeds only if all lanes saw the phase complete
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile uint32_t *ab,
                                           uint64_t limit) {
@@ -879,7 +895,10 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
             float *mine = args.partials + (static_cast<int64_t>(w.tile) * shape.tail_splits + w.split) * 2 * blk +
                           rank * blk;
 #pragma unroll
-            for (int j = 0; j < C::kCPT; ++j) __stcg(mine + (col0 + j) * 128 + row, acc[j]);
+            for (int j = 0; j < C::kCPT; ++j)
+              if (write_ok(args, (mine - args.partials) + (col0 + j) * 128 + row <
+                                     args.partials_bytes / 4))
+                __stcg(mine + (col0 + j) * 128 + row, acc[j]);
             named_bar_sync(2, C::kEpiThreads);
             if (et == 0) {
               const uint32_t prev = atom_add_acq_rel_gpu(args.counters + 2 * w.tile + rank, 1u);
@@ -944,12 +963,13 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
               }
               fence_proxy_async_smem();
               __syncwarp();
-              if (lane == 0 && row0 < w.row_end && nbase + bx * C::kYBoxCols < args.N) {
+              if (lane == 0 && row0 < w.row_end && nbase + bx * C::kYBoxCols < args.N &&
+                  write_ok(args, row0 >= 0 && w.row_end <= args.M)) {
                 tma_store_2d(&tmY, stg, nbase + bx * C::kYBoxCols, row0);
                 bulk_commit_group();
               }
             }
-          } else if (m < w.row_end) {
+          } else if (m < w.row_end && write_ok(args, m >= 0 && m < args.M)) {
             store_row<C::kCPT>(y, acc, m, nbase, args);
           }
         } else {
@@ -1005,7 +1025,8 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
               }
               if (bias && n < args.N) v[j] += bf16_bits_to_float(bias[n]);
             }
-            if (m < w.row_end) store_row<C::kCW>(y, v, m, nbase + c * C::kCW, args);
+            if (m < w.row_end && write_ok(args, m >= 0 && m < args.M))
+              store_row<C::kCW>(y, v, m, nbase + c * C::kCW, args);
           }
         }
       } else {
@@ -1126,7 +1147,9 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
               uint32_t *dst = part + static_cast<int64_t>(w.split) * args.M * args.N + n;
 #pragma unroll
               for (int j = 0; j < C::kCPT; ++j)
-                if (j < args.M)
+                if (j < args.M &&
+                    write_ok(args, (dst - part) + static_cast<int64_t>(j) * args.N <
+                                       args.partials_bytes / 4))
                   st_relaxed_gpu(dst + static_cast<int64_t>(j) * args.N, __float_as_uint(acc[j]) + 1u);
             }
           } else if (n_ok) {

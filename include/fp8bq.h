@@ -87,7 +87,9 @@ typedef enum fp8bq_status {
   FP8BQ_ERR_ARCH = 5,        /* current device is not compute capability 10.3       */
   FP8BQ_ERR_WORKSPACE = 6,   /* workspace NULL or smaller than required             */
   FP8BQ_ERR_CUDA = 7,        /* a CUDA runtime call failed; see fp8bq_last_cuda_error */
-  FP8BQ_ERR_TIMEOUT = 8      /* a device wait gave up (reported by fp8bq_poll_status) */
+  FP8BQ_ERR_TIMEOUT = 8,     /* a device wait gave up (reported by fp8bq_poll_status) */
+  FP8BQ_ERR_BOUNDS = 9       /* debug builds only: a GEMM epilogue write fell outside its
+                                buffer and was skipped (reported by fp8bq_poll_status) */
 } fp8bq_status;
 
 enum { FP8BQ_SCALE_ROW_MAJOR = 0, FP8BQ_SCALE_COL_MAJOR = 1 };
@@ -128,7 +130,9 @@ FP8BQ_API size_t fp8bq_workspace_bytes(int op, int64_t M, int64_t N, int64_t K);
 FP8BQ_API int fp8bq_workspace_init(void *ws, size_t ws_bytes, void *stream);
 
 /* Synchronises `stream`, then returns and clears the workspace status word:
- * FP8BQ_OK, or FP8BQ_ERR_TIMEOUT if a kernel's bounded wait ran out. */
+ * FP8BQ_OK, or FP8BQ_ERR_TIMEOUT if a kernel's bounded wait ran out, or (a
+ * library built with FP8BQ_DEBUG_CHECKS) FP8BQ_ERR_BOUNDS if a GEMM's bounds
+ * check skipped a write. */
 FP8BQ_API int fp8bq_poll_status(void *ws, void *stream);
 
 /* ------------------------------------------------ block path (group/block 128) */

@@ -42,7 +42,7 @@ def test_only_declared_symbols_are_exported():
 
 def test_version_and_status_strings():
     assert fb.fp8bq_version() == 10000
-    for s in range(9):
+    for s in range(10):
         assert fb.fp8bq_status_string(s) != "unknown status"
     assert fb.fp8bq_status_string(99) == "unknown status"
     assert fb.fp8bq_last_cuda_error() == 0
