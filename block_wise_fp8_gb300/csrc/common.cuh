@@ -131,6 +131,9 @@ struct GemmArgs {
   // that the GEMM quantises itself; nullptr otherwise
   const void *xq;
   int64_t ldxq;
+  // decode tiles: token rows of the B operand each stage copies (set by the
+  // launcher: M rounded up to 8, at most the tile's width)
+  int b_box_rows;
 };
 
 struct DeviceInfo {

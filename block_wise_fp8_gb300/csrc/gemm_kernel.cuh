@@ -104,10 +104,13 @@ struct Cfg {
   // idle warp) hands registers to the epilogue warpgroups with setmaxnreg
   static constexpr bool kRegSplit = (MODE == kModeBlock) && !SWAP;
   static constexpr int kEpiBase = kRegSplit ? 4 : 1 + kIssuers;  // first epilogue warp
-  // fused decode linear (FUSEQ): four more warps quantise each stage's BF16
-  // activation slice into the stage's E4M3 operand
+  // fused decode linear (FUSEQ): more warps quantise each stage's BF16
+  // activation slice into the stage's E4M3 operand -- eight for the 16- and
+  // 32-token tiles, so that groups of them take the stages in turn
+  // (measured 11.3 -> 9.9 us at 1 x 6144 x 6144, 12.0 -> 11.3 us at 16
+  // tokens); four for the 64-token tile, whose registers would spill with eight
   static constexpr bool kFuseQ = FUSEQ;
-  static constexpr int kQWarps = FUSEQ ? 4 : 0;
+  static constexpr int kQWarps = FUSEQ ? (BN <= 32 ? 8 : 4) : 0;
   static constexpr int kQBase = kEpiBase + EPI_WARPS;          // first quantiser warp
   static constexpr int kThreads = 32 * (kEpiBase + EPI_WARPS + kQWarps);
   // register budget: warps are dealt round-robin to the SM's four schedulers,
@@ -146,7 +149,6 @@ struct Cfg {
   static constexpr int kBbytes = kBrows * 128 + kXbytes;
   static constexpr int kStageBytes = kAbytes + kBbytes;
   // bytes that land on a stage's full barrier
-  static constexpr int kTxBytes = FUSEQ ? kAbytes + kXbytes : kStageBytes;
   // block pair and normal tiles: promotion factors come through a shared-memory
   // ring filled by the TMA producer, kScQuad K blocks per slot: s_x of this
   // CTA's 128 rows and s_w of the tile's (at most two) 128-row weight blocks
@@ -393,6 +395,17 @@ __device__ __forceinline__ bool poll_partials(const uint32_t *src, int64_t strid
   }
 }
 
+// Fused decode linear: quantiser warps that quantise one stage -- the token
+// rows below M at eight threads each, rounded up to whole warps (at most
+// QWARPS; a power of two, so the warps split into QWARPS / it groups).
+template <int BN, int QWARPS>
+__device__ __forceinline__ int fused_quant_warps_per_stage(int M) {
+  const int need = (min(M, BN) * 8 + 31) / 32;
+  int w = 1;
+  while (w < need && w < QWARPS) w <<= 1;
+  return w;
+}
+
 // Store `n` (multiple of 8 unless ragged) BF16 values of row m starting at column c0.
 template <int CNT>
 __device__ __forceinline__ void store_row(uint16_t *y, const float *v, int m, int c0,
@@ -466,7 +479,8 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
       mbar_init(&bars->sc_full[s], 1);
       mbar_init(&bars->sc_empty[s], EPI_WARPS);
     }
-    for (int s = 0; s < (C::kFuseQ ? STAGES : 0); ++s) mbar_init(&bars->qfull[s], C::kQWarps);
+    for (int s = 0; s < (C::kFuseQ ? STAGES : 0); ++s)
+      mbar_init(&bars->qfull[s], fused_quant_warps_per_stage<BN, C::kQWarps>(args.M));
     mbar_init(&bars->drain, C::kIssuers);
     bars->abort = 0;
     bars->is_last = 0;
@@ -629,11 +643,15 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
             } else if (C::kFuseQ) {
               // the weight tile and the BF16 activations of K block kb (all
               // tokens; rows >= M and columns >= K read as zero)
-              mbar_arrive_expect_tx(&bars->full[s], C::kTxBytes);
+              mbar_arrive_expect_tx(&bars->full[s], kAbytes + args.b_box_rows * 256);
               tma_load_2d(sA + s * kAbytes, &tmA, &bars->full[s], kb * 128, w.a_row0);
               tma_load_2d(sB + s * C::kBbytes + C::kBrows * 128, &tmB, &bars->full[s], kb * 128, 0);
             } else {
-              mbar_arrive_expect_tx(&bars->full[s], C::kStageBytes + C::kSfStageBytes);
+              // decode tiles copy only the token rows in use (b_box_rows): the
+              // other rows of the operand only feed output columns past M
+              mbar_arrive_expect_tx(&bars->full[s],
+                                    (SWAP ? kAbytes + args.b_box_rows * 128 : C::kStageBytes) +
+                                        C::kSfStageBytes);
               tma_load_2d(sA + s * kAbytes, &tmA, &bars->full[s], kb * 128, w.a_row0);
               tma_load_2d(sB + s * C::kBbytes, &tmB, &bars->full[s], kb * 128, w.b_load_row0);
               if (MODE == kModeMx) {
@@ -1199,7 +1217,23 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
     // same bits), codes into the stage's E4M3 operand in the 128-byte swizzled
     // layout the MMA reads, scales into sx_stage for the promotion.  Eight
     // threads per token, 16 values each.
-    const int qt = threadIdx.x - 32 * C::kQBase;  // 0 .. 127
+    const int qt = threadIdx.x - 32 * C::kQBase;  // 0 .. 32 * kQWarps - 1
+    const int qw = qt >> 5;
+    // Token rows >= M only feed output columns that are never stored, so a
+    // stage needs only the tasks of rows below M, rounded up to whole warps
+    // (every lane of a warp that works runs the shuffles; only rows < M
+    // store).  The quantiser warps form groups of `wps` warps that take the
+    // stages in turn -- with four tokens or fewer and eight quantiser warps,
+    // each warp quantises every eighth stage.  The number of groups divides
+    // STAGES, so each group owns
+    // fixed stages and its previous wait on a stage was one ring ago: a
+    // barrier phase it waits for is never two phases away.
+    const int lim = min(BN * 8, (args.M * 8 + 31) / 32 * 32);
+    const int wps = fused_quant_warps_per_stage<BN, C::kQWarps>(args.M);  // warps per stage
+    int groups = C::kQWarps / wps;  // a power of two
+    while (STAGES % groups != 0) groups >>= 1;
+    const int grp = qw / wps;                // this warp's group
+    const int t0 = (qw % wps) * 32 + lane;   // first task of this thread in a stage
     ScaleTable &table = *reinterpret_cast<ScaleTable *>(sx_stage + shape.sx_stage);
     for (int m = qt; m <= 128; m += 32 * C::kQWarps) {
       const float a = m < 128 ? 1.0f + static_cast<float>(m) * 0.0078125f : kFloor;
@@ -1214,6 +1248,7 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
     for (int u = cl_id; ok && u < units; u += cl_num) {
       const Unit w = decode_unit<SWAP, PAIR, GROUPED>(u, num_a, shape.splits, shape.kps, KB, BN, rank, args.M, args.N, gt, shape);
       for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
+        if (grp >= groups || static_cast<int>(it & (groups - 1)) != grp) continue;
         const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
         if (!warp_wait(&bars->full[s], ph, abort_flag, limit)) {
           ok = false;
@@ -1221,12 +1256,7 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
         }
         uint8_t *codes = sB + s * C::kBbytes;
         const uint8_t *xs = codes + C::kBrows * 128;
-        // Token rows >= M only feed output columns that are never stored, so
-        // whole warps past them skip the work.  The bound is rounded up to
-        // whole warps: every lane of a warp that enters runs the shuffles
-        // (rows below BN, inside the stage), only rows < M store.
-        const int lim = min(BN * 8, (args.M * 8 + 31) / 32 * 32);
-        for (int task = qt; task < lim; task += 32 * C::kQWarps) {
+        for (int task = t0; task < lim; task += 32 * wps) {
           const int t = task >> 3, sub = task & 7;
           uint4 v[2];
           v[0] = *reinterpret_cast<const uint4 *>(xs + t * 256 + sub * 32);
@@ -1308,6 +1338,10 @@ cudaError_t run(const GemmArgs &a, const void *q_act, const void *w, const Launc
   std::memset(&tsx, 0, sizeof tsx);
   std::memset(&tsw, 0, sizeof tsw);
   GemmArgs args = a;
+  // decode tiles: B carries the tokens, and only the first M rows (rounded up
+  // to the 8-row swizzle atom) are copied
+  args.b_box_rows = SWAP ? ((a.M + 7) / 8 * 8 < C::kBrows ? (a.M + 7) / 8 * 8 : C::kBrows)
+                         : C::kBrows;
   args.y_tma = 0;
   args.sc_tma = 0;
   auto al16 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
@@ -1350,8 +1384,8 @@ cudaError_t run(const GemmArgs &a, const void *q_act, const void *w, const Launc
   // fused quantisation: B is the BF16 activation matrix [M, K] (pitch ldxq),
   // loaded unswizzled in [kBrows tokens x 128 values] boxes
   const bool b_ok = FUSEQ ? (a.xq != nullptr && al16(a.xq) &&
-                             cached_bf16_pitched_map(&tb, a.xq, a.M, a.K, a.ldxq, 128, C::kBrows))
-                          : cached_kmajor_map(&tb, b_ptr, b_rows, a.K, C::kBrows);
+                             cached_bf16_pitched_map(&tb, a.xq, a.M, a.K, a.ldxq, 128, args.b_box_rows))
+                          : cached_kmajor_map(&tb, b_ptr, b_rows, a.K, args.b_box_rows);
   if (!cached_kmajor_map(&ta, a_ptr, a_rows, a.K, kBM) || !b_ok) {
     *status = 4;  // FP8BQ_ERR_UNSUPPORTED: tensor map rejected
     return cudaSuccess;
