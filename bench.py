@@ -66,8 +66,8 @@ ORACLE_ROWS = 8      # token rows of a large output that the CPU baseline recomp
 # digest is recorded; anything else reports null.
 NCU_TRAFFIC = {
     # profiles/block_gemm_prefill_4096x24576x6144.md (N = 24576 launch)
-    "source_sha256": "bfcb2cb2dfae42890cf3f56ae0fa52d38e9c3aa7844af138669b2c9df496ca05",
-    "bytes_per_launch": 188278016 + 183880448,
+    "source_sha256": "cbfb5ef6b15f900a5f2bc84e0dbc86254fe758f1909e6d72bd421e9757a1e46f",
+    "bytes_per_launch": 188326912 + 183659520,
 }
 
 

@@ -201,14 +201,17 @@ def test_empty_batch():
     torch.cuda.synchronize()
 
 
-@pytest.mark.parametrize("M,N,K", [(1, 6144, 6144), (5, 200, 208), (16, 384, 256), (17, 640, 1040),
-                                   (33, 1000, 2048), (64, 6144, 6144), (8, 24576, 6144)])
+@pytest.mark.parametrize("M,N,K", [(1, 6144, 6144), (4, 1024, 6144), (5, 200, 208), (9, 384, 4000),
+                                   (16, 384, 256), (17, 640, 1040), (33, 1000, 2048), (64, 6144, 6144),
+                                   (8, 24576, 6144)])
 def test_decode_linear_fuses_quantisation_bit_exactly(M, N, K):
-    """Up to 64 tokens fp8bq_linear is one launch: the GEMM's CTAs quantise their
-    own K range of X as the stages arrive.  Its output must be bit for bit that
-    of the quantiser followed by the GEMM (the same codes, scales, MMAs and
-    promotion order), with the bias and a row pitch wider than K, and within the
-    GEMM tolerance of the oracle."""
+    """Up to 16 tokens fp8bq_linear is one launch: the GEMM's CTAs quantise their
+    own K range of X as the stages arrive, the quantiser warps in groups that
+    take the stages in turn (one warp per stage up to 4 tokens, two up to 8,
+    four up to 16).  Its output must be bit for bit that of the quantiser
+    followed by the GEMM (the same codes, scales, MMAs and promotion order),
+    with the bias and a row pitch wider than K, and within the GEMM tolerance
+    of the oracle.  Above 16 tokens the linear is the two launches themselves."""
     x = si.activations(M, K, base_seed=M + K)
     qw, sw = _weights(N, K)
     bias = si.f32_to_bf16_bits(np.linspace(-2, 2, N).astype(np.float32))
