@@ -66,7 +66,7 @@ ORACLE_ROWS = 8      # token rows of a large output that the CPU baseline recomp
 # digest is recorded; anything else reports null.
 NCU_TRAFFIC = {
     # profiles/block_gemm_prefill_4096x24576x6144.md (N = 24576 launch)
-    "source_sha256": "cbfb5ef6b15f900a5f2bc84e0dbc86254fe758f1909e6d72bd421e9757a1e46f",
+    "source_sha256": "37f0c1fa633f86ff42a27a2fdfd367a646d88ad655bb1c230aa788dedd8c213d",
     "bytes_per_launch": 188326912 + 183659520,
 }
 

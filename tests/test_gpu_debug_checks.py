@@ -6,7 +6,8 @@ a write outside and report FP8BQ_ERR_BOUNDS through the workspace status word
 A process loads one build, so the debug build runs in a child process
 (FP8BQ_LIBRARY points the binding at it).  Every GEMM form runs on ragged
 shapes: decode split-K tiles (16, 32 and 64 tokens), the one-launch decode
-linear, 2-CTA prefill tiles with split tail tiles, grouped segments that end
+linear, 2-CTA prefill tiles with split tail tiles (one wave or several),
+grouped segments that end
 inside tiles, MXFP8, per-tensor and channelwise tiles.  No check may fire
 and every output must match the oracle."""
 import json
@@ -52,6 +53,7 @@ for M in (1, 20, 64):
 res["linear_5"] = block(5, 1000, 1040, linear=True)
 res["prefill_split_tail"] = block(300, 1000, 6016)
 res["prefill_ragged"] = block(257, 300, 512)
+res["prefill_waves"] = block(1200, 3400, 1040)
 
 counts, N, K = [300, 1, 0, 513], 384, 512
 T = sum(counts) + 2

@@ -84,6 +84,24 @@ def test_gemm_prefill_sampled(N):
     assert np.all(np.isfinite(y))
 
 
+@pytest.mark.parametrize("M,N,K", [(1200, 3400, 1040), (2048, 4864, 6016)])
+@pytest.mark.parametrize("layout", [fb.SCALE_ROW_MAJOR, fb.SCALE_COL_MAJOR])
+def test_gemm_prefill_ragged_waves(M, N, K, layout):
+    """Pair tiles over more than one wave of clusters, with ragged M (five
+    m-tiles at 1200 rows, the last one short), ragged N and K, and a split
+    tail.  Every 128 x 128 output block is sampled, with a bias, and the output
+    and the workspace sit between canary bands."""
+    qa, sa = oracle.quant_group(si.activations(M, K, base_seed=M + 1))
+    qw, sw = _weights(N, K)
+    bias = si.f32_to_bf16_bits(np.linspace(-2, 2, N).astype(np.float32))
+    y = _gemm(qa, sa, qw, sw, bias=bias, layout=layout)
+    rows, cols = sample_indices(M, N)
+    assert_covers_every_block(rows, cols, M, N)
+    ref = oracle.gemm_block_sampled(qa, sa, qw, sw, rows, cols, bias=bias)
+    check_close(y[rows, cols], ref, f"prefill ragged {M}x{N}x{K}")
+    assert np.all(np.isfinite(y))
+
+
 def test_gemm_bias():
     M, N, K = 48, 256, 384
     qa, sa = oracle.quant_group(si.activations(M, K))
