@@ -1176,7 +1176,7 @@ def run_reference(args):
 
 
 PROFILE_CASES = ("mx", "norm_group", "norm_static", "grouped_w13", "grouped_w2", "channel",
-                 "ue8m0", "quant_group", "decode_m1", "decode_m64", "static_4096")
+                 "ue8m0", "quant_group", "decode_m1", "decode_m64", "static_4096", "static_512")
 
 
 def run_profile_case(case: str, launches: int = 3):
@@ -1241,8 +1241,8 @@ def run_profile_case(case: str, launches: int = 3):
         y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
         ws = fb.new_workspace(fb.OP_GEMM, M, N, K, device=dev)
         fn = lambda: fb.fp8bq_gemm(q, sx, w, sw, y, ws)
-    elif case == "static_4096":
-        M, K, N = 4096, si.STATIC["K"], si.STATIC["N"]
+    elif case in ("static_4096", "static_512"):
+        M, K, N = int(case.split("_")[1]), si.STATIC["K"], si.STATIC["N"]
         q, w = codes(M, K), codes(N, K)
         sxs = torch.full((1,), 0.01, dtype=torch.float32, device=dev)
         sp = torch.rand(len(si.STATIC["parts"]), device=dev) * 1e-3
