@@ -1176,7 +1176,8 @@ def run_reference(args):
 
 
 PROFILE_CASES = ("mx", "norm_group", "norm_static", "grouped_w13", "grouped_w2", "channel",
-                 "ue8m0", "quant_group", "decode_m1", "decode_m64", "static_4096", "static_512")
+                 "ue8m0", "quant_group", "decode_m1", "decode_m64", "static_4096", "static_512",
+                 "decode_linear_m1", "decode_linear_m16")
 
 
 def run_profile_case(case: str, launches: int = 3):
@@ -1233,6 +1234,15 @@ def run_profile_case(case: str, launches: int = 3):
         q = torch.empty(M, K, dtype=torch.uint8, device=dev)
         sx = torch.empty(M, K // 128, dtype=torch.float32, device=dev)
         fn = lambda: fb.fp8bq_quant_act(x, q, sx)
+    elif case.startswith("decode_linear"):
+        # the one-launch decode linear: BF16 activations quantised inside the GEMM
+        M, K, N = int(case[len("decode_linear_m"):]), si.DECODE["K"], si.DECODE["N"]
+        x = torch.randn(M, K, device=dev).to(torch.bfloat16)
+        w = codes(N, K)
+        sw = torch.rand(N // 128, K // 128, device=dev) * 1e-3
+        y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        ws = fb.new_workspace(fb.OP_LINEAR, M, N, K, device=dev)
+        fn = lambda: fb.fp8bq_linear(x, w, sw, y, ws)
     elif case.startswith("decode"):
         M, K, N = int(case[len("decode_m"):]), si.DECODE["K"], si.DECODE["N"]
         q, w = codes(M, K), codes(N, K)
