@@ -66,8 +66,8 @@ ORACLE_ROWS = 8      # token rows of a large output that the CPU baseline recomp
 # digest is recorded; anything else reports null.
 NCU_TRAFFIC = {
     # profiles/block_gemm_prefill_4096x24576x6144.md (N = 24576 launch)
-    "source_sha256": "37f0c1fa633f86ff42a27a2fdfd367a646d88ad655bb1c230aa788dedd8c213d",
-    "bytes_per_launch": 188326912 + 183659520,
+    "source_sha256": "73f22334ed45986b93dc5da0d06be7dcb2f54060635c1c0c0972aca1055691a8",
+    "bytes_per_launch": 185408256 + 183538944,
 }
 
 

@@ -104,6 +104,23 @@ __device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t *p) {
   return v;
 }
 
+// the same for four consecutive 32-bit elements (16-byte aligned); each
+// element is its own relaxed access (the four may be seen in any order)
+__device__ __forceinline__ void st_relaxed_gpu_v4(uint32_t *p, uint4 v) {
+  asm volatile("st.relaxed.gpu.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x),
+               "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+__device__ __forceinline__ uint4 ld_relaxed_gpu_v4(const uint32_t *p) {
+  uint4 v;
+  asm volatile("ld.relaxed.gpu.global.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p)
+               : "memory");
+  return v;
+}
+
 // atomic add with acquire-release semantics at GPU scope; returns the old value
 __device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t *p, uint32_t v) {
   uint32_t old;
