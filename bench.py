@@ -66,7 +66,7 @@ ORACLE_ROWS = 8      # token rows of a large output that the CPU baseline recomp
 # digest is recorded; anything else reports null.
 NCU_TRAFFIC = {
     # profiles/block_gemm_prefill_4096x24576x6144.md (N = 24576 launch)
-    "source_sha256": "73f22334ed45986b93dc5da0d06be7dcb2f54060635c1c0c0972aca1055691a8",
+    "source_sha256": "1222c83da2fbd5d4acf58ae923fbc6dfb16786e907e448c50815cd60a17e3d9d",
     "bytes_per_launch": 185408256 + 183538944,
 }
 

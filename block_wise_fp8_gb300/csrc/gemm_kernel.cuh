@@ -98,7 +98,12 @@ struct Cfg {
   // are so short that one MMA instruction's issue latency, not its work, sets
   // the pace (measured 10.4 -> 9.1 us at 1 x 6144 x 6144; the 64-token tile
   // measured slower with four)
-  static constexpr int kIssuers = (MODE == kModeBlock) ? ((SWAP && BN <= 32) ? 4 : 2) : 1;
+  // The per-tensor and channel decode tiles (full-K accumulation) issue from
+  // four warps too, each into its own TMEM accumulator over its K blocks; the
+  // epilogue adds the four in a fixed order
+  static constexpr int kIssuers = (MODE == kModeBlock) ? ((SWAP && BN <= 32) ? 4 : 2)
+                                  : (SWAP && BN <= 32 && MODE != kModeMx) ? 4 : 1;
+  static constexpr int kSubAcc = (MODE != kModeBlock) ? kIssuers : 1;  // accumulators per tile buffer
   // block pair and normal tiles keep the promoted FP32 accumulators in the
   // epilogue warps' registers: warpgroup 0 (producer, the two issuers and one
   // idle warp) hands registers to the epilogue warpgroups with setmaxnreg
@@ -160,7 +165,7 @@ struct Cfg {
   static constexpr int kScWBytes = 2 * kScQuad * 4;             // 32 B
   static constexpr int kScSlotBytes = kScXBytes + 128;          // s_w at +kScXBytes
   static constexpr int kScBytes = kScSlots * kScSlotBytes;
-  static constexpr int kAccCols = ACCB * BN;     // accumulators / partials
+  static constexpr int kAccCols = ACCB * BN * kSubAcc;  // accumulators / partials
   static constexpr int kSfBase = kAccCols;
   static constexpr uint32_t kTmemCols =
       pow2_at_least(kAccCols + (MODE == kModeMx ? kSfSlots * kSfSlotCols : 0));
@@ -505,7 +510,7 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
       mbar_init(&bars->empty[s], 1);
     }
     for (int b = 0; b < ACCB; ++b) {
-      mbar_init(&bars->tfull[b], 1);
+      mbar_init(&bars->tfull[b], C::kSubAcc);  // one commit per accumulating issuer
       mbar_init(&bars->tempty[b], PAIR ? 2 * EPI_WARPS : EPI_WARPS);
     }
     for (int s = 0; s < C::kScSlots; ++s) {
@@ -724,6 +729,7 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
         bool ok = true;
         for (int u = cl_id; ok && u < units; u += cl_num, ++uit) {
           const Unit w = decode_unit<SWAP, PAIR, GROUPED>(u, num_a, shape.splits, shape.kps, KB, BN, rank, args.M, args.N, gt, shape);
+          const uint32_t it0 = it;  // this unit's first K block
           if (MODE != kModeBlock) {
             const uint32_t b = uit % ACCB, ph = (uit / ACCB) & 1u;
             if (!mbar_wait(&bars->tempty[b], ph ^ 1u, abort_flag, limit)) {
@@ -743,7 +749,7 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
               }
               d_tmem = tmem_base + b * BN;
             } else {
-              d_tmem = tmem_base + (uit % ACCB) * BN;
+              d_tmem = tmem_base + ((uit % ACCB) * C::kSubAcc + (C::kSubAcc > 1 ? me : 0u)) * BN;
             }
             const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
             // fused: the quantiser warps have seen the stage land and written its operand
@@ -772,7 +778,10 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
   #pragma unroll
             for (int k = 0; k < 4; ++k) {
               // advance 32 K-bytes inside the 128-byte swizzled row: +2 in the >>4 field
-              const uint32_t acc = (MODE == kModeBlock) ? (k > 0) : (kb > w.kb0 || k > 0);
+              // block tiles: one K block per partial; full-K tiles: accumulate
+              // after this accumulator's first K block of the unit
+              const uint32_t acc = (MODE == kModeBlock) ? (k > 0)
+                                   : ((it - it0) >= static_cast<uint32_t>(C::kSubAcc) || k > 0);
               if (MODE == kModeMx) {
                 const uint32_t sfcol = tmem_base + C::kSfBase + sfslot * C::kSfSlotCols;
                 if (PAIR)
@@ -1136,12 +1145,20 @@ __global__ void __launch_bounds__(Cfg<MODE, SWAP, BN, STAGES, EPI_WARPS, ACCB, P
             ok = false;
           } else {
             tc_fence_after();
-            const uint32_t tbase = tmem_base + lane_base + b * BN;
+            // the issuers' accumulators that received K blocks, added in order
+            const int nsub = min(C::kSubAcc, w.kb1 - w.kb0);
             uint32_t r[C::kCPT];
+            for (int i = 0; i < nsub; ++i) {
+              const uint32_t tbase = tmem_base + lane_base + (b * C::kSubAcc + i) * BN;
+              uint32_t t[C::kCPT];
 #pragma unroll
-            for (int c = 0; c < C::kCPT / C::kCW; ++c)
-              tmem_ld_chunk<C::kCW>(tbase + c * C::kCW, r + c * C::kCW);
-            tmem_ld_wait();
+              for (int c = 0; c < C::kCPT / C::kCW; ++c)
+                tmem_ld_chunk<C::kCW>(tbase + c * C::kCW, t + c * C::kCW);
+              tmem_ld_wait();
+#pragma unroll
+              for (int j = 0; j < C::kCPT; ++j)
+                r[j] = i == 0 ? t[j] : __float_as_uint(__uint_as_float(r[j]) + __uint_as_float(t[j]));
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) release_acc(b);
