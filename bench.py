@@ -66,7 +66,7 @@ ORACLE_ROWS = 8      # token rows of a large output that the CPU baseline recomp
 # digest is recorded; anything else reports null.
 NCU_TRAFFIC = {
     # profiles/block_gemm_prefill_4096x24576x6144.md (N = 24576 launch)
-    "source_sha256": "1222c83da2fbd5d4acf58ae923fbc6dfb16786e907e448c50815cd60a17e3d9d",
+    "source_sha256": "4e3efad97d785c9e2e1e7e0d8b08b272b386ea2ce87892662fa9ba02e8abb606",
     "bytes_per_launch": 185408256 + 183538944,
 }
 

@@ -99,10 +99,10 @@ struct Cfg {
   // the pace (measured 10.4 -> 9.1 us at 1 x 6144 x 6144; the 64-token tile
   // measured slower with four)
   // The per-tensor and channel decode tiles (full-K accumulation) issue from
-  // four warps too, each into its own TMEM accumulator over its K blocks; the
-  // epilogue adds the four in a fixed order
+  // four warps too (two for the 64-token tile), each into its own TMEM
+  // accumulator over its K blocks; the epilogue adds them in a fixed order
   static constexpr int kIssuers = (MODE == kModeBlock) ? ((SWAP && BN <= 32) ? 4 : 2)
-                                  : (SWAP && BN <= 32 && MODE != kModeMx) ? 4 : 1;
+                                  : (SWAP && MODE != kModeMx) ? (BN <= 32 ? 4 : 2) : 1;
   static constexpr int kSubAcc = (MODE != kModeBlock) ? kIssuers : 1;  // accumulators per tile buffer
   // block pair and normal tiles keep the promoted FP32 accumulators in the
   // epilogue warps' registers: warpgroup 0 (producer, the two issuers and one
