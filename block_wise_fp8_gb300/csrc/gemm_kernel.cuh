@@ -26,8 +26,12 @@
 // Roles (warp index):
 //   0            TMA producer: A and B tiles, 128 K per stage, 128B-swizzled.
 //   1            TMEM allocator and single-thread MMA issuer.
-//   2            (block tiles) the second MMA issuer, alternate K blocks.
-//   rest         epilogue: TMEM -> registers -> promotion -> BF16 -> global.
+//   2 ..         further MMA issuers taking alternate K blocks: block tiles
+//                (two; four for the 16- and 32-token decode tiles) and the
+//                per-tensor / channel decode tiles (four; two at 64 tokens),
+//                whose issuers each accumulate into their own TMEM columns.
+//   then         epilogue: TMEM -> registers -> promotion -> BF16 -> global.
+//   then         (fused decode linear) the activation quantiser warps.
 //
 // Tile forms:
 //   pair    (prefill) a cluster of two CTAs on two SMs computes a 256 x BN tile
