@@ -63,9 +63,11 @@ def _operands(M, N, K, seed=0):
     return qa, sa, qw, sw
 
 
+# (8, 9728, 768) and (3, 6400, 768): decode tiles whose splits hold 3 and 2 K
+# blocks, so only some of the four MMA issuers' accumulators receive any
 @pytest.mark.parametrize("M,N,K", [(16, 384, 256), (5, 200, 208), (130, 136, 224),
                                    (257, 300, 512), (520, 392, 512), (64, 640, 1024),
-                                   (1, 128, 128)])
+                                   (1, 128, 128), (8, 9728, 768), (3, 6400, 768)])
 def test_channel_gemm_small_shapes(M, N, K):
     qa, sa, qw, sw = _operands(M, N, K)
     check_close(_gemm(qa, sa, qw, sw), oracle.gemm_channel(qa, sa, qw, sw), f"channel {M}x{N}x{K}")

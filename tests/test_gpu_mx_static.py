@@ -135,7 +135,7 @@ def test_static_gemm_workload(static_weights, M):
 
 
 @pytest.mark.parametrize("M,N,K,parts", [(3, 200, 208, [72, 128]), (150, 384, 256, [100, 284]),
-                                         (64, 256, 4096, [256])])
+                                         (64, 256, 4096, [256]), (5, 9728, 768, [4864, 4864])])
 def test_static_gemm_small(M, N, K, parts):
     qw, sp = oracle.quant_weight_static(si.weights(N, K), parts)
     s_x = oracle.absmax_scale(si.calibration(32, K))
